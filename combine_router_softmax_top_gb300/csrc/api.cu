@@ -1,0 +1,451 @@
+// C ABI entry points (include/moe.h): argument checks, workspace carving and
+// the launch sequence of each call. No entry point allocates device memory.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "moe_internal.cuh"
+#include "moe_layer_ops.h"
+
+namespace moe {
+
+namespace {
+thread_local char g_err[512] = "";
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+moe_status_t check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("%s: %s", what, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+WsLayout ws_layout(const moe_layer_desc_t& d) {
+  WsLayout w;
+  const long long N = (long long)d.T * d.k;
+  const int nb = d.T > 0 ? ceil_div(d.T, kLayoutTokensPerBlock) : 1;
+  const long long chunks = (N + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk + d.E;
+  size_t o = 0;
+  w.status = o;
+  o += kStatusBytes;
+  w.logits = o;
+  o = align256(o + (size_t)d.T * d.E * sizeof(float));
+  w.hist = o;
+  o = align256(o + (size_t)nb * d.E * sizeof(int));
+  w.dz = o;
+  o = align256(o + (size_t)N * sizeof(float));
+  w.dwr_part = o;
+  o = align256(o + (size_t)chunks * d.H * sizeof(float));
+  w.total = o;
+  return w;
+}
+
+moe_status_t validate(const moe_layer_desc_t* d) {
+  if (!d) { set_error("descriptor is NULL"); return MOE_ERR_INVALID_ARG; }
+  if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->k <= 0 || d->F <= 0 || d->R <= 0) {
+    set_error("shape must have T >= 0 and H, E, k, F, R > 0 (T=%d H=%d E=%d k=%d F=%d R=%d)",
+              d->T, d->H, d->E, d->k, d->F, d->R);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (d->k > d->E) { set_error("k=%d exceeds E=%d: the k experts of a token must be distinct", d->k, d->E); return MOE_ERR_INVALID_ARG; }
+  if (d->E % d->R) { set_error("E=%d is not a multiple of R=%d", d->E, d->R); return MOE_ERR_INVALID_ARG; }
+  if (d->mode != MOE_ROUTE_SOFTMAX_TOPK && d->mode != MOE_ROUTE_FORCED_BALANCED) {
+    set_error("unknown routing mode %d", d->mode); return MOE_ERR_INVALID_ARG;
+  }
+  if (d->flags != 0) { set_error("flags must be 0"); return MOE_ERR_INVALID_ARG; }
+  if (d->H % 64 || d->F % 64) {
+    set_error("H=%d and F=%d must be multiples of 64", d->H, d->F); return MOE_ERR_UNSUPPORTED;
+  }
+  if (d->E > 256 || d->k > 32) { set_error("E <= 256 and k <= 32 are supported (E=%d k=%d)", d->E, d->k); return MOE_ERR_UNSUPPORTED; }
+  if (d->H > 16384 || d->F > 16384) { set_error("H, F <= 16384 are supported"); return MOE_ERR_UNSUPPORTED; }
+  if ((long long)d->T * d->k >= (1ll << 31) || (long long)d->T * d->H >= (1ll << 40)) {
+    set_error("T*k must stay below 2^31"); return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+#define MOE_CHECK(x)                 \
+  do {                               \
+    moe_status_t _s = (x);           \
+    if (_s != MOE_OK) return _s;     \
+  } while (0)
+
+#define MOE_PTR(p)                                                             \
+  do {                                                                         \
+    if (!(p)) { set_error("%s is NULL", #p); return MOE_ERR_INVALID_ARG; }     \
+    if (!aligned16(p)) { set_error("%s is not 16-byte aligned", #p); return MOE_ERR_INVALID_ARG; } \
+  } while (0)
+
+#define MOE_PTR_OPT(p)                                                         \
+  do {                                                                         \
+    if ((p) && !aligned16(p)) { set_error("%s is not 16-byte aligned", #p); return MOE_ERR_INVALID_ARG; } \
+  } while (0)
+
+static moe_status_t check_ws(const moe_layer_desc_t& d, void* ws, size_t ws_bytes) {
+  MOE_PTR(ws);
+  if (ws_bytes < ws_layout(d).total) {
+    set_error("workspace of %zu bytes is smaller than moe_workspace_size() = %zu", ws_bytes,
+              ws_layout(d).total);
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+static int* status_of(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws)); }
+template <typename T>
+static T* ws_at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+// ------------------------------------------------------------------ internal ops
+moe_status_t op_route(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r, const float* bias,
+                      float* logits, int32_t* idx, float* gates, void* ws, cudaStream_t st) {
+  float* z = logits ? logits : ws_at<float>(ws, ws_layout(d).logits);
+  return launch_route(d, x, w_r, bias, z, idx, gates, status_of(ws), st);
+}
+
+moe_status_t op_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_t* cnt, int32_t* off,
+                       int32_t* slot, int32_t* row_src, int32_t* cnt_re, int32_t* rank_off,
+                       void* ws, cudaStream_t st) {
+  return launch_layout(d, idx, cnt, off, slot, row_src, cnt_re, rank_off,
+                       ws_at<int>(ws, ws_layout(d).hist), status_of(ws), st);
+}
+
+moe_status_t op_ffn_fwd(const moe_layer_desc_t& d, const bf16* x_perm, const int32_t* off,
+                        const bf16* w1, const bf16* w2, bf16* a, bf16* h, bf16* o, void* ws,
+                        int max_ctas, cudaStream_t st) {
+  GemmArgs g = {};
+  g.mode = GEMM_FC1_FWD;
+  g.A = x_perm;
+  g.B = w1;
+  g.off = off;
+  g.out0 = a;
+  g.out1 = h;
+  g.status = status_of(ws);
+  g.max_ctas = max_ctas;
+  MOE_CHECK(launch_grouped_gemm(d, g, st));
+  g.mode = GEMM_FC2_FWD;
+  g.A = h;
+  g.B = w2;
+  g.out0 = o;
+  g.out1 = nullptr;
+  return launch_grouped_gemm(d, g, st);
+}
+
+moe_status_t op_dgrad(const moe_layer_desc_t& d, const bf16* d_o, const bf16* a,
+                      const int32_t* off, const bf16* w1, const bf16* w2, bf16* da,
+                      bf16* dx_perm, void* ws, int max_ctas, cudaStream_t st) {
+  GemmArgs g = {};
+  g.mode = GEMM_FC2_DGRAD;
+  g.A = d_o;
+  g.B = w2;
+  g.off = off;
+  g.out0 = da;
+  g.aux = a;
+  g.status = status_of(ws);
+  g.max_ctas = max_ctas;
+  MOE_CHECK(launch_grouped_gemm(d, g, st));
+  g.mode = GEMM_FC1_DGRAD;
+  g.A = da;
+  g.B = w1;
+  g.out0 = dx_perm;
+  g.aux = nullptr;
+  return launch_grouped_gemm(d, g, st);
+}
+
+moe_status_t op_wgrad(const moe_layer_desc_t& d, const bf16* x_perm, const bf16* h,
+                      const bf16* d_o, const bf16* da, const int32_t* off, bf16* dw1, bf16* dw2,
+                      void* ws, int max_ctas, cudaStream_t st) {
+  GemmArgs g = {};
+  g.mode = GEMM_WGRAD_W1;
+  g.A = da;
+  g.B = x_perm;
+  g.off = off;
+  g.out0 = dw1;
+  g.status = status_of(ws);
+  g.max_ctas = max_ctas;
+  MOE_CHECK(launch_grouped_gemm(d, g, st));
+  g.mode = GEMM_WGRAD_W2;
+  g.A = d_o;
+  g.B = h;
+  g.out0 = nullptr;
+  g.out1 = dw2;
+  return launch_grouped_gemm(d, g, st);
+}
+
+moe_status_t op_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,
+                          const int32_t* idx, const bf16* x, const bf16* w_r,
+                          const int32_t* row_src, const int32_t* off, const float* dx32, bf16* dx,
+                          float* dw_r, void* ws, cudaStream_t st) {
+  const WsLayout w = ws_layout(d);
+  return launch_route_bwd(d, dgates, gates, idx, x, w_r, row_src, off, dx32, dx, dw_r,
+                          ws_at<float>(ws, w.dz), ws_at<float>(ws, w.dwr_part), status_of(ws), st);
+}
+
+moe_status_t op_dispatch(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st) {
+  const bf16* x = reinterpret_cast<const bf16*>(b->x);
+  MOE_CHECK(op_route(d, x, reinterpret_cast<const bf16*>(b->w_r), b->bias, b->logits, b->idx,
+                     b->gates, b->ws, st));
+  MOE_CHECK(op_layout(d, b->idx, b->cnt, b->off, b->slot, b->row_src, b->cnt_re, b->rank_off,
+                      b->ws, st));
+  return launch_permute(d, x, b->row_src, reinterpret_cast<bf16*>(b->x_perm), st);
+}
+
+moe_status_t op_ffn_fwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
+                           cudaStream_t st) {
+  return op_ffn_fwd(d, reinterpret_cast<const bf16*>(b->x_perm), b->off,
+                    reinterpret_cast<const bf16*>(b->w1), reinterpret_cast<const bf16*>(b->w2),
+                    reinterpret_cast<bf16*>(b->a), reinterpret_cast<bf16*>(b->h),
+                    reinterpret_cast<bf16*>(b->o), b->ws, max_ctas, st);
+}
+
+moe_status_t op_combine_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st) {
+  return launch_combine(d, reinterpret_cast<const bf16*>(b->o), b->slot, b->gates,
+                        reinterpret_cast<bf16*>(b->y), st);
+}
+
+moe_status_t op_combine_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b,
+                               cudaStream_t st) {
+  return launch_combine_bwd(d, reinterpret_cast<const bf16*>(b->dy),
+                            reinterpret_cast<const bf16*>(b->o), b->slot, b->gates,
+                            reinterpret_cast<bf16*>(b->d_o), b->dgates, st);
+}
+
+moe_status_t op_dgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
+                         cudaStream_t st) {
+  return op_dgrad(d, reinterpret_cast<const bf16*>(b->d_o), reinterpret_cast<const bf16*>(b->a),
+                  b->off, reinterpret_cast<const bf16*>(b->w1),
+                  reinterpret_cast<const bf16*>(b->w2), reinterpret_cast<bf16*>(b->da),
+                  reinterpret_cast<bf16*>(b->dx_perm), b->ws, max_ctas, st);
+}
+
+moe_status_t op_dispatch_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b,
+                                cudaStream_t st) {
+  MOE_CHECK(launch_permute_bwd(d, reinterpret_cast<const bf16*>(b->dx_perm), b->slot, b->dx32, st));
+  return op_route_bwd(d, b->dgates, b->gates, b->idx, reinterpret_cast<const bf16*>(b->x),
+                      reinterpret_cast<const bf16*>(b->w_r), b->row_src, b->off, b->dx32,
+                      reinterpret_cast<bf16*>(b->dx), b->dw_r, b->ws, st);
+}
+
+moe_status_t op_wgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
+                         cudaStream_t st) {
+  return op_wgrad(d, reinterpret_cast<const bf16*>(b->x_perm), reinterpret_cast<const bf16*>(b->h),
+                  reinterpret_cast<const bf16*>(b->d_o), reinterpret_cast<const bf16*>(b->da),
+                  b->off, reinterpret_cast<bf16*>(b->dw1), reinterpret_cast<bf16*>(b->dw2), b->ws,
+                  max_ctas, st);
+}
+
+moe_status_t check_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, bool bwd) {
+  if (!b) { set_error("buffer struct is NULL"); return MOE_ERR_INVALID_ARG; }
+  MOE_PTR(b->x); MOE_PTR(b->w_r); MOE_PTR(b->w1); MOE_PTR(b->w2); MOE_PTR_OPT(b->bias);
+  MOE_PTR_OPT(b->logits); MOE_PTR(b->idx); MOE_PTR(b->gates); MOE_PTR(b->cnt); MOE_PTR(b->off);
+  MOE_PTR(b->slot); MOE_PTR(b->row_src); MOE_PTR(b->cnt_re); MOE_PTR(b->rank_off);
+  MOE_PTR(b->x_perm); MOE_PTR(b->a); MOE_PTR(b->h); MOE_PTR(b->o); MOE_PTR(b->y);
+  if (bwd) {
+    MOE_PTR(b->dy); MOE_PTR(b->d_o); MOE_PTR(b->dgates); MOE_PTR(b->da); MOE_PTR(b->dx_perm);
+    MOE_PTR(b->dx32); MOE_PTR(b->dx); MOE_PTR(b->dw_r); MOE_PTR(b->dw1); MOE_PTR(b->dw2);
+  }
+  return check_ws(d, b->ws, b->ws_bytes);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define S(st) static_cast<cudaStream_t>(st)
+#define BF(p) reinterpret_cast<const bf16*>(p)
+#define BFW(p) reinterpret_cast<bf16*>(p)
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return 1; }
+
+const char* moe_last_error(void) { return g_err; }
+
+moe_status_t moe_layer_desc_validate(const moe_layer_desc_t* d) {
+  moe_status_t s = validate(d);
+  if (s == MOE_OK) g_err[0] = 0;
+  return s;
+}
+
+size_t moe_workspace_size(const moe_layer_desc_t* d) {
+  if (validate(d) != MOE_OK) return 0;
+  return ws_layout(*d).total;
+}
+
+moe_status_t moe_device_status(const moe_layer_desc_t* d, void* ws, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(ws);
+  int h[ST_NUM] = {0};
+  cudaError_t e = cudaStreamSynchronize(S(stream));
+  if (e == cudaSuccess) e = cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(ws, 0, sizeof(h));
+  if (e != cudaSuccess) {
+    set_error("moe_device_status: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  if (h[ST_TIMEOUT]) {
+    set_error("a pipeline wait ran out of time (site %d)", h[ST_TIMEOUT]);
+    return MOE_ERR_TIMEOUT;
+  }
+  if (h[ST_BAD_INDEX]) {
+    set_error("%d out-of-range expert or row indices were skipped", h[ST_BAD_INDEX]);
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_layer_desc_t* d, const moe_bf16* x, const moe_bf16* w_r,
+                       const float* bias, float* logits, int32_t* idx, float* gates, void* ws,
+                       size_t ws_bytes, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(x); MOE_PTR(w_r); MOE_PTR_OPT(bias); MOE_PTR_OPT(logits); MOE_PTR(idx); MOE_PTR(gates);
+  MOE_CHECK(check_ws(*d, ws, ws_bytes));
+  return op_route(*d, BF(x), BF(w_r), bias, logits, idx, gates, ws, S(stream));
+}
+
+moe_status_t moe_dispatch_layout(const moe_layer_desc_t* d, const int32_t* idx, int32_t* cnt,
+                                 int32_t* off, int32_t* slot, int32_t* row_src, int32_t* cnt_re,
+                                 int32_t* rank_off, void* ws, size_t ws_bytes, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(idx); MOE_PTR(cnt); MOE_PTR(off); MOE_PTR(slot); MOE_PTR(row_src); MOE_PTR(cnt_re);
+  MOE_PTR(rank_off);
+  MOE_CHECK(check_ws(*d, ws, ws_bytes));
+  return op_layout(*d, idx, cnt, off, slot, row_src, cnt_re, rank_off, ws, S(stream));
+}
+
+moe_status_t moe_permute(const moe_layer_desc_t* d, const moe_bf16* x, const int32_t* row_src,
+                         moe_bf16* x_perm, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(x); MOE_PTR(row_src); MOE_PTR(x_perm);
+  return launch_permute(*d, BF(x), row_src, BFW(x_perm), S(stream));
+}
+
+moe_status_t moe_expert_ffn_fwd(const moe_layer_desc_t* d, const moe_bf16* x_perm,
+                                const int32_t* off, const moe_bf16* w1, const moe_bf16* w2,
+                                moe_bf16* a, moe_bf16* h, moe_bf16* o, void* ws, size_t ws_bytes,
+                                void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(x_perm); MOE_PTR(off); MOE_PTR(w1); MOE_PTR(w2); MOE_PTR(a); MOE_PTR(h); MOE_PTR(o);
+  MOE_CHECK(check_ws(*d, ws, ws_bytes));
+  return op_ffn_fwd(*d, BF(x_perm), off, BF(w1), BF(w2), BFW(a), BFW(h), BFW(o), ws, 0, S(stream));
+}
+
+moe_status_t moe_combine(const moe_layer_desc_t* d, const moe_bf16* o, const int32_t* slot,
+                         const float* gates, moe_bf16* y, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(o); MOE_PTR(slot); MOE_PTR(gates); MOE_PTR(y);
+  return launch_combine(*d, BF(o), slot, gates, BFW(y), S(stream));
+}
+
+moe_status_t moe_combine_bwd(const moe_layer_desc_t* d, const moe_bf16* dy, const moe_bf16* o,
+                             const int32_t* slot, const float* gates, moe_bf16* d_o,
+                             float* dgates, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(dy); MOE_PTR(o); MOE_PTR(slot); MOE_PTR(gates); MOE_PTR(d_o); MOE_PTR(dgates);
+  return launch_combine_bwd(*d, BF(dy), BF(o), slot, gates, BFW(d_o), dgates, S(stream));
+}
+
+moe_status_t moe_expert_ffn_bwd_dgrad(const moe_layer_desc_t* d, const moe_bf16* d_o,
+                                      const moe_bf16* a, const int32_t* off, const moe_bf16* w1,
+                                      const moe_bf16* w2, moe_bf16* da, moe_bf16* dx_perm,
+                                      void* ws, size_t ws_bytes, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(d_o); MOE_PTR(a); MOE_PTR(off); MOE_PTR(w1); MOE_PTR(w2); MOE_PTR(da); MOE_PTR(dx_perm);
+  MOE_CHECK(check_ws(*d, ws, ws_bytes));
+  return op_dgrad(*d, BF(d_o), BF(a), off, BF(w1), BF(w2), BFW(da), BFW(dx_perm), ws, 0,
+                  S(stream));
+}
+
+moe_status_t moe_expert_ffn_bwd_wgrad(const moe_layer_desc_t* d, const moe_bf16* x_perm,
+                                      const moe_bf16* h, const moe_bf16* d_o, const moe_bf16* da,
+                                      const int32_t* off, moe_bf16* dw1, moe_bf16* dw2, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(x_perm); MOE_PTR(h); MOE_PTR(d_o); MOE_PTR(da); MOE_PTR(off); MOE_PTR(dw1); MOE_PTR(dw2);
+  MOE_CHECK(check_ws(*d, ws, ws_bytes));
+  return op_wgrad(*d, BF(x_perm), BF(h), BF(d_o), BF(da), off, BFW(dw1), BFW(dw2), ws, 0,
+                  S(stream));
+}
+
+moe_status_t moe_permute_bwd(const moe_layer_desc_t* d, const moe_bf16* dx_perm,
+                             const int32_t* slot, float* dx32, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(dx_perm); MOE_PTR(slot); MOE_PTR(dx32);
+  return launch_permute_bwd(*d, BF(dx_perm), slot, dx32, S(stream));
+}
+
+moe_status_t moe_route_bwd(const moe_layer_desc_t* d, const float* dgates, const float* gates,
+                           const int32_t* idx, const moe_bf16* x, const moe_bf16* w_r,
+                           const int32_t* row_src, const int32_t* off, const float* dx32,
+                           moe_bf16* dx, float* dw_r, void* ws, size_t ws_bytes, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(dgates); MOE_PTR(gates); MOE_PTR(idx); MOE_PTR(x); MOE_PTR(w_r); MOE_PTR(row_src);
+  MOE_PTR(off); MOE_PTR(dx32); MOE_PTR(dx); MOE_PTR(dw_r);
+  MOE_CHECK(check_ws(*d, ws, ws_bytes));
+  return op_route_bwd(*d, dgates, gates, idx, BF(x), BF(w_r), row_src, off, dx32, BFW(dx), dw_r,
+                      ws, S(stream));
+}
+
+moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_CHECK(check_mb(*d, b, false));
+  MOE_CHECK(op_dispatch(*d, b, S(stream)));
+  MOE_CHECK(op_ffn_fwd_mb(*d, b, 0, S(stream)));
+  return op_combine_mb(*d, b, S(stream));
+}
+
+moe_status_t moe_layer_backward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
+                                int32_t run_wgrad, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_CHECK(check_mb(*d, b, true));
+  MOE_CHECK(op_combine_bwd_mb(*d, b, S(stream)));
+  MOE_CHECK(op_dgrad_mb(*d, b, 0, S(stream)));
+  MOE_CHECK(op_dispatch_bwd_mb(*d, b, S(stream)));
+  if (run_wgrad) MOE_CHECK(op_wgrad_mb(*d, b, 0, S(stream)));
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
+                                 const moe_bf16* host_x, const moe_bf16* host_dy, moe_bf16* host_y,
+                                 moe_bf16* host_dx, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_CHECK(check_mb(*d, b, true));
+  if (!host_x || !host_dy || !host_y || !host_dx) {
+    set_error("host buffers must not be NULL");
+    return MOE_ERR_INVALID_ARG;
+  }
+  const size_t bytes = (size_t)d->T * d->H * sizeof(moe_bf16);
+  cudaStream_t st = S(stream);
+  cudaError_t e = cudaMemcpyAsync(const_cast<moe_bf16*>(b->x), host_x, bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<moe_bf16*>(b->dy), host_dy, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) { set_error("host to device copy: %s", cudaGetErrorString(e)); return MOE_ERR_CUDA; }
+  MOE_CHECK(moe_layer_forward(d, b, stream));
+  MOE_CHECK(moe_layer_backward(d, b, 1, stream));
+  e = cudaMemcpyAsync(host_y, b->y, bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(host_dx, b->dx, bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) { set_error("device to host copy: %s", cudaGetErrorString(e)); return MOE_ERR_CUDA; }
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------- workspace map
+// The workspace starts with status words; the rest is carved per call kind.
+enum StatusWord {
+  ST_BAD_INDEX = 0,   // count of out-of-range indices a kernel skipped
+  ST_TIMEOUT = 1,     // a bounded pipeline wait gave up (nonzero = where)
+  ST_NUM = 8
+};
+constexpr size_t kStatusBytes = 256;
+constexpr int kLayoutTokensPerBlock = 256;
+constexpr int kRouteBwdRowsPerChunk = 64;
+
+struct WsLayout {
+  size_t status, logits, hist, dz, dwr_part, total;
+};
+WsLayout ws_layout(const moe_layer_desc_t& d);
+
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// ---------------------------------------------------------------- errors
+void set_error(const char* fmt, ...);
+moe_status_t check_launch(const char* what);
+
+int device_sm_count();
+
+// ---------------------------------------------------------------- launchers
+moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
+                          const float* bias, float* logits, int32_t* idx, float* gates,
+                          int* status, cudaStream_t st);
+moe_status_t launch_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_t* cnt,
+                           int32_t* off, int32_t* slot, int32_t* row_src, int32_t* cnt_re,
+                           int32_t* rank_off, int* hist, int* status, cudaStream_t st);
+moe_status_t launch_permute(const moe_layer_desc_t& d, const bf16* x, const int32_t* row_src,
+                            bf16* x_perm, cudaStream_t st);
+moe_status_t launch_combine(const moe_layer_desc_t& d, const bf16* o, const int32_t* slot,
+                            const float* gates, bf16* y, cudaStream_t st);
+moe_status_t launch_combine_bwd(const moe_layer_desc_t& d, const bf16* dy, const bf16* o,
+                                const int32_t* slot, const float* gates, bf16* d_o,
+                                float* dgates, cudaStream_t st);
+moe_status_t launch_permute_bwd(const moe_layer_desc_t& d, const bf16* dx_perm,
+                                const int32_t* slot, float* dx32, cudaStream_t st);
+moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,
+                              const int32_t* idx, const bf16* x, const bf16* w_r,
+                              const int32_t* row_src, const int32_t* off, const float* dx32,
+                              bf16* dx, float* dw_r, float* dz, float* dwr_part, int* status,
+                              cudaStream_t st);
+
+enum GemmMode {
+  GEMM_FC1_FWD = 0,   // a, h = SwiGLU(x_perm @ W1^T)
+  GEMM_FC2_FWD = 1,   // o = h @ W2^T
+  GEMM_FC2_DGRAD = 2, // da = SwiGLU'(d_o @ W2, a)
+  GEMM_FC1_DGRAD = 3, // dx_perm = da @ W1
+  GEMM_WGRAD_W1 = 4,  // dW1_e = da_e^T @ x_perm_e
+  GEMM_WGRAD_W2 = 5   // dW2_e = d_o_e^T @ h_e
+};
+
+struct GemmArgs {
+  int mode;
+  const bf16* A;      // activation operand
+  const bf16* B;      // weight (fwd/dgrad) or second activation (wgrad)
+  const int32_t* off; // [E+1]
+  bf16* out0;
+  bf16* out1;
+  const bf16* aux;
+  int* status;
+  int max_ctas;       // 0 = all SMs
+};
+moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, cudaStream_t st);
+
+}  // namespace moe

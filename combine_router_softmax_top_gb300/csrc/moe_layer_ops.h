@@ -1,0 +1,27 @@
+// Per-phase operations on one micro-batch's buffers, shared by the C ABI's
+// whole-layer calls and the two-stream scheduler.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+moe_status_t validate(const moe_layer_desc_t* d);
+moe_status_t check_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, bool bwd);
+
+// route + dispatch layout + permute
+moe_status_t op_dispatch(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st);
+moe_status_t op_ffn_fwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
+                           cudaStream_t st);
+moe_status_t op_combine_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st);
+moe_status_t op_combine_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b,
+                               cudaStream_t st);
+moe_status_t op_dgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
+                         cudaStream_t st);
+// permute backward + router backward
+moe_status_t op_dispatch_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b,
+                                cudaStream_t st);
+moe_status_t op_wgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
+                         cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,291 @@
+// Permute (dispatch: write the EP send buffer), combine (receive + unpermute
+// with the gate-weighted sum) and their backward passes. These are the
+// "dispatch" and "combine" phases of the EP-overlap note ("1. MoE EP Overlap",
+// section "how the 8 fwd/bwd operations are split out") with the all-to-all
+// itself replaced by writing the rank-major, expert-contiguous buffer.
+//
+// All four are HBM-bound row gathers. A thread moves one 16-byte chunk
+// (8 bf16) per row at a time; a token's k source rows are loaded before any is
+// used so k independent 16-byte loads are in flight per thread. The token
+// input x (T*H*2 bytes, e.g. 16.8 MB) stays resident in the 129 MB L2, so the
+// k-fold re-reads of permute come from L2 and DRAM sees roughly one read of x
+// plus one write of x_perm.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    f[2 * q] = __uint_as_float(w[q] << 16);
+    f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 out;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);
+    o[q] = *reinterpret_cast<uint32_t*>(&b2);
+  }
+  return out;
+}
+
+// x_perm[s] = x[row_src[s] / k]; one warp per destination row, grid-stride.
+__global__ void __launch_bounds__(256) permute_kernel(const bf16* __restrict__ x,
+                                                      const int32_t* __restrict__ row_src,
+                                                      bf16* __restrict__ x_perm, int T, int H,
+                                                      int k, long long N) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int cpr = H / 8;
+  for (long long s = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); s < N;
+       s += warps) {
+    const int src = row_src[s];
+    const int t = src / k;
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + s * H);
+    if (src < 0 || t >= T) {
+      for (int c = lane; c < cpr; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* srcp = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    int c = lane;
+    for (; c + 96 < cpr; c += 128) {
+      const uint4 v0 = __ldg(srcp + c), v1 = __ldg(srcp + c + 32), v2 = __ldg(srcp + c + 64),
+                  v3 = __ldg(srcp + c + 96);
+      __stcs(dst + c, v0);
+      __stcs(dst + c + 32, v1);
+      __stcs(dst + c + 64, v2);
+      __stcs(dst + c + 96, v3);
+    }
+    for (; c < cpr; c += 32) __stcs(dst + c, __ldg(srcp + c));
+  }
+}
+
+// Threads of one token row: tpr threads (a power of two >= H/8, at most 256),
+// 256/tpr tokens per block; thread `sub` handles chunks sub, sub+tpr, ...
+struct RowMap {
+  int t, sub, tpr;
+};
+__device__ __forceinline__ RowMap row_map(int tpr) {
+  RowMap m;
+  m.tpr = tpr;
+  m.t = blockIdx.x * (blockDim.x / tpr) + threadIdx.x / tpr;
+  m.sub = threadIdx.x % tpr;
+  return m;
+}
+
+constexpr int kMaxKBatch = 8;
+
+// y[t] = bf16(sum_j g[t,j] * o[slot[t,j]]), fp32 in ascending j.
+__global__ void __launch_bounds__(256) combine_kernel(const bf16* __restrict__ o,
+                                                      const int32_t* __restrict__ slot,
+                                                      const float* __restrict__ gates,
+                                                      bf16* __restrict__ y, int T, int H, int k,
+                                                      long long N, int tpr) {
+  const RowMap m = row_map(tpr);
+  if (m.t >= T) return;
+  const int cpr = H / 8;
+  for (int c = m.sub; c < cpr; c += tpr) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j0 = 0; j0 < k; j0 += kMaxKBatch) {
+      const int nj = min(kMaxKBatch, k - j0);
+      uint4 v[kMaxKBatch];
+      float g[kMaxKBatch];
+#pragma unroll
+      for (int u = 0; u < kMaxKBatch; ++u) {
+        v[u] = make_uint4(0, 0, 0, 0);
+        g[u] = 0.f;
+        if (u < nj) {
+          const int s = slot[(size_t)m.t * k + j0 + u];
+          g[u] = gates[(size_t)m.t * k + j0 + u];
+          if (s >= 0 && s < N) v[u] = __ldcs(reinterpret_cast<const uint4*>(o + (size_t)s * H) + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMaxKBatch; ++u) {
+        if (u < nj) {
+          float f[8];
+          unpack8(v[u], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(g[u], f[q], acc[q]);
+        }
+      }
+    }
+    reinterpret_cast<uint4*>(y + (size_t)m.t * H)[c] = pack8(acc);
+  }
+}
+
+// d_o[slot[t,j]] = bf16(g[t,j] * dy[t]); dgates[t,j] = <dy[t], o[slot[t,j]]>.
+// The dot product is reduced over the token's threads in a fixed tree order.
+template <int KMAX>
+__global__ void __launch_bounds__(256) combine_bwd_kernel(
+    const bf16* __restrict__ dy, const bf16* __restrict__ o, const int32_t* __restrict__ slot,
+    const float* __restrict__ gates, bf16* __restrict__ d_o, float* __restrict__ dgates, int T,
+    int H, int k, long long N, int tpr) {
+  __shared__ float s_part[8][KMAX];
+  const RowMap m = row_map(tpr);
+  const bool active = m.t < T;
+  const int cpr = H / 8;
+  float dot[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) dot[j] = 0.f;
+  if (active) {
+    for (int c = m.sub; c < cpr; c += tpr) {
+      float fy[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(dy + (size_t)m.t * H) + c), fy);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          const int s = slot[(size_t)m.t * k + j];
+          const float g = gates[(size_t)m.t * k + j];
+          if (s >= 0 && s < N) {
+            float fo[8];
+            unpack8(__ldcs(reinterpret_cast<const uint4*>(o + (size_t)s * H) + c), fo);
+            float prod[8];
+            float d = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              d = fmaf(fy[q], fo[q], d);
+              prod[q] = g * fy[q];
+            }
+            dot[j] += d;
+            __stcs(reinterpret_cast<uint4*>(d_o + (size_t)s * H) + c, pack8(prod));
+          }
+        }
+      }
+    }
+  }
+  // reduce dot[] over the tpr threads of the token
+  const int width = tpr < 32 ? tpr : 32;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+#pragma unroll
+    for (int o2 = 16; o2; o2 >>= 1)
+      if (o2 < width) dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], o2, width);
+  }
+  if (tpr <= 32) {
+    if (active && m.sub == 0) {
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) dgates[(size_t)m.t * k + j] = dot[j];
+    }
+    return;
+  }
+  // tpr > 32: the token's tpr/32 warps combine their sums in warp order
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) s_part[warp][j] = dot[j];
+  }
+  __syncthreads();
+  const int wbase = (threadIdx.x / tpr) * (tpr / 32);
+  if (active && m.sub < k) {
+    float sum = 0.f;
+    for (int w = 0; w < tpr / 32; ++w) sum += s_part[wbase + w][m.sub];
+    dgates[(size_t)m.t * k + m.sub] = sum;
+  }
+}
+
+// dx32[t] = sum_j dx_perm[slot[t,j]] in fp32, ascending j.
+__global__ void __launch_bounds__(256) permute_bwd_kernel(const bf16* __restrict__ dx_perm,
+                                                          const int32_t* __restrict__ slot,
+                                                          float* __restrict__ dx32, int T, int H,
+                                                          int k, long long N, int tpr) {
+  const RowMap m = row_map(tpr);
+  if (m.t >= T) return;
+  const int cpr = H / 8;
+  for (int c = m.sub; c < cpr; c += tpr) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j0 = 0; j0 < k; j0 += kMaxKBatch) {
+      const int nj = min(kMaxKBatch, k - j0);
+      uint4 v[kMaxKBatch];
+#pragma unroll
+      for (int u = 0; u < kMaxKBatch; ++u) {
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (u < nj) {
+          const int s = slot[(size_t)m.t * k + j0 + u];
+          if (s >= 0 && s < N) v[u] = __ldcs(reinterpret_cast<const uint4*>(dx_perm + (size_t)s * H) + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMaxKBatch; ++u) {
+        if (u < nj) {
+          float f[8];
+          unpack8(v[u], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] += f[q];
+        }
+      }
+    }
+    float4* dst = reinterpret_cast<float4*>(dx32 + (size_t)m.t * H + c * 8);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+int threads_per_row(int H) {
+  const int cpr = H / 8;
+  int tpr = 1;
+  while (tpr < cpr && tpr < 256) tpr <<= 1;
+  return tpr;
+}
+
+}  // namespace
+
+moe_status_t launch_permute(const moe_layer_desc_t& d, const bf16* x, const int32_t* row_src,
+                            bf16* x_perm, cudaStream_t st) {
+  const long long N = (long long)d.T * d.k;
+  if (N == 0) return MOE_OK;
+  const int warps_per_block = 8;
+  long long blocks = (N + warps_per_block - 1) / warps_per_block;
+  const long long cap = (long long)device_sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  permute_kernel<<<(int)blocks, 256, 0, st>>>(x, row_src, x_perm, d.T, d.H, d.k, N);
+  return check_launch("permute_kernel");
+}
+
+moe_status_t launch_combine(const moe_layer_desc_t& d, const bf16* o, const int32_t* slot,
+                            const float* gates, bf16* y, cudaStream_t st) {
+  if (d.T == 0) return MOE_OK;
+  const int tpr = threads_per_row(d.H);
+  combine_kernel<<<ceil_div(d.T, 256 / tpr), 256, 0, st>>>(o, slot, gates, y, d.T, d.H, d.k,
+                                                           (long long)d.T * d.k, tpr);
+  return check_launch("combine_kernel");
+}
+
+moe_status_t launch_combine_bwd(const moe_layer_desc_t& d, const bf16* dy, const bf16* o,
+                                const int32_t* slot, const float* gates, bf16* d_o,
+                                float* dgates, cudaStream_t st) {
+  if (d.T == 0) return MOE_OK;
+  const int tpr = threads_per_row(d.H);
+  const dim3 grid(ceil_div(d.T, 256 / tpr));
+  const long long N = (long long)d.T * d.k;
+  if (d.k <= 2)
+    combine_bwd_kernel<2><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+  else if (d.k <= 4)
+    combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+  else if (d.k <= 8)
+    combine_bwd_kernel<8><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+  else if (d.k <= 16)
+    combine_bwd_kernel<16><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+  else
+    combine_bwd_kernel<32><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+  return check_launch("combine_bwd_kernel");
+}
+
+moe_status_t launch_permute_bwd(const moe_layer_desc_t& d, const bf16* dx_perm,
+                                const int32_t* slot, float* dx32, cudaStream_t st) {
+  if (d.T == 0) return MOE_OK;
+  const int tpr = threads_per_row(d.H);
+  permute_bwd_kernel<<<ceil_div(d.T, 256 / tpr), 256, 0, st>>>(dx_perm, slot, dx32, d.T, d.H,
+                                                               d.k, (long long)d.T * d.k, tpr);
+  return check_launch("permute_bwd_kernel");
+}
+
+}  // namespace moe

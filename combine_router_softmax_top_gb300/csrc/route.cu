@@ -1,0 +1,389 @@
+// Router: fp32 logits in a fixed summation order, softmax over all experts,
+// top-k by logit (ties to the lower expert), renormalised gates; and the
+// router's backward (gate softmax Jacobian, dx and dW_r).
+//
+// The router is the "moe_router" scope that precedes dispatch in the EP-overlap
+// pages (skill card, "HybridEP production benchmark": CUDA-graph scopes
+// moe_router + moe_preprocess). Its arithmetic is the layer definition in moe.h.
+#include <float.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouteTok = 32;   // tokens per CTA (one per lane)
+constexpr int kRouteEpw = 8;    // experts per warp
+constexpr int kRouteHc = 64;    // hidden elements per shared-memory chunk
+constexpr int kRouteXPitch = kRouteHc + 4;  // floats; 272-byte rows keep LDS.128 conflict-free
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// z[t, e] for a tile of 32 tokens x (warps * 8) experts. Lane <-> token,
+// warp <-> 8 experts. Every accumulator runs over h = 0..H-1 in ascending order
+// with one fmaf per step; since a bf16*bf16 product is exact in fp32, each step
+// is a single fp32 rounding of (acc + x*w), the order both sides of the parity
+// check use.
+__global__ void __launch_bounds__(256) route_logits_kernel(const bf16* __restrict__ x,
+                                                           const bf16* __restrict__ w_r,
+                                                           const float* __restrict__ bias,
+                                                           float* __restrict__ z, int T, int H,
+                                                           int E) {
+  extern __shared__ float4 smem_f4[];
+  float* sm = reinterpret_cast<float*>(smem_f4);
+  const int nwarps = blockDim.x >> 5;
+  const int eb = nwarps * kRouteEpw;  // experts in this CTA
+  float* xs = sm;                                   // [32][kRouteXPitch]
+  float* ws = sm + kRouteTok * kRouteXPitch;        // [eb][kRouteHc]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kRouteTok;
+  const int e0 = blockIdx.y * eb;
+
+  float acc[kRouteEpw];
+#pragma unroll
+  for (int i = 0; i < kRouteEpw; ++i) acc[i] = 0.f;
+
+  const uint16_t* xb = reinterpret_cast<const uint16_t*>(x);
+  const uint16_t* wb = reinterpret_cast<const uint16_t*>(w_r);
+  for (int h0 = 0; h0 < H; h0 += kRouteHc) {
+    // stage x[t0..t0+31][h0..h0+63] and w_r[e0..e0+eb-1][h0..h0+63] as fp32
+    for (int i = threadIdx.x; i < kRouteTok * (kRouteHc / 8); i += blockDim.x) {
+      const int r = i / (kRouteHc / 8), c = (i % (kRouteHc / 8)) * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t0 + r < T) v = __ldg(reinterpret_cast<const uint4*>(xb + (size_t)(t0 + r) * H + h0 + c));
+      float* dst = xs + r * kRouteXPitch + c;
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dst[2 * q] = bf16_bits_to_f32(w[q] & 0xFFFFu);
+        dst[2 * q + 1] = bf16_bits_to_f32(w[q] >> 16);
+      }
+    }
+    for (int i = threadIdx.x; i < eb * (kRouteHc / 8); i += blockDim.x) {
+      const int r = i / (kRouteHc / 8), c = (i % (kRouteHc / 8)) * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (e0 + r < E) v = __ldg(reinterpret_cast<const uint4*>(wb + (size_t)(e0 + r) * H + h0 + c));
+      float* dst = ws + r * kRouteHc + c;
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dst[2 * q] = bf16_bits_to_f32(w[q] & 0xFFFFu);
+        dst[2 * q + 1] = bf16_bits_to_f32(w[q] >> 16);
+      }
+    }
+    __syncthreads();
+    const float* xr = xs + lane * kRouteXPitch;
+    const float* wr = ws + warp * kRouteEpw * kRouteHc;
+#pragma unroll 4
+    for (int h = 0; h < kRouteHc; h += 4) {
+      const float4 xv = *reinterpret_cast<const float4*>(xr + h);
+#pragma unroll
+      for (int i = 0; i < kRouteEpw; ++i) {
+        const float4 wv = *reinterpret_cast<const float4*>(wr + i * kRouteHc + h);  // broadcast
+        acc[i] = fmaf(xv.x, wv.x, acc[i]);
+        acc[i] = fmaf(xv.y, wv.y, acc[i]);
+        acc[i] = fmaf(xv.z, wv.z, acc[i]);
+        acc[i] = fmaf(xv.w, wv.w, acc[i]);
+      }
+    }
+    __syncthreads();
+  }
+  const int t = t0 + lane;
+  if (t < T) {
+#pragma unroll
+    for (int i = 0; i < kRouteEpw; ++i) {
+      const int e = e0 + warp * kRouteEpw + i;
+      if (e < E) {
+        float v = acc[i];
+        if (bias) v = __fadd_rn(v, __ldg(bias + e));
+        z[(size_t)t * E + e] = v;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
+  return v1 > v2 || (v1 == v2 && e1 < e2);
+}
+
+// One warp per token: top-k (or the forced set), softmax over all E, gates.
+template <int EPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ z,
+                                                         int32_t* __restrict__ idx,
+                                                         float* __restrict__ gates, int T, int E,
+                                                         int k, int forced) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* zt = z + (size_t)t * E;
+  float v[EPL];
+  float m = -FLT_MAX;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? zt[e] : -INFINITY;
+    m = fmaxf(m, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    if (lane + 32 * i < E) s += expf(v[i] - m);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+
+  // chosen expert and its softmax probability for slot j, held by lane j
+  int my_e = -1;
+  float my_p = 0.f;
+  if (forced) {
+    if (lane < k) {
+      my_e = (int)(((long long)k * t + lane) % E);
+      my_p = expf(zt[my_e] - m) / s;
+    }
+  } else {
+    uint32_t taken = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (be == 0x7fffffff || better(v[i], e, bv, be))) {
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (oe != 0x7fffffff && (be == 0x7fffffff || better(ov, oe, bv, be))) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if (be != 0x7fffffff && (be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == j) {
+        my_e = be;
+        my_p = expf(bv - m) / s;
+      }
+    }
+  }
+  float ps = lane < k ? my_p : 0.f;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_e;
+    gates[(size_t)t * k + lane] = my_p / ps;
+  }
+}
+
+// ------------------------------------------------------------------ backward
+// One 256-thread block per group of tokens; each thread owns 16-byte chunks of
+// one token row. dz_j = g_j (dg_j - <g, dg>) on the chosen set;
+// dx = bf16(dx32 + sum_j dz_j * w_r[i_j]).
+__global__ void __launch_bounds__(256) route_bwd_dx_kernel(
+    const float* __restrict__ dgates, const float* __restrict__ gates,
+    const int32_t* __restrict__ idx, const bf16* __restrict__ w_r, const float* __restrict__ dx32,
+    bf16* __restrict__ dx, float* __restrict__ dz, int T, int H, int E, int k, int tpr,
+    int* status) {
+  const int rpb = blockDim.x / tpr;
+  const int t = blockIdx.x * rpb + threadIdx.x / tpr;
+  const int sub = threadIdx.x % tpr;
+  if (t >= T) return;
+  float inner = 0.f;
+  for (int j = 0; j < k; ++j) inner = fmaf(gates[(size_t)t * k + j], dgates[(size_t)t * k + j], inner);
+  const int cpr = H / 8;
+  for (int c = sub; c < cpr; c += tpr) {
+    const float4* src = reinterpret_cast<const float4*>(dx32 + (size_t)t * H + c * 8);
+    float4 p0 = src[0], p1 = src[1];
+    float acc[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[(size_t)t * k + j];
+      if ((unsigned)e >= (unsigned)E) continue;
+      const float g = gates[(size_t)t * k + j];
+      const float dzj = g * (dgates[(size_t)t * k + j] - inner);
+      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)e * H + c * 8));
+      const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = fmaf(dzj, bf16_bits_to_f32(w[q] & 0xFFFFu), acc[2 * q]);
+        acc[2 * q + 1] = fmaf(dzj, bf16_bits_to_f32(w[q] >> 16), acc[2 * q + 1]);
+      }
+    }
+    uint4 out;
+    uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      o[q] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(dx + (size_t)t * H + c * 8) = out;
+  }
+  if (sub == 0) {
+    for (int j = 0; j < k; ++j) {
+      const float g = gates[(size_t)t * k + j];
+      dz[(size_t)t * k + j] = g * (dgates[(size_t)t * k + j] - inner);
+      if ((unsigned)idx[(size_t)t * k + j] >= (unsigned)E) atomicAdd(status + ST_BAD_INDEX, 1);
+    }
+  }
+}
+
+// Expert row chunks: expert e's rows off[e]..off[e+1]-1 are cut into chunks of
+// kRouteBwdRowsPerChunk; chunk c of the whole layer maps to (e, first row).
+// Each block finds its chunk from the per-expert chunk prefix.
+__device__ int find_chunk(const int32_t* __restrict__ off, int E, int chunk, int* e_out,
+                          int* r0_out, int* r1_out, int* s_prefix) {
+  // s_prefix: shared [E+1]; computed by warp 0
+  if (threadIdx.x < 32) {
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + threadIdx.x;
+      int c = 0;
+      if (e < E) c = (off[e + 1] - off[e] + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if ((int)threadIdx.x >= o) incl += n;
+      }
+      if (e < E) s_prefix[e] = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (threadIdx.x == 0) s_prefix[E] = carry;
+  }
+  __syncthreads();
+  if (chunk >= s_prefix[E]) return 0;
+  int lo = 0, hi = E - 1;  // last e with s_prefix[e] <= chunk
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_prefix[mid] <= chunk) lo = mid; else hi = mid - 1;
+  }
+  // skip experts with zero chunks that share the same prefix value
+  const int e = lo;
+  const int r0 = off[e] + (chunk - s_prefix[e]) * kRouteBwdRowsPerChunk;
+  *e_out = e;
+  *r0_out = r0;
+  *r1_out = min(r0 + kRouteBwdRowsPerChunk, (int)off[e + 1]);
+  return 1;
+}
+
+// Pass A: partial[chunk][h] = sum over the chunk's rows s (ascending) of
+// dz[row_src[s]] * x[row_src[s] div k][h].
+__global__ void __launch_bounds__(256) route_bwd_dwr_partial_kernel(
+    const int32_t* __restrict__ off, const int32_t* __restrict__ row_src,
+    const float* __restrict__ dz, const bf16* __restrict__ x, float* __restrict__ part, int T,
+    int H, int E, int k, int* status) {
+  extern __shared__ int s_prefix[];
+  int e, r0, r1;
+  if (!find_chunk(off, E, blockIdx.x, &e, &r0, &r1, s_prefix)) return;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;  // 16-byte chunk of the row
+  if (c * 8 >= H) return;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const long long N = (long long)T * k;
+  for (int s = r0; s < r1; ++s) {
+    const int src = row_src[s];
+    if (src < 0 || src >= N) continue;
+    const float w = dz[src];
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(src / k) * H + c * 8));
+    const uint32_t q4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[2 * q] = fmaf(w, bf16_bits_to_f32(q4[q] & 0xFFFFu), acc[2 * q]);
+      acc[2 * q + 1] = fmaf(w, bf16_bits_to_f32(q4[q] >> 16), acc[2 * q + 1]);
+    }
+  }
+  float4* dst = reinterpret_cast<float4*>(part + (size_t)blockIdx.x * H + c * 8);
+  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+// Pass B: dW_r[e][h] = sum of expert e's chunk partials in chunk order (0 if none).
+__global__ void __launch_bounds__(256) route_bwd_dwr_reduce_kernel(
+    const int32_t* __restrict__ off, const float* __restrict__ part, float* __restrict__ dw_r,
+    int H, int E) {
+  __shared__ int s_first, s_n;
+  const int e = blockIdx.x;
+  if (threadIdx.x == 0) {
+    int first = 0;
+    for (int i = 0; i < e; ++i)
+      first += (off[i + 1] - off[i] + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk;
+    s_first = first;
+    s_n = (off[e + 1] - off[e] + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk;
+  }
+  __syncthreads();
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
+  if (c * 4 >= H) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < s_n; ++i) {
+    const float4 p = *reinterpret_cast<const float4*>(part + (size_t)(s_first + i) * H + c * 4);
+    acc.x += p.x;
+    acc.y += p.y;
+    acc.z += p.z;
+    acc.w += p.w;
+  }
+  *reinterpret_cast<float4*>(dw_r + (size_t)e * H + c * 4) = acc;
+}
+
+}  // namespace
+
+moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
+                          const float* bias, float* logits, int32_t* idx, float* gates,
+                          int* status, cudaStream_t st) {
+  (void)status;
+  if (d.T == 0) return MOE_OK;
+  const int eb = d.E >= 64 ? 64 : ((d.E + kRouteEpw - 1) / kRouteEpw) * kRouteEpw;
+  const int threads = (eb / kRouteEpw) * 32;
+  const size_t smem = (size_t)(kRouteTok * kRouteXPitch + eb * kRouteHc) * sizeof(float);
+  dim3 grid(ceil_div(d.T, kRouteTok), ceil_div(d.E, eb));
+  route_logits_kernel<<<grid, threads, smem, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+  moe_status_t s = check_launch("route_logits_kernel");
+  if (s != MOE_OK) return s;
+  const int tpb = 256, warps = tpb / 32;
+  dim3 g2(ceil_div(d.T, warps));
+  const int forced = d.mode == MOE_ROUTE_FORCED_BALANCED;
+  if (d.E <= 32)
+    route_topk_kernel<1><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+  else if (d.E <= 64)
+    route_topk_kernel<2><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+  else if (d.E <= 128)
+    route_topk_kernel<4><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+  else
+    route_topk_kernel<8><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+  return check_launch("route_topk_kernel");
+}
+
+moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,
+                              const int32_t* idx, const bf16* x, const bf16* w_r,
+                              const int32_t* row_src, const int32_t* off, const float* dx32,
+                              bf16* dx, float* dw_r, float* dz, float* dwr_part, int* status,
+                              cudaStream_t st) {
+  const int cpr = d.H / 8;
+  int tpr = 1;
+  while (tpr < cpr && tpr < 256) tpr <<= 1;
+  const int rpb = 256 / tpr;
+  if (d.T > 0) {
+    route_bwd_dx_kernel<<<ceil_div(d.T, rpb), 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz,
+                                                            d.T, d.H, d.E, d.k, tpr, status);
+    moe_status_t s = check_launch("route_bwd_dx_kernel");
+    if (s != MOE_OK) return s;
+  }
+  const long long N = (long long)d.T * d.k;
+  const int max_chunks = (int)((N + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk) + d.E;
+  if (N > 0) {
+    dim3 ga(max_chunks, ceil_div(cpr, 256));
+    route_bwd_dwr_partial_kernel<<<ga, 256, (d.E + 1) * sizeof(int), st>>>(
+        off, row_src, dz, x, dwr_part, d.T, d.H, d.E, d.k, status);
+    moe_status_t s = check_launch("route_bwd_dwr_partial_kernel");
+    if (s != MOE_OK) return s;
+  }
+  dim3 gb(d.E, ceil_div(d.H / 4, 256));
+  route_bwd_dwr_reduce_kernel<<<gb, 256, 0, st>>>(off, dwr_part, dw_r, d.H, d.E);
+  return check_launch("route_bwd_dwr_reduce_kernel");
+}
+
+}  // namespace moe

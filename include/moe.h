@@ -1,0 +1,288 @@
+/*
+ * moe.h -- C ABI of a GB300 (sm_103a) MoE layer hot path: router softmax/top-k,
+ * dispatch layout, permute into the expert-parallel send layout, grouped SwiGLU
+ * expert FFN on tcgen05 tensor cores, gate-weighted combine, and the backward
+ * split into activation-gradient (dgrad) and weight-gradient (wgrad) calls so
+ * the wgrad can be deferred.
+ *
+ * Where the operations come from.
+ *   - The phases dispatch -> mlp -> combine and the backward chain
+ *     combine -> mlp -> dispatch: the "1. MoE EP Overlap" note (obnotes),
+ *     section "how the 8 fwd/bwd operations are split out".
+ *   - The dgrad-first / wgrad-later split and the deferral (delay_wgrad_compute):
+ *     same note, section "MoE 1F1B overlap"; the MoE expert-parallel overlap
+ *     skill card, section "what it is".
+ *   - The standard all-to-all dispatcher whose send buffer the permute writes:
+ *     skill card, "what it is", dispatcher table.
+ *   - Two streams and two micro-batches overlapping dispatch/combine with the
+ *     expert GEMMs: the note, section "MoE 1F1B overlap".
+ *   The pages give no formulas. The arithmetic is the layer definition stated
+ *   per function below (fp32 logits, softmax, top-k, renormalised gates,
+ *   SwiGLU experts, gate-weighted combine).
+ *
+ * Conventions for every call.
+ *   - Pointers are device pointers unless a name starts with host_. bf16 data is
+ *     passed as moe_bf16 (the raw 16-bit pattern). Matrices are row-major.
+ *   - The caller allocates and owns every buffer, including the workspace whose
+ *     size moe_workspace_size() returns. No call allocates or frees device memory.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls only
+ *     enqueue work on it; none synchronises the host, except moe_device_status()
+ *     and moe_layer_step_host(), which say so.
+ *   - Host-side argument checks return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED
+ *     synchronously, before anything is enqueued; moe_last_error() then holds
+ *     a message (thread-local). A failed launch gives MOE_ERR_CUDA.
+ *   - Device-side checks (an expert index out of range, a pipeline wait that
+ *     ran out of time) never trap: the kernel records a code in the workspace's
+ *     status words, skips the access, and returns; moe_device_status() reads it.
+ *   - Shapes: T >= 0 tokens, H hidden, E experts, k top-k, F expert inner size,
+ *     R emulated expert-parallel ranks. N = T*k routed rows (dropless).
+ *     Limits: 1 <= E <= 256, 1 <= k <= min(E, 32), E % R == 0, H % 64 == 0,
+ *     F % 64 == 0, H <= 16384, F <= 16384, T*k < 2^31.
+ *   - Every device pointer must be 16-byte aligned.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16; /* bfloat16 bit pattern */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_CUDA = 3,
+  MOE_ERR_TIMEOUT = 4
+} moe_status_t;
+
+typedef enum {
+  MOE_ROUTE_SOFTMAX_TOPK = 0,   /* top-k experts by logit, ties to the lower index */
+  MOE_ROUTE_FORCED_BALANCED = 1 /* token t -> experts (k*t + j) mod E, j = 0..k-1 */
+} moe_route_mode_t;
+
+/* One MoE layer's shape. flags must be 0. */
+typedef struct moe_layer_desc {
+  int32_t T, H, E, k, F, R;
+  int32_t mode;  /* moe_route_mode_t */
+  int32_t flags;
+} moe_layer_desc_t;
+
+/* ------------------------------------------------------------------ setup */
+
+/* Checks a descriptor against the limits above. */
+moe_status_t moe_layer_desc_validate(const moe_layer_desc_t* d);
+
+/* Bytes of device workspace every call of this layer shape needs (0 on an
+ * invalid descriptor). One workspace may be shared by calls on one stream; calls
+ * that can overlap on the GPU need workspaces of their own. */
+size_t moe_workspace_size(const moe_layer_desc_t* d);
+
+/* Message of the last error on this host thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Library ABI version (increments on incompatible changes). */
+int32_t moe_abi_version(void);
+
+/* Synchronises `stream`, reads the workspace's device status words and clears
+ * them. MOE_OK, MOE_ERR_INVALID_ARG (a kernel met an out-of-range index and
+ * skipped it) or MOE_ERR_TIMEOUT (a pipeline wait ran out of time). */
+moe_status_t moe_device_status(const moe_layer_desc_t* d, void* ws, void* stream);
+
+/* ------------------------------------------------------------------ forward */
+
+/* Router (the "router" scope ahead of dispatch). For each token t:
+ *   z[t,e] = sum_{h=0..H-1} x[t,h] * w_r[e,h] in fp32, h ascending from 0
+ *            (bf16*bf16 is exact in fp32, so each step is one fp32 rounding),
+ *            plus bias[e] in fp32 when bias != NULL;
+ *   p = softmax(z[t,:]) over all E;
+ *   SOFTMAX_TOPK: idx[t,0..k-1] = the k largest z, descending, ties to the
+ *                 lower expert index;
+ *   FORCED_BALANCED: idx[t,j] = (k*t + j) mod E;
+ *   gates[t,j] = p[idx[t,j]] / sum_l p[idx[t,l]].
+ * x [T,H] bf16, w_r [E,H] bf16, bias [E] fp32 or NULL, logits [T,E] fp32 or NULL
+ * (written when given), idx [T,k] int32, gates [T,k] fp32. */
+moe_status_t moe_route(const moe_layer_desc_t* d, const moe_bf16* x, const moe_bf16* w_r,
+                       const float* bias, float* logits, int32_t* idx, float* gates,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch layout (the preprocessing ahead of the all-to-all): dropless, stable.
+ *   cnt[e]      = #{(t,j) : idx[t,j] = e}
+ *   off[0..E]   = exclusive prefix sum of cnt (off[E] = N)
+ *   slot[t,j]   = off[e] + #{t' < t : e in idx[t',:]}   (e = idx[t,j])
+ *   row_src[s]  = t*k + j for s = slot[t,j]
+ *   cnt_re[r,l] = cnt[r*E/R + l]      rows per (destination rank, local expert)
+ *   rank_off[r] = off[r*E/R], r = 0..R (first row of each rank's chunk)
+ * With rank(e) = e div (E/R) the expert-ordered buffer is the rank-major,
+ * expert-contiguous send buffer an EP all-to-all exchanges, and these tables
+ * are the counts it exchanges first. Every token must pick k distinct experts.
+ * idx [T,k]; cnt [E]; off [E+1]; slot [T,k]; row_src [N]; cnt_re [R,E/R];
+ * rank_off [R+1]; all int32. */
+moe_status_t moe_dispatch_layout(const moe_layer_desc_t* d, const int32_t* idx, int32_t* cnt,
+                                 int32_t* off, int32_t* slot, int32_t* row_src,
+                                 int32_t* cnt_re, int32_t* rank_off, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/* Permute = write the EP send buffer: x_perm[s,:] = x[row_src[s] div k, :].
+ * x [T,H] bf16, row_src [N] int32, x_perm [N,H] bf16. */
+moe_status_t moe_permute(const moe_layer_desc_t* d, const moe_bf16* x, const int32_t* row_src,
+                         moe_bf16* x_perm, void* stream);
+
+/* Expert FFN forward (the "mlp" phase), per expert e on its rows off[e]..off[e+1]-1:
+ *   a = bf16(x_perm_e @ w1[e]^T)               [rows, 2F], fp32 accumulate
+ *   h = bf16(silu(a[:, :F]) * a[:, F:])        [rows, F] (from the bf16 a)
+ *   o = bf16(h @ w2[e]^T)                      [rows, H]
+ * w1 [E,2F,H] bf16 (rows 0..F-1 gate, F..2F-1 up), w2 [E,H,F] bf16, off [E+1]
+ * int32 on the device (read by the kernels' tile schedulers; never by the host).
+ * a [N,2F], h [N,F], o [N,H] bf16; a and h are kept for the backward. */
+moe_status_t moe_expert_ffn_fwd(const moe_layer_desc_t* d, const moe_bf16* x_perm,
+                                const int32_t* off, const moe_bf16* w1, const moe_bf16* w2,
+                                moe_bf16* a, moe_bf16* h, moe_bf16* o, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/* Combine = receive + unpermute (the "combine" phase):
+ *   y[t,:] = bf16( sum_{j=0..k-1} gates[t,j] * o[slot[t,j], :] ), fp32, j ascending.
+ * o [N,H] bf16, slot [T,k] int32, gates [T,k] fp32, y [T,H] bf16. */
+moe_status_t moe_combine(const moe_layer_desc_t* d, const moe_bf16* o, const int32_t* slot,
+                         const float* gates, moe_bf16* y, void* stream);
+
+/* ------------------------------------------------------------------ backward */
+
+/* Combine backward (first step of the backward chain):
+ *   d_o[slot[t,j], :] = bf16(gates[t,j] * dy[t,:])
+ *   dgates[t,j]       = sum_h dy[t,h] * o[slot[t,j], h]   (fp32)
+ * dy [T,H] bf16, o [N,H] bf16, slot [T,k], gates [T,k] fp32 -> d_o [N,H] bf16,
+ * dgates [T,k] fp32. */
+moe_status_t moe_combine_bwd(const moe_layer_desc_t* d, const moe_bf16* dy, const moe_bf16* o,
+                             const int32_t* slot, const float* gates, moe_bf16* d_o,
+                             float* dgates, void* stream);
+
+/* Expert FFN activation gradient (dgrad; runs before wgrad so dispatch-backward
+ * can start early), per expert e on its rows:
+ *   dh      = d_o_e @ w2[e]                          (fp32, not stored)
+ *   da_up   = bf16(dh * silu(a_g))
+ *   da_gate = bf16(dh * a_u * s(a_g) * (1 + a_g * (1 - s(a_g))))   s = sigmoid
+ *   dx_perm = bf16(da_e @ w1[e])
+ * d_o [N,H], a [N,2F] -> da [N,2F] (kept for wgrad), dx_perm [N,H]; bf16. */
+moe_status_t moe_expert_ffn_bwd_dgrad(const moe_layer_desc_t* d, const moe_bf16* d_o,
+                                      const moe_bf16* a, const int32_t* off, const moe_bf16* w1,
+                                      const moe_bf16* w2, moe_bf16* da, moe_bf16* dx_perm,
+                                      void* ws, size_t ws_bytes, void* stream);
+
+/* Expert FFN weight gradient (wgrad; may be deferred, delay_wgrad_compute):
+ *   dw1[e] = bf16(da_e^T @ x_perm_e)   [2F,H]
+ *   dw2[e] = bf16(d_o_e^T @ h_e)       [H,F]
+ * The reduction runs over the expert's own rows only; an expert with no rows
+ * gets zeros. Overwrites dw1 [E,2F,H] and dw2 [E,H,F] (bf16). */
+moe_status_t moe_expert_ffn_bwd_wgrad(const moe_layer_desc_t* d, const moe_bf16* x_perm,
+                                      const moe_bf16* h, const moe_bf16* d_o, const moe_bf16* da,
+                                      const int32_t* off, moe_bf16* dw1, moe_bf16* dw2, void* ws,
+                                      size_t ws_bytes, void* stream);
+
+/* Permute backward (dispatch backward): dx32[t,:] = sum_j dx_perm[slot[t,j], :]
+ * in fp32, j ascending. dx_perm [N,H] bf16, slot [T,k] -> dx32 [T,H] fp32. */
+moe_status_t moe_permute_bwd(const moe_layer_desc_t* d, const moe_bf16* dx_perm,
+                             const int32_t* slot, float* dx32, void* stream);
+
+/* Router backward through the renormalised gates (softmax over the chosen set S):
+ *   dz[t,i_j] = g_j * (dgates_j - sum_l g_l dgates_l), dz = 0 off S
+ *   dx[t,:]   = bf16(dx32[t,:] + sum_j dz[t,i_j] * w_r[i_j,:])
+ *   dw_r[e,:] = sum_{t : e in S_t} dz[t,e] * x[t,:]    (fp32, rows of e in layout order)
+ * dgates, gates [T,k] fp32; idx [T,k]; x [T,H] bf16; w_r [E,H] bf16; row_src [N],
+ * off [E+1] from the layout; dx32 [T,H] fp32 (from moe_permute_bwd);
+ * -> dx [T,H] bf16, dw_r [E,H] fp32 (overwritten). */
+moe_status_t moe_route_bwd(const moe_layer_desc_t* d, const float* dgates, const float* gates,
+                           const int32_t* idx, const moe_bf16* x, const moe_bf16* w_r,
+                           const int32_t* row_src, const int32_t* off, const float* dx32,
+                           moe_bf16* dx, float* dw_r, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ whole layer */
+
+/* Every buffer of one micro-batch (all device pointers, caller-owned). */
+typedef struct moe_mb_bufs {
+  const moe_bf16* x;  /* [T,H] */
+  const moe_bf16* dy; /* [T,H] */
+  const moe_bf16* w_r; const float* bias; const moe_bf16* w1; const moe_bf16* w2;
+  float* logits; int32_t* idx; float* gates;                            /* route   */
+  int32_t* cnt; int32_t* off; int32_t* slot; int32_t* row_src;          /* layout  */
+  int32_t* cnt_re; int32_t* rank_off;
+  moe_bf16* x_perm; moe_bf16* a; moe_bf16* h; moe_bf16* o; moe_bf16* y; /* forward */
+  moe_bf16* d_o; float* dgates; moe_bf16* da; moe_bf16* dx_perm;        /* backward*/
+  float* dx32; moe_bf16* dx; float* dw_r; moe_bf16* dw1; moe_bf16* dw2;
+  void* ws; size_t ws_bytes;
+} moe_mb_bufs_t;
+
+/* Forward: route, dispatch layout, permute, expert FFN, combine. */
+moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b, void* stream);
+
+/* Backward in the chain order combine -> experts (dgrad) -> dispatch -> router,
+ * then the expert wgrad when run_wgrad != 0. */
+moe_status_t moe_layer_backward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
+                                int32_t run_wgrad, void* stream);
+
+/* One training step of the layer from host memory: copies host_x and host_dy
+ * into b->x and b->dy (which must then be writable device buffers), runs the
+ * forward and the backward (with wgrad), and copies y and dx back into host_y
+ * and host_dx. Host buffers should be pinned. Synchronises `stream` at the end. */
+moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
+                                 const moe_bf16* host_x, const moe_bf16* host_dy,
+                                 moe_bf16* host_y, moe_bf16* host_dx, void* stream);
+
+/* ------------------------------------------------------------------ two-stream scheduler */
+
+typedef enum {
+  MOE_PHASE_DISPATCH = 0,     /* route + layout + permute            (comm stream) */
+  MOE_PHASE_FFN_FWD = 1,      /* expert FFN forward                  (GEMM stream) */
+  MOE_PHASE_COMBINE = 2,      /* combine                             (comm stream) */
+  MOE_PHASE_COMBINE_BWD = 3,  /* combine backward                    (comm stream) */
+  MOE_PHASE_DGRAD = 4,        /* expert dgrad                        (GEMM stream) */
+  MOE_PHASE_DISPATCH_BWD = 5, /* permute backward + router backward  (comm stream) */
+  MOE_PHASE_WGRAD = 6         /* expert wgrad                        (GEMM stream) */
+} moe_phase_t;
+
+typedef struct moe_phase_time {
+  int32_t mb;       /* micro-batch 0 or 1 */
+  int32_t phase;    /* moe_phase_t */
+  int32_t stream;   /* 0 = comm stream, 1 = GEMM stream */
+  float start_ms;   /* from the step's start event */
+  float end_ms;
+} moe_phase_time_t;
+
+typedef struct moe_sched moe_sched_t;
+
+/* Creates a scheduler for two micro-batches of shape d on two caller-owned
+ * streams (stream_comm runs route/dispatch/combine and their backward,
+ * stream_gemm the grouped GEMMs). gemm_sms caps the persistent GEMM grid while
+ * overlapping (0 = all SMs). Allocates CUDA events only. */
+moe_status_t moe_sched_create(const moe_layer_desc_t* d, void* stream_comm, void* stream_gemm,
+                              int32_t gemm_sms, moe_sched_t** out);
+
+/* One step = forward and backward of both micro-batches mb[0], mb[1] (each with
+ * its own buffers and workspace; weights may be shared, weight gradients must
+ * not be). overlap = 0: every phase on stream_comm in the order F0 F1 B0 B1.
+ * overlap = 1: phases spread over the two streams so one micro-batch's
+ * dispatch/combine runs beside the other's GEMMs, ordered by events on data
+ * dependencies only. defer_wgrad = 1: micro-batch 1's wgrad is not run in this
+ * step but at the start of the next one (beside micro-batch 0's dispatch), or by
+ * moe_sched_flush(). Outputs are bit-identical to the serial schedule's. */
+moe_status_t moe_sched_step(moe_sched_t* s, const moe_mb_bufs_t* mb, int32_t overlap,
+                            int32_t defer_wgrad);
+
+/* Runs a deferred wgrad, if one is pending, on stream_gemm. */
+moe_status_t moe_sched_flush(moe_sched_t* s);
+
+/* Per-phase start/end times of the last step (synchronises both streams).
+ * Writes up to cap entries and the count to *n. */
+moe_status_t moe_sched_timings(moe_sched_t* s, moe_phase_time_t* out, int32_t cap, int32_t* n);
+
+void moe_sched_destroy(moe_sched_t* s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,93 @@
+"""The C-ABI library: it loads, exports every function include/moe.h declares,
+and its host-side checks (no GPU work) behave as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_router_softmax_top_gb300 as moe
+from combine_router_softmax_top_gb300 import build
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return moe.lib()
+
+
+def declared_functions():
+    text = open(moe.HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_whole_path():
+    names = declared_functions()
+    for want in ("moe_route", "moe_dispatch_layout", "moe_permute", "moe_expert_ffn_fwd",
+                 "moe_combine", "moe_combine_bwd", "moe_expert_ffn_bwd_dgrad",
+                 "moe_expert_ffn_bwd_wgrad", "moe_permute_bwd", "moe_route_bwd",
+                 "moe_sched_create", "moe_sched_step", "moe_sched_timings", "moe_sched_destroy"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+    # and the binding wraps every one of them
+    assert set(declared_functions()) <= set(moe._SIGS)
+
+
+def test_library_is_in_tree_and_sm103a(L):
+    assert os.path.dirname(moe.LIB_PATH) == os.path.dirname(os.path.abspath(moe.__file__))
+    assert L.moe_abi_version() == 1
+    assert "compute_103a,code=sm_103a" in " ".join(build.ARCH)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=256, H=128, E=8, k=2, F=256), moe.MOE_OK),
+    (dict(T=0, H=128, E=8, k=2, F=256), moe.MOE_OK),
+    (dict(T=-1, H=128, E=8, k=2, F=256), moe.MOE_ERR_INVALID_ARG),
+    (dict(T=16, H=128, E=8, k=9, F=256), moe.MOE_ERR_INVALID_ARG),      # k > E
+    (dict(T=16, H=128, E=8, k=2, F=256, R=3), moe.MOE_ERR_INVALID_ARG),  # E % R
+    (dict(T=16, H=100, E=8, k=2, F=256), moe.MOE_ERR_UNSUPPORTED),      # H % 64
+    (dict(T=16, H=128, E=8, k=2, F=96), moe.MOE_ERR_UNSUPPORTED),       # F % 64
+    (dict(T=16, H=128, E=300, k=2, F=256), moe.MOE_ERR_UNSUPPORTED),    # E > 256
+    (dict(T=16, H=128, E=64, k=33, F=256), moe.MOE_ERR_UNSUPPORTED),    # k > 32
+    (dict(T=16, H=128, E=8, k=2, F=256, mode=7), moe.MOE_ERR_INVALID_ARG),
+])
+def test_descriptor_validation(L, kw, status):
+    d = moe.LayerDesc.of(**kw)
+    assert moe.moe_layer_desc_validate(d) == status
+    if status != moe.MOE_OK:
+        assert L.moe_last_error()
+
+
+def test_workspace_size_covers_every_scratch_area(L):
+    d = moe.LayerDesc.of(T=4096, H=2048, E=128, k=8, F=768)
+    n = moe.moe_workspace_size(d)
+    N = 4096 * 8
+    # status words + logits + histograms + dz + router-backward partials
+    assert n >= 256 + 4096 * 128 * 4 + 16 * 128 * 4 + N * 4 + (N // 64 + 128) * 2048 * 4
+    with pytest.raises(moe.MoeError):
+        moe.moe_workspace_size(moe.LayerDesc.of(T=1, H=100, E=8, k=2, F=256))
+
+
+def test_null_and_misaligned_pointers_are_rejected_before_any_launch(L):
+    d = moe.LayerDesc.of(T=16, H=128, E=8, k=2, F=256)
+    st = L.moe_permute(ctypes.byref(d), None, ctypes.c_void_p(16), ctypes.c_void_p(16), None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"NULL" in L.moe_last_error()
+    st = L.moe_permute(ctypes.byref(d), ctypes.c_void_p(18), ctypes.c_void_p(16),
+                       ctypes.c_void_p(16), None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"aligned" in L.moe_last_error()
+    st = L.moe_route(ctypes.byref(d), ctypes.c_void_p(16), ctypes.c_void_p(16), None, None,
+                     ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), 8, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"workspace" in L.moe_last_error()
+
+
+def test_scheduler_needs_two_streams(L):
+    d = moe.LayerDesc.of(T=16, H=128, E=8, k=2, F=256)
+    h = ctypes.c_void_p()
+    st = L.moe_sched_create(ctypes.byref(d), ctypes.c_void_p(1), ctypes.c_void_p(1), 0,
+                            ctypes.byref(h))
+    assert st == moe.MOE_ERR_INVALID_ARG
