@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark: one MoE layer's forward + backward (dgrad and wgrad) on GB300.
+
+A step is one pass of the whole hot path over one batch: route, dispatch
+layout, permute, expert FFN forward, combine, combine backward, expert dgrad,
+permute backward, router backward and expert wgrad, all through the C ABI on
+one stream, with inputs already resident in HBM. The default workload is the
+Qwen3-30B-A3B-shaped layer with forced-balanced routing (T=4096 tokens,
+H=2048, 128 experts, top-8, SwiGLU inner 768), the configuration the pages
+benchmark EP overlap on; data are synthetic (seeded, see moe_synth).
+
+Prints one JSON line (rank 0). With --impl reference the CPU oracle is timed
+instead, on a bounded token sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+Under torchrun (N > 1) each rank runs an independent replica (weak scaling,
+no collective on the data path; the barrier and the max-over-ranks timing use
+the process group).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(d) -> dict:
+    """Minimum bytes moved and flops per launch of each kernel for shape d.
+
+    Bytes count each tensor the kernel must read or write once (x re-reads of
+    the gathers are served by L2 and not counted); flops count multiply-adds
+    as 2."""
+    T, H, E, k, F = d["T"], d["H"], d["E"], d["k"], d["F"]
+    N = T * k
+    b2, b4 = 2, 4
+    out = {
+        "route_logits": (T * H * b2 + E * H * b2 + T * E * b4, 2.0 * T * H * E),
+        "route_topk": (T * E * b4 + 2 * N * b4, 0.0),
+        "layout_count": (N * b4, 0.0),
+        "layout_assign": (N * b4 + 2 * N * b4, 0.0),
+        "permute": (T * H * b2 + N * b4 + N * H * b2, 0.0),
+        "combine": (N * H * b2 + 2 * N * b4 + T * H * b2, 2.0 * N * H),
+        "combine_bwd": (T * H * b2 + N * H * b2 + 2 * N * b4 + N * H * b2 + N * b4, 3.0 * N * H),
+        "permute_bwd": (N * H * b2 + N * b4 + T * H * b4, 1.0 * N * H),
+        "route_bwd_dx": (T * H * b4 + E * H * b2 + 3 * N * b4 + T * H * b2, 2.0 * N * H),
+        "route_bwd_dwr_partial": (T * H * b2 + 2 * N * b4, 2.0 * N * H),
+        "route_bwd_dwr_reduce": (E * H * b4, 0.0),
+        "gemm_fc1_fwd": (N * H * b2 + E * 2 * F * H * b2 + N * 2 * F * b2 + N * F * b2,
+                         2.0 * N * H * 2 * F),
+        "gemm_fc2_fwd": (N * F * b2 + E * H * F * b2 + N * H * b2, 2.0 * N * F * H),
+        "gemm_fc2_dgrad": (N * H * b2 + E * H * F * b2 + 2 * N * 2 * F * b2, 2.0 * N * H * F),
+        "gemm_fc1_dgrad": (N * 2 * F * b2 + E * 2 * F * H * b2 + N * H * b2, 2.0 * N * 2 * F * H),
+        "gemm_wgrad_w1": (N * 2 * F * b2 + N * H * b2 + E * 2 * F * H * b2, 2.0 * N * 2 * F * H),
+        "gemm_wgrad_w2": (N * H * b2 + N * F * b2 + E * H * F * b2, 2.0 * N * H * F),
+    }
+    return out
+
+
+def source_digest() -> str:
+    """Hash of the CUDA sources: ncu traffic figures are used only while it matches."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_router_softmax_top_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        if t.get("source_digest") != source_digest():
+            return None
+        v = t.get("kernels", {}).get(workload, {}).get(kernel)
+        return None if v is None else float(v)
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.proc = None
+        try:
+            bus = torch.cuda.get_device_properties(device).pci_bus_id
+        except Exception:
+            bus = str(device)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(bus), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (the slowest rank sets the time)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def emit(obj):
+    print(json.dumps(obj), flush=True)
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_tokens_per_s(workload: str, T_sample: int):
+    """Times the CPU oracle (fwd + bwd) on the first T_sample tokens of the workload."""
+    import moe_synth
+    from oracle import moe_oracle as O
+    inp = moe_synth.workload(workload, T=T_sample)
+    t0 = time.perf_counter()
+    fwd = O.layer_forward(inp)
+    O.layer_backward(inp, fwd)
+    dt = time.perf_counter() - t0
+    return T_sample / dt, dt
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import moe_synth
+    import combine_router_softmax_top_gb300 as moe
+    from combine_router_softmax_top_gb300 import build
+
+    build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, pk_kind = peaks()
+    inp = moe_synth.workload(args.workload, microbatch=rank)
+    shape = inp.shape_dict()
+    d = moe.LayerDesc.of(**shape)
+    b = moe.LayerBuffers(d, dev)
+    b.load_inputs(inp)
+    st = torch.cuda.Stream(device=dev)
+
+    def step():
+        moe.moe_layer_forward(d, b, st)
+        moe.moe_layer_backward(d, b, True, st)
+
+    for _ in range(args.warmup):
+        step()
+    status = moe.moe_device_status(d, b.ws, st)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device status {status}: {moe.lib().moe_last_error()}")
+    torch.cuda.synchronize(dev)
+    per_step_launches = 0
+    l0 = moe.moe_kernel_launches()
+    step()
+    torch.cuda.synchronize(dev)
+    per_step_launches = moe.moe_kernel_launches() - l0
+
+    # ---- timed region
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    time.sleep(0.25)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = moe.moe_kernel_launches()
+    moe.moe_profile_start(per_step_launches * args.steps + 8)
+    e0.record(st)
+    for _ in range(args.steps):
+        step()
+    e1.record(st)
+    torch.cuda.synchronize(dev)
+    prof = moe.moe_profile_stop(per_step_launches * args.steps + 8)
+    launches = moe.moe_kernel_launches() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms_local, world)
+    status = moe.moe_device_status(d, b.ws, st)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device status {status}: {moe.lib().moe_last_error()}")
+    tokens_per_s = world * inp.T / (ms / 1e3)
+
+    # ---- per-kernel figures from the live events
+    algo = algorithmic(shape)
+    agg = {}
+    for name, t in prof:
+        a = agg.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += t
+    kernels = {}
+    for name, (n, tot) in agg.items():
+        avg_ms = tot / n
+        by, fl = algo.get(name, (0.0, 0.0))
+        gbs = by / (avg_ms * 1e-3) / 1e9 if avg_ms > 0 else 0.0
+        tfl = fl / (avg_ms * 1e-3) / 1e12 if avg_ms > 0 else 0.0
+        t_hbm = by / (pk["hbm_gbs"] * 1e9)
+        t_tc = fl / (pk["bf16_tflops_sustained"] * 1e12) if name.startswith("gemm") else 0.0
+        bound = "tensor" if t_tc > t_hbm else "hbm"
+        frac = (t_tc if bound == "tensor" else t_hbm) / (avg_ms * 1e-3) if avg_ms > 0 else 0.0
+        kernels[name] = {"launches": n, "avg_us": round(avg_ms * 1e3, 2),
+                         "share": None, "GB_s": round(gbs, 1), "TFLOP_s": round(tfl, 1),
+                         "bound": bound, "roofline_frac": round(frac, 3),
+                         "algo_bytes": int(by), "algo_flops": fl}
+    total = sum(v[1] for v in agg.values())
+    for name in kernels:
+        kernels[name]["share"] = round(agg[name][1] / total, 4) if total else None
+    dom = max(agg, key=lambda n: agg[n][1])
+    kd = kernels[dom]
+    if kd["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": kd["TFLOP_s"], "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": kd["GB_s"], "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = traffic_for(dom, args.workload)
+    roof["kernel"] = dom
+    roof["peak_kind"] = pk_kind
+    gemm_names = [n for n in kernels if n.startswith("gemm")]
+    gemm_ms = sum(agg[n][1] for n in gemm_names) / args.steps
+    gemm_fl = sum(algo[n][1] for n in gemm_names)
+    pc_names = [n for n in ("permute", "combine", "combine_bwd", "permute_bwd") if n in agg]
+    pc_ms = sum(agg[n][1] for n in pc_names) / args.steps
+    pc_bytes = sum(algo[n][0] for n in pc_names)
+
+    # ---- end to end through the host-buffer C-ABI call
+    hx = inp.x.clone().pin_memory()
+    hdy = inp.dy.clone().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    moe.moe_layer_step_host(d, b, hx, hdy, hy, hdx, st)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        moe.moe_layer_step_host(d, b, hx, hdy, hy, hdx, st)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world)
+    nbytes = inp.T * inp.H * 2
+
+    out = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded moe_synth inputs; random-init weights of the layer's shape)",
+        "config": {"workload": args.workload, **shape, "steps_per_call": "fwd+dgrad+wgrad",
+                   "l2": "inputs larger than L2: %.2f GB of expert weights and %.2f GB of "
+                         "activations streamed per step" % (
+                             inp.E * 3 * inp.F * inp.H * 2 / 1e9,
+                             inp.T * inp.k * (4 * inp.H + 6 * inp.F) * 2 / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(world * inp.T / e2e_s, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes},
+        "gpu_launches": int(launches),
+        "roofline": roof,
+        "clocks": clk,
+        "permute_combine_GB_s": round(pc_bytes / (pc_ms * 1e-3) / 1e9, 1) if pc_ms else None,
+        "grouped_gemm_TFLOP_s": round(gemm_fl / (gemm_ms * 1e-3) / 1e12, 1) if gemm_ms else None,
+        "kernels": kernels,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt = oracle_tokens_per_s(args.workload, args.cpu_sample_tokens)
+        out["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cpu_cores(),
+                               "kind": "oracle",
+                               "sample": f"first {args.cpu_sample_tokens} tokens of the workload, "
+                                         f"one fwd+bwd ({dt:.1f} s), numpy float64 + OpenBLAS"}
+    if rank == 0:
+        emit(out)
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on a bounded token sample per step."""
+    if rank != 0:
+        return
+    import moe_synth
+    from oracle import moe_oracle as O
+    Ts = args.ref_sample_tokens
+    inp = moe_synth.workload(args.workload, T=Ts)
+    shape = inp.shape_dict()
+
+    def step():
+        fwd = O.layer_forward(inp)
+        O.layer_backward(inp, fwd)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    v = Ts / dt
+    emit({"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tokens/s",
+          "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+          "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+          "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+          "config": {"workload": args.workload, **shape, "T_full": moe_synth.WORKLOADS[args.workload]["T"],
+                     "parallelism": "single process"},
+          "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": cpu_cores(),
+                           "kind": "oracle",
+                           "sample": f"first {Ts} tokens of the workload per step"},
+          "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}})
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_30b_a3b_balanced")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=256)
+    ap.add_argument("--ref-sample-tokens", type=int, default=64)
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps, always
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

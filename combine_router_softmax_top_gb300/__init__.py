@@ -58,6 +58,10 @@ class PhaseTime(ctypes.Structure):
                 ("start_ms", ctypes.c_float), ("end_ms", ctypes.c_float)]
 
 
+class KernelTime(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("ms", ctypes.c_float)]
+
+
 _lib = None
 
 _VP, _I32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
@@ -68,6 +72,10 @@ _SIGS = {
     "moe_layer_desc_validate": ([_DP], _I32),
     "moe_workspace_size": ([_DP], _SZ),
     "moe_device_status": ([_DP, _VP, _VP], _I32),
+    "moe_kernel_launches": ([], ctypes.c_uint64),
+    "moe_kernel_name": ([_I32], ctypes.c_char_p),
+    "moe_profile_start": ([_I32], _I32),
+    "moe_profile_stop": ([ctypes.POINTER(KernelTime), _I32, ctypes.POINTER(_I32)], _I32),
     "moe_route": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_dispatch_layout": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_permute": ([_DP, _VP, _VP, _VP, _VP], _I32),
@@ -142,6 +150,26 @@ def moe_workspace_size(desc: LayerDesc) -> int:
 
 def moe_device_status(desc, ws, stream=None) -> int:
     return lib().moe_device_status(_d(desc), _p(ws), _s(stream))
+
+
+def moe_kernel_launches() -> int:
+    return int(lib().moe_kernel_launches())
+
+
+def moe_kernel_name(kernel: int) -> str:
+    return lib().moe_kernel_name(int(kernel)).decode()
+
+
+def moe_profile_start(capacity: int):
+    _check(lib().moe_profile_start(int(capacity)), "moe_profile_start")
+
+
+def moe_profile_stop(cap: int = 4096):
+    """[(kernel name, ms), ...] of the launches recorded since moe_profile_start."""
+    buf = (KernelTime * cap)()
+    n = ctypes.c_int32()
+    _check(lib().moe_profile_stop(buf, cap, ctypes.byref(n)), "moe_profile_stop")
+    return [(moe_kernel_name(buf[i].kernel), float(buf[i].ms)) for i in range(n.value)]
 
 
 def moe_route(desc, x, w_r, bias, logits, idx, gates, ws, stream=None):

@@ -522,7 +522,10 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KPara
     set_error("cudaFuncSetAttribute failed: %s", cudaGetErrorString(attr_err));
     return MOE_ERR_CUDA;
   }
-  grouped_gemm_kernel<MODE><<<grid, kThreads, kDynSmem, st>>>(a, b, p);
+  {
+    LaunchScope _ls(K_GEMM_FC1_FWD + MODE, st);
+    grouped_gemm_kernel<MODE><<<grid, kThreads, kDynSmem, st>>>(a, b, p);
+  }
   return check_launch("grouped_gemm_kernel");
 }
 

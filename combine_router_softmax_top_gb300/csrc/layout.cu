@@ -135,12 +135,18 @@ moe_status_t launch_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_
                            int32_t* off, int32_t* slot, int32_t* row_src, int32_t* cnt_re,
                            int32_t* rank_off, int* hist, int* status, cudaStream_t st) {
   const int nb = d.T > 0 ? ceil_div(d.T, kTok) : 1;
-  layout_count_kernel<<<nb, kTok, d.E * sizeof(int), st>>>(idx, hist, d.T, d.E, d.k, status);
+  {
+    LaunchScope _ls(K_LAYOUT_COUNT, st);
+    layout_count_kernel<<<nb, kTok, d.E * sizeof(int), st>>>(idx, hist, d.T, d.E, d.k, status);
+  }
   moe_status_t s = check_launch("layout_count_kernel");
   if (s != MOE_OK) return s;
   const size_t smem = (size_t)d.E * (2 + 2 * kWarps) * sizeof(int);
-  layout_assign_kernel<<<nb, kTok, smem, st>>>(idx, hist, cnt, off, slot, row_src, cnt_re,
-                                               rank_off, d.T, d.E, d.k, d.R, nb);
+  {
+    LaunchScope _ls(K_LAYOUT_ASSIGN, st);
+    layout_assign_kernel<<<nb, kTok, smem, st>>>(idx, hist, cnt, off, slot, row_src, cnt_re,
+                                                 rank_off, d.T, d.E, d.k, d.R, nb);
+  }
   return check_launch("layout_assign_kernel");
 }
 

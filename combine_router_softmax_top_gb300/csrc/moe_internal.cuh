@@ -30,6 +30,29 @@ WsLayout ws_layout(const moe_layer_desc_t& d);
 
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
+// ---------------------------------------------------------------- launch accounting
+enum KernelId {
+  K_ROUTE_LOGITS = 0, K_ROUTE_TOPK, K_LAYOUT_COUNT, K_LAYOUT_ASSIGN, K_PERMUTE, K_COMBINE,
+  K_COMBINE_BWD, K_PERMUTE_BWD, K_ROUTE_BWD_DX, K_ROUTE_BWD_DWR_PARTIAL, K_ROUTE_BWD_DWR_REDUCE,
+  K_GEMM_FC1_FWD, K_GEMM_FC2_FWD, K_GEMM_FC2_DGRAD, K_GEMM_FC1_DGRAD, K_GEMM_WGRAD_W1,
+  K_GEMM_WGRAD_W2, K_NUM
+};
+
+// Wraps one kernel launch: counts it and, while profiling is on, brackets it
+// with CUDA events on its stream.
+class LaunchScope {
+ public:
+  LaunchScope(int kernel, cudaStream_t st);
+  ~LaunchScope();
+  LaunchScope(const LaunchScope&) = delete;
+  LaunchScope& operator=(const LaunchScope&) = delete;
+
+ private:
+  int kernel_;
+  cudaStream_t st_;
+  int rec_;
+};
+
 // ---------------------------------------------------------------- errors
 void set_error(const char* fmt, ...);
 moe_status_t check_launch(const char* what);

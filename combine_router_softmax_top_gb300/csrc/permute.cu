@@ -246,7 +246,10 @@ moe_status_t launch_permute(const moe_layer_desc_t& d, const bf16* x, const int3
   long long blocks = (N + warps_per_block - 1) / warps_per_block;
   const long long cap = (long long)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
-  permute_kernel<<<(int)blocks, 256, 0, st>>>(x, row_src, x_perm, d.T, d.H, d.k, N);
+  {
+    LaunchScope _ls(K_PERMUTE, st);
+    permute_kernel<<<(int)blocks, 256, 0, st>>>(x, row_src, x_perm, d.T, d.H, d.k, N);
+  }
   return check_launch("permute_kernel");
 }
 
@@ -254,8 +257,11 @@ moe_status_t launch_combine(const moe_layer_desc_t& d, const bf16* o, const int3
                             const float* gates, bf16* y, cudaStream_t st) {
   if (d.T == 0) return MOE_OK;
   const int tpr = threads_per_row(d.H);
-  combine_kernel<<<ceil_div(d.T, 256 / tpr), 256, 0, st>>>(o, slot, gates, y, d.T, d.H, d.k,
-                                                           (long long)d.T * d.k, tpr);
+  {
+    LaunchScope _ls(K_COMBINE, st);
+    combine_kernel<<<ceil_div(d.T, 256 / tpr), 256, 0, st>>>(o, slot, gates, y, d.T, d.H, d.k,
+                                                             (long long)d.T * d.k, tpr);
+  }
   return check_launch("combine_kernel");
 }
 
@@ -267,15 +273,30 @@ moe_status_t launch_combine_bwd(const moe_layer_desc_t& d, const bf16* dy, const
   const dim3 grid(ceil_div(d.T, 256 / tpr));
   const long long N = (long long)d.T * d.k;
   if (d.k <= 2)
-    combine_bwd_kernel<2><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    {
+      LaunchScope _ls(K_COMBINE_BWD, st);
+      combine_bwd_kernel<2><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    }
   else if (d.k <= 4)
-    combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    {
+      LaunchScope _ls(K_COMBINE_BWD, st);
+      combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    }
   else if (d.k <= 8)
-    combine_bwd_kernel<8><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    {
+      LaunchScope _ls(K_COMBINE_BWD, st);
+      combine_bwd_kernel<8><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    }
   else if (d.k <= 16)
-    combine_bwd_kernel<16><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    {
+      LaunchScope _ls(K_COMBINE_BWD, st);
+      combine_bwd_kernel<16><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    }
   else
-    combine_bwd_kernel<32><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    {
+      LaunchScope _ls(K_COMBINE_BWD, st);
+      combine_bwd_kernel<32><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+    }
   return check_launch("combine_bwd_kernel");
 }
 
@@ -283,8 +304,11 @@ moe_status_t launch_permute_bwd(const moe_layer_desc_t& d, const bf16* dx_perm,
                                 const int32_t* slot, float* dx32, cudaStream_t st) {
   if (d.T == 0) return MOE_OK;
   const int tpr = threads_per_row(d.H);
-  permute_bwd_kernel<<<ceil_div(d.T, 256 / tpr), 256, 0, st>>>(dx_perm, slot, dx32, d.T, d.H,
-                                                               d.k, (long long)d.T * d.k, tpr);
+  {
+    LaunchScope _ls(K_PERMUTE_BWD, st);
+    permute_bwd_kernel<<<ceil_div(d.T, 256 / tpr), 256, 0, st>>>(dx_perm, slot, dx32, d.T, d.H,
+                                                                 d.k, (long long)d.T * d.k, tpr);
+  }
   return check_launch("permute_bwd_kernel");
 }
 

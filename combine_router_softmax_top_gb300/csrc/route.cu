@@ -340,20 +340,35 @@ moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* 
   const int threads = (eb / kRouteEpw) * 32;
   const size_t smem = (size_t)(kRouteTok * kRouteXPitch + eb * kRouteHc) * sizeof(float);
   dim3 grid(ceil_div(d.T, kRouteTok), ceil_div(d.E, eb));
-  route_logits_kernel<<<grid, threads, smem, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+  {
+    LaunchScope _ls(K_ROUTE_LOGITS, st);
+    route_logits_kernel<<<grid, threads, smem, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+  }
   moe_status_t s = check_launch("route_logits_kernel");
   if (s != MOE_OK) return s;
   const int tpb = 256, warps = tpb / 32;
   dim3 g2(ceil_div(d.T, warps));
   const int forced = d.mode == MOE_ROUTE_FORCED_BALANCED;
   if (d.E <= 32)
-    route_topk_kernel<1><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+    {
+      LaunchScope _ls(K_ROUTE_TOPK, st);
+      route_topk_kernel<1><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+    }
   else if (d.E <= 64)
-    route_topk_kernel<2><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+    {
+      LaunchScope _ls(K_ROUTE_TOPK, st);
+      route_topk_kernel<2><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+    }
   else if (d.E <= 128)
-    route_topk_kernel<4><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+    {
+      LaunchScope _ls(K_ROUTE_TOPK, st);
+      route_topk_kernel<4><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+    }
   else
-    route_topk_kernel<8><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+    {
+      LaunchScope _ls(K_ROUTE_TOPK, st);
+      route_topk_kernel<8><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
+    }
   return check_launch("route_topk_kernel");
 }
 
@@ -367,8 +382,11 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
   while (tpr < cpr && tpr < 256) tpr <<= 1;
   const int rpb = 256 / tpr;
   if (d.T > 0) {
-    route_bwd_dx_kernel<<<ceil_div(d.T, rpb), 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz,
-                                                            d.T, d.H, d.E, d.k, tpr, status);
+    {
+      LaunchScope _ls(K_ROUTE_BWD_DX, st);
+      route_bwd_dx_kernel<<<ceil_div(d.T, rpb), 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz,
+                                                              d.T, d.H, d.E, d.k, tpr, status);
+    }
     moe_status_t s = check_launch("route_bwd_dx_kernel");
     if (s != MOE_OK) return s;
   }
@@ -376,13 +394,19 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
   const int max_chunks = (int)((N + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk) + d.E;
   if (N > 0) {
     dim3 ga(max_chunks, ceil_div(cpr, 256));
-    route_bwd_dwr_partial_kernel<<<ga, 256, (d.E + 1) * sizeof(int), st>>>(
-        off, row_src, dz, x, dwr_part, d.T, d.H, d.E, d.k, status);
+    {
+      LaunchScope _ls(K_ROUTE_BWD_DWR_PARTIAL, st);
+      route_bwd_dwr_partial_kernel<<<ga, 256, (d.E + 1) * sizeof(int), st>>>(
+          off, row_src, dz, x, dwr_part, d.T, d.H, d.E, d.k, status);
+    }
     moe_status_t s = check_launch("route_bwd_dwr_partial_kernel");
     if (s != MOE_OK) return s;
   }
   dim3 gb(d.E, ceil_div(d.H / 4, 256));
-  route_bwd_dwr_reduce_kernel<<<gb, 256, 0, st>>>(off, dwr_part, dw_r, d.H, d.E);
+  {
+    LaunchScope _ls(K_ROUTE_BWD_DWR_REDUCE, st);
+    route_bwd_dwr_reduce_kernel<<<gb, 256, 0, st>>>(off, dwr_part, dw_r, d.H, d.E);
+  }
   return check_launch("route_bwd_dwr_reduce_kernel");
 }
 

@@ -93,6 +93,28 @@ int32_t moe_abi_version(void);
  * skipped it) or MOE_ERR_TIMEOUT (a pipeline wait ran out of time). */
 moe_status_t moe_device_status(const moe_layer_desc_t* d, void* ws, void* stream);
 
+/* ------------------------------------------------------------------ diagnostics */
+
+/* Number of kernels this library has launched in the process so far. */
+uint64_t moe_kernel_launches(void);
+
+/* Name of kernel id `kernel` as reported by moe_profile_stop ("" if unknown). */
+const char* moe_kernel_name(int32_t kernel);
+
+typedef struct moe_kernel_time {
+  int32_t kernel; /* kernel id, see moe_kernel_name() */
+  float ms;       /* duration between events recorded just before and after the
+                     launch on the launch's own stream */
+} moe_kernel_time_t;
+
+/* Starts recording per-launch durations of the next `capacity` launches (on any
+ * stream). Creates CUDA events on first use; allocates no device memory. */
+moe_status_t moe_profile_start(int32_t capacity);
+
+/* Stops recording, waits for the recorded events and returns up to cap entries
+ * in launch order; *n receives the count. */
+moe_status_t moe_profile_stop(moe_kernel_time_t* out, int32_t cap, int32_t* n);
+
 /* ------------------------------------------------------------------ forward */
 
 /* Router (the "router" scope ahead of dispatch). For each token t:
