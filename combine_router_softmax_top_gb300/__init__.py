@@ -78,6 +78,7 @@ _SIGS = {
     "moe_profile_stop": ([ctypes.POINTER(KernelTime), _I32, ctypes.POINTER(_I32)], _I32),
     "moe_route": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_dispatch_layout": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
+    "moe_dispatch_layout_static": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
     "moe_permute": ([_DP, _VP, _VP, _VP, _VP], _I32),
     "moe_expert_ffn_fwd": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_combine": ([_DP, _VP, _VP, _VP, _VP, _VP], _I32),
@@ -182,6 +183,13 @@ def moe_dispatch_layout(desc, idx, cnt, off, slot, row_src, cnt_re, rank_off, ws
                                      _p(cnt_re), _p(rank_off), _p(ws),
                                      ws.numel() * ws.element_size(), _s(stream)),
            "moe_dispatch_layout")
+
+
+def moe_dispatch_layout_static(desc, idx, cnt, off, slot, row_src, cnt_re, rank_off, stream=None):
+    """Dispatch layout without a workspace (library-owned scratch; see include/moe.h)."""
+    _check(lib().moe_dispatch_layout_static(_d(desc), _p(idx), _p(cnt), _p(off), _p(slot),
+                                            _p(row_src), _p(cnt_re), _p(rank_off), _s(stream)),
+           "moe_dispatch_layout_static")
 
 
 def moe_permute(desc, x, row_src, x_perm, stream=None):

@@ -149,6 +149,26 @@ moe_status_t moe_dispatch_layout(const moe_layer_desc_t* d, const int32_t* idx, 
                                  int32_t* cnt_re, int32_t* rank_off, void* ws, size_t ws_bytes,
                                  void* stream);
 
+/* The same dispatch layout for callers that cannot allocate device memory:
+ * a plugin that receives only its input and output tensors from a host
+ * framework that owns the allocator, code recorded into a CUDA graph (where
+ * cudaMalloc is not allowed while the stream is being captured), or a path
+ * that must not block on allocator locks. Instead of a caller workspace it
+ * uses a fixed scratch array inside the library's device memory, sized for at
+ * most T = 65536 tokens and E = 256 experts (256 KB plus 256 bytes, held on
+ * every GPU that loads the library until the process exits); larger shapes
+ * return MOE_ERR_UNSUPPORTED. The pages describe no such call; it exists for
+ * these callers only. The first call on each device looks up the scratch
+ * array's device address (with that device current), so make that first call
+ * before any stream capture. All calls share the one array: calls whose GPU
+ * work can overlap (unordered streams) race and must not be issued; calls on
+ * one stream are safe. Out-of-range expert indices are skipped (slot = -1).
+ * Outputs and argument meaning as for moe_dispatch_layout. Allocates nothing. */
+moe_status_t moe_dispatch_layout_static(const moe_layer_desc_t* d, const int32_t* idx,
+                                        int32_t* cnt, int32_t* off, int32_t* slot,
+                                        int32_t* row_src, int32_t* cnt_re, int32_t* rank_off,
+                                        void* stream);
+
 /* Permute = write the EP send buffer: x_perm[s,:] = x[row_src[s] div k, :].
  * x [T,H] bf16, row_src [N] int32, x_perm [N,H] bf16. */
 moe_status_t moe_permute(const moe_layer_desc_t* d, const moe_bf16* x, const int32_t* row_src,
