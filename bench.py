@@ -81,24 +81,35 @@ def algorithmic(d) -> dict:
     return out
 
 
-def source_digest() -> str:
-    """Hash of the CUDA sources: ncu traffic figures are used only while it matches."""
+KERNEL_SOURCES = {  # the files each kernel family is built from
+    "gemm": ("grouped_gemm.cu", "sm100_ptx.cuh", "moe_internal.cuh"),
+    "route": ("route.cu", "moe_internal.cuh"),
+    "layout": ("layout.cu", "moe_internal.cuh"),
+    "permute": ("permute.cu", "moe_internal.cuh"),
+    "combine": ("permute.cu", "moe_internal.cuh"),
+}
+
+
+def source_digest(kernel: str) -> str:
+    """Hash of the sources of one kernel: ncu traffic figures count only while it matches."""
+    files = KERNEL_SOURCES.get(kernel.split("_")[0], ())
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_router_softmax_top_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu record, or None if stale/absent."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
-        if t.get("source_digest") != source_digest():
+        rec = t.get(workload, {}).get(kernel)
+        if not rec or rec.get("source_digest") != source_digest(kernel):
             return None
-        v = t.get("kernels", {}).get(workload, {}).get(kernel)
-        return None if v is None else float(v)
+        return float(rec["dram_bytes_per_launch"])
     except Exception:
         return None
 
