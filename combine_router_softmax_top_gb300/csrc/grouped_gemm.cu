@@ -8,7 +8,8 @@
 // One persistent kernel per call, one CTA per SM, warp-specialised:
 //   warp 0      TMA producer (4-stage ring of 48 KB A|B stages)
 //   warp 1      TMEM allocator + single-thread MMA issuer
-//   warps 2..5  epilogue: TMEM -> registers -> fused math -> global stores
+//   warps 2..9  epilogue: TMEM -> registers -> fused math -> coalesced global stores
+//               (two warps per TMEM lane quarter, each owning half the columns)
 // Tiles are 128 x 256 (one tcgen05.mma M=128, N=256, K=16 per step, 4 steps
 // per 64-wide K stage). The 512 TMEM columns hold two accumulators, so the
 // epilogue of one tile overlaps the MMAs of the next.
@@ -41,11 +42,12 @@ constexpr int kStages = 4;
 constexpr int kABytes = BM * BK * 2;   // 16 KB
 constexpr int kBBytes = BN * BK * 2;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
 constexpr int kTmemCols = 512;
 constexpr int kMaxE = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress -> give up
-constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + 1024;
+constexpr size_t kEpiStageBytes = 8 * 2048;  // one 32x32 bf16 staging buffer per epilogue warp
+constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + kEpiStageBytes + 1024;
 
 struct KParams {
   int E, H, F;
@@ -62,6 +64,10 @@ struct Mode {
   static constexpr bool kRagK = MODE == GEMM_WGRAD_W1 || MODE == GEMM_WGRAD_W2;
   static constexpr int kAMn = kRagK ? 1 : 0;
   static constexpr int kBMn = (MODE == GEMM_FC2_DGRAD || MODE == GEMM_FC1_DGRAD || kRagK) ? 1 : 0;
+  // CTAs per cluster. Wgrad tiles are short in K, so their operand reads
+  // through L2 dominate; 4 CTAs on consecutive M blocks of one (expert, N block)
+  // each load a quarter of the shared B tile and multicast it to all four.
+  static constexpr int kCS = kRagK ? 4 : 1;
   // reduction depth for the row-ragged modes
   __device__ static int kdim(const KParams& p) {
     return MODE == GEMM_FC1_FWD ? p.H : MODE == GEMM_FC2_FWD ? p.F
@@ -104,7 +110,8 @@ struct SmemCtl {
 };
 
 template <int MODE>
-__device__ __forceinline__ Tile tile_at(const KParams& p, const SmemCtl& c, int tile, int& cursor) {
+__device__ __forceinline__ Tile tile_at(const KParams& p, const SmemCtl& c, int tile, int& cursor,
+                                       uint32_t rank = 0) {
   while (c.tstart[cursor + 1] <= tile) ++cursor;
   Tile t;
   t.e = cursor;
@@ -112,9 +119,11 @@ __device__ __forceinline__ Tile tile_at(const KParams& p, const SmemCtl& c, int 
   const int cnt = c.off[t.e + 1] - t.row0;
   const int local = tile - c.tstart[t.e];
   if (Mode<MODE>::kRagK) {
-    const int mt = (Mode<MODE>::wg_mdim(p) + BM - 1) / BM;
-    t.m0 = (local % mt) * BM;
-    t.n0 = (local / mt) * BN;
+    // one cluster tile = kCS consecutive M blocks of one (expert, N block)
+    constexpr int cs = Mode<MODE>::kCS;
+    const int mg = ((Mode<MODE>::wg_mdim(p) + BM - 1) / BM + cs - 1) / cs;
+    t.m0 = ((local % mg) * cs + (int)rank) * BM;
+    t.n0 = (local / mg) * BN;
     t.rows = cnt;
     t.nk = (cnt + BK - 1) / BK;
   } else {
@@ -137,25 +146,55 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
-__device__ __forceinline__ void store32(bf16* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+// Writes a warp's 32 rows x 32 columns (thread i holds row i) to global memory
+// as bf16 with full-sector stores: the rows go through a 2 KB shared buffer,
+// then each store instruction covers 8 rows x 64 contiguous bytes. 16-byte
+// chunk c of row r sits at chunk c ^ ((r >> 1) & 3) of the row in the buffer,
+// which keeps both the row-wise writes and the transposed reads free of bank
+// conflicts. Rows >= valid_rows and a chunk with cols_ok == false are skipped.
+__device__ __forceinline__ void warp_store32(uint4* stage, const float* v, bf16* base, int ld,
+                                             int lane, int valid_rows, bool cols_ok) {
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    d[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                      pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-}
-
-__device__ __forceinline__ void load32(const bf16* src, float* v) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 u = s[q];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    stage[lane * 4 + (q ^ ((lane >> 1) & 3))] =
+        make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                   pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+  __syncwarp();
+  if (cols_ok) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
-      v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      const int row = i * 8 + (lane >> 2), c = lane & 3;
+      if (row < valid_rows)
+        reinterpret_cast<uint4*>(base + (size_t)row * ld)[c] = stage[row * 4 + (c ^ ((row >> 1) & 3))];
     }
+  }
+  __syncwarp();
+}
+
+// Element i (0..31) of 32 bf16 held as 4 x uint4.
+__device__ __forceinline__ float bf16_at(const uint4 (&u)[4], int i) {
+  const uint4& w = u[i >> 3];
+  const uint32_t word = ((i >> 1) & 3) == 0 ? w.x : ((i >> 1) & 3) == 1 ? w.y : ((i >> 1) & 3) == 2 ? w.z : w.w;
+  return __uint_as_float((i & 1) ? (word & 0xFFFF0000u) : (word << 16));
+}
+
+// Stores this warp's half of a plain fp32 accumulator tile (BN/64 chunks of 32
+// columns starting at chunk c0) as bf16; the TMEM load of the next chunk is in
+// flight while the current one is written out.
+__device__ __forceinline__ void store_chunks(uint4* stage, uint32_t tbase, int c0, bf16* slab,
+                                             int ld, int n0, int lane, int slab_rows) {
+  uint32_t va[32], vb[32];
+  ptx::tmem_ld_32x32b_x32(tbase + 32 * c0, va);
+  ptx::tmem_ld_wait(va);
+#pragma unroll
+  for (int i = 0; i < BN / 64; ++i) {
+    const int cc = c0 + i;
+    uint32_t(&cur)[32] = (i & 1) ? vb : va;
+    uint32_t(&nxt)[32] = (i & 1) ? va : vb;
+    if (i + 1 < BN / 64) ptx::tmem_ld_32x32b_x32(tbase + 32 * (cc + 1), nxt);
+    warp_store32(stage, reinterpret_cast<float*>(cur), slab + 32 * cc, ld, lane, slab_rows,
+                 n0 + 32 * cc < ld);
+    if (i + 1 < BN / 64) ptx::tmem_ld_wait(nxt);
   }
 }
 
@@ -180,11 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&ctl.full[s], 1);
-      ptx::mbar_init(&ctl.empty[s], 1);
+      ptx::mbar_init(&ctl.empty[s], M::kCS);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl.tmem_full[b], 1);
-      ptx::mbar_init(&ctl.tmem_empty[b], 128);
+      ptx::mbar_init(&ctl.tmem_empty[b], 256);
     }
     ptx::mbar_init(&ctl.tail, 1);
     ptx::mbar_init(&ctl.drain, 1);
@@ -204,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n = 0;
       if (e < E) {
         const int cnt = ctl.off[e + 1] - ctl.off[e];
-        if (M::kRagK) n = ((M::wg_mdim(p) + BM - 1) / BM) * M::ntiles(p);
+        if (M::kRagK)
+          n = (((M::wg_mdim(p) + BM - 1) / BM + M::kCS - 1) / M::kCS) * M::ntiles(p);
         else n = ((cnt + BM - 1) / BM) * M::ntiles(p);
         if (cnt < 0) n = 0;
       }
@@ -222,8 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // peers multicast into this CTA's shared memory and barriers: all must be
+  // initialised first
+  if (M::kCS > 1) ptx::cluster_sync();
   const int total = ctl.tstart[E];
   const uint32_t tmem_base = ctl.tmem_base;
+  const uint32_t crank = M::kCS > 1 ? ptx::cluster_ctarank() : 0;
+  const int first = M::kCS > 1 ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
+  const int stride = M::kCS > 1 ? (int)ptx::cluster_count_x() : (int)gridDim.x;
+  const uint16_t cmask = (uint16_t)((1u << M::kCS) - 1u);
 
   if (warp == 0) {
     // ================================================================ producer
@@ -234,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, cursor = 0;
     uint32_t phase = 0, tail_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const Tile t = tile_at<MODE>(p, ctl, tile, cursor);
+    for (int tile = first; tile < total && ok; tile += stride) {
+      const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
       for (int kt = 0; kt < t.nk; ++kt) {
         if (!ptx::mbar_wait(&ctl.empty[stage], phase ^ 1, &ctl.abort, kWaitLimitNs)) {
           if (lane == 0) flag_timeout(ctl, p.status, 1);
@@ -248,14 +295,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool tail = M::kRagK && (t.rows - k0 < BK);
         uint64_t* bar = tail ? &ctl.tail : &ctl.full[stage];
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(bar, kStageBytes);
           if (M::kRagK) {
+            // A: this CTA's own M block. B: slice i of the shared tile is loaded
+            // by cluster rank i % kCS and multicast to every CTA of the cluster,
+            // so full[stage] collects all 32 KB of B in every CTA. On the tail
+            // stage A goes to the tail barrier and full[stage] gets its arrival
+            // only after the zeroing below.
+            if (tail) {
+              ptx::mbar_arrive_expect_tx(&ctl.tail, kABytes);
+              ptx::mbar_expect_tx(&ctl.full[stage], kBBytes);
+            } else {
+              ptx::mbar_arrive_expect_tx(&ctl.full[stage], kStageBytes);
+            }
             const int r = t.row0 + k0;
             ptx::tma_load_2d(sA, &tmA, bar, t.m0, r);
             ptx::tma_load_2d(sA + 8192, &tmA, bar, t.m0 + 64, r);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ptx::tma_load_2d(sB + 8192 * i, &tmB, bar, t.n0 + 64 * i, r);
+            for (int i = 0; i < 4; ++i) {
+              if (M::kCS == 1)
+                ptx::tma_load_2d(sB + 8192 * i, &tmB, &ctl.full[stage], t.n0 + 64 * i, r);
+              else if (i % M::kCS == (int)crank)
+                ptx::tma_load_2d_multicast(sB + 8192 * i, &tmB, &ctl.full[stage], t.n0 + 64 * i,
+                                           r, cmask);
+            }
           } else {
+            ptx::mbar_arrive_expect_tx(bar, kStageBytes);
             ptx::tma_load_2d(sA, &tmA, bar, k0, t.row0 + t.m0);
             if (MODE == GEMM_FC1_FWD) {
               const int base = t.e * 2 * p.F;
@@ -306,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, cursor = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = tile_at<MODE>(p, ctl, tile, cursor);
+      for (int tile = first; tile < total && ok; tile += stride) {
+        const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
         if (t.nk == 0) continue;
         if (!ptx::mbar_wait(&ctl.tmem_empty[acc], acc_phase ^ 1, &ctl.abort, kWaitLimitNs)) {
           flag_timeout(ctl, p.status, 3);
@@ -330,7 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk)
             ptx::umma_bf16(d_tmem, adesc + (uint64_t)(kk * a_adv), bdesc + (uint64_t)(kk * b_adv),
                            idesc, (kt | kk) != 0);
-          ptx::umma_commit(&ctl.empty[stage]);
+          // the stage is free once every CTA that received the multicast B
+          // slices has consumed it
+          if (M::kCS > 1) ptx::umma_commit_multicast(&ctl.empty[stage], cmask);
+          else ptx::umma_commit(&ctl.empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -354,24 +421,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ================================================================ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // 8 warps: warp w reads TMEM lane quarter w % 4 (hardware rule) and owns
+    // half hf of the tile's columns.
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int hf = ew >> 2;
     const int r = q * 32 + lane;
+    uint4* stage = reinterpret_cast<uint4*>(smem + kStages * kStageBytes) + ew * 128;
     int cursor = 0, acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = tile_at<MODE>(p, ctl, tile, cursor);
+    for (int tile = first; tile < total; tile += stride) {
+      const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
+      const int c0 = hf * (BN / 64);  // first 32-column chunk of this warp's half
       if (M::kRagK) {
         const int Md = M::wg_mdim(p), Nd = M::wg_ndim(p);
-        const int row = t.m0 + r;
         bf16* outp = (MODE == GEMM_WGRAD_W1 ? p.out0 : p.out1) + (size_t)t.e * Md * Nd;
+        const int slab_rows = min(32, Md - (t.m0 + q * 32));
+        bf16* slab = outp + (size_t)(t.m0 + q * 32) * Nd;
         if (t.nk == 0) {
-          if (row < Md) {
-            float z[32];
+          float z[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) z[i] = 0.f;
-            for (int cc = 0; cc < BN / 32; ++cc)
-              if (t.n0 + 32 * cc < Nd) store32(outp + (size_t)row * Nd + t.n0 + 32 * cc, z);
-          }
+          for (int i = 0; i < 32; ++i) z[i] = 0.f;
+          for (int cc = c0; cc < c0 + BN / 64; ++cc)
+            warp_store32(stage, z, slab + t.n0 + 32 * cc, Nd, lane, slab_rows, t.n0 + 32 * cc < Nd);
           continue;
         }
         if (!ptx::mbar_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
@@ -380,13 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
-          ptx::tmem_ld_wait();
-          if (row < Md && t.n0 + 32 * cc < Nd)
-            store32(outp + (size_t)row * Nd + t.n0 + 32 * cc, reinterpret_cast<float*>(v));
-        }
+        store_chunks(stage, tbase, c0, slab + t.n0, Nd, t.n0, lane, slab_rows);
       } else {
         if (!ptx::mbar_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
           if (lane == 0) flag_timeout(ctl, p.status, 5);
@@ -396,61 +462,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
         const bool row_ok = r < t.rows;
         const size_t grow = (size_t)t.row0 + t.m0 + r;
+        // this warp's 32-row slab of the tile, for the coalesced stores
+        const size_t slab_row0 = (size_t)t.row0 + t.m0 + q * 32;
+        const int slab_rows = min(32, t.rows - q * 32);
         if (MODE == GEMM_FC1_FWD) {
-          // columns 0..127: gate f0.., columns 128..255: up f0..
-          for (int cc = 0; cc < 4; ++cc) {
+          // columns 0..127: gate f0.., columns 128..255: up f0..; this half: 2 chunks
+          for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
             uint32_t g[32], u[32];
             ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, g);
             ptx::tmem_ld_32x32b_x32(tbase + 128 + 32 * cc, u);
-            ptx::tmem_ld_wait();
+            ptx::tmem_ld_wait(g, u);
             const int f = t.n0 + 32 * cc;
-            if (row_ok && f < p.F) {
-              float ag[32], au[32], hv[32];
+            const bool cols_ok = f < p.F;
+            // round gate/up to bf16 in place, then h from the rounded values
+            float* ag = reinterpret_cast<float*>(g);
+            float* au = reinterpret_cast<float*>(u);
+            float hv[32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                ag[i] = round_bf16(__uint_as_float(g[i]));
-                au[i] = round_bf16(__uint_as_float(u[i]));
-                hv[i] = ag[i] / (1.f + __expf(-ag[i])) * au[i];
-              }
-              bf16* arow = p.out0 + grow * (size_t)(2 * p.F);
-              store32(arow + f, ag);
-              store32(arow + p.F + f, au);
-              store32(p.out1 + grow * (size_t)p.F + f, hv);
+            for (int i = 0; i < 32; ++i) {
+              ag[i] = round_bf16(ag[i]);
+              au[i] = round_bf16(au[i]);
+              hv[i] = ag[i] / (1.f + __expf(-ag[i])) * au[i];
             }
+            bf16* abase = p.out0 + slab_row0 * (size_t)(2 * p.F);
+            warp_store32(stage, ag, abase + f, 2 * p.F, lane, slab_rows, cols_ok);
+            warp_store32(stage, au, abase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
+            warp_store32(stage, hv, p.out1 + slab_row0 * (size_t)p.F + f, p.F, lane, slab_rows,
+                         cols_ok);
           }
         } else if (MODE == GEMM_FC2_DGRAD) {
-          for (int cc = 0; cc < BN / 32; ++cc) {
+          const bf16* arow = p.aux + grow * (size_t)(2 * p.F);
+          bf16* dbase = p.out0 + slab_row0 * (size_t)(2 * p.F);
+          // the saved pre-activation (gate and up) of each chunk
+          uint4 gc[4], uc[4];
+          auto fetch = [&](int f, uint4 (&g)[4], uint4 (&u)[4]) {
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              g[k2] = make_uint4(0, 0, 0, 0);
+              u[k2] = make_uint4(0, 0, 0, 0);
+            }
+            if (row_ok && f < p.F) {
+#pragma unroll
+              for (int k2 = 0; k2 < 4; ++k2) {
+                g[k2] = reinterpret_cast<const uint4*>(arow + f)[k2];
+                u[k2] = reinterpret_cast<const uint4*>(arow + p.F + f)[k2];
+              }
+            }
+          };
+#pragma unroll 1
+          for (int cc = c0; cc < c0 + BN / 64; ++cc) {
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
-            ptx::tmem_ld_wait();
+            fetch(t.n0 + 32 * cc, gc, uc);  // in flight together with the TMEM load
+            ptx::tmem_ld_wait(v);
             const int f = t.n0 + 32 * cc;
-            if (row_ok && f < p.F) {
-              const bf16* arow = p.aux + grow * (size_t)(2 * p.F);
-              float ag[32], au[32], dg[32], du[32];
-              load32(arow + f, ag);
-              load32(arow + p.F + f, au);
+            const bool cols_ok = f < p.F;
+            float out[32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float dh = __uint_as_float(v[i]);
-                const float s = 1.f / (1.f + __expf(-ag[i]));
-                du[i] = dh * ag[i] * s;
-                dg[i] = dh * au[i] * s * (1.f + ag[i] * (1.f - s));
-              }
-              bf16* drow = p.out0 + grow * (size_t)(2 * p.F);
-              store32(drow + f, dg);
-              store32(drow + p.F + f, du);
+            for (int i = 0; i < 32; ++i) {  // da_up = dh * silu(a_g)
+              const float ag = bf16_at(gc, i);
+              out[i] = __uint_as_float(v[i]) * ag / (1.f + __expf(-ag));
             }
+            warp_store32(stage, out, dbase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {  // da_gate = dh * a_u * silu'(a_g)
+              const float ag = bf16_at(gc, i);
+              const float sg = 1.f / (1.f + __expf(-ag));
+              out[i] = __uint_as_float(v[i]) * bf16_at(uc, i) * sg * (1.f + ag * (1.f - sg));
+            }
+            warp_store32(stage, out, dbase + f, 2 * p.F, lane, slab_rows, cols_ok);
           }
         } else {
           const int Nd = MODE == GEMM_FC2_FWD || MODE == GEMM_FC1_DGRAD ? p.H : p.F;
-          for (int cc = 0; cc < BN / 32; ++cc) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
-            ptx::tmem_ld_wait();
-            const int n = t.n0 + 32 * cc;
-            if (row_ok && n < Nd)
-              store32(p.out0 + grow * (size_t)Nd + n, reinterpret_cast<float*>(v));
-          }
+          store_chunks(stage, tbase, c0, p.out0 + slab_row0 * (size_t)Nd + t.n0, Nd, t.n0, lane,
+                       slab_rows);
         }
       }
       ptx::tc_fence_before();
@@ -465,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // peers may still arrive on this CTA's barriers until they are done
+  if (M::kCS > 1) ptx::cluster_sync();
   if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
 }
 
@@ -512,19 +599,57 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
 template <int MODE>
 moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
                          cudaStream_t st) {
+  constexpr int cs = Mode<MODE>::kCS;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+    if (attr_err == cudaSuccess && cs > 1) {
+      // how many clusters of cs CTAs (one per SM) can be resident at once
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = cs;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(device_sm_count() / cs * cs);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kDynSmem;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_kernel<MODE>, &cfg);
+    }
   });
   if (attr_err != cudaSuccess) {
-    set_error("cudaFuncSetAttribute failed: %s", cudaGetErrorString(attr_err));
+    set_error("kernel attribute setup failed: %s", cudaGetErrorString(attr_err));
     return MOE_ERR_CUDA;
   }
-  {
-    LaunchScope _ls(K_GEMM_FC1_FWD + MODE, st);
+  LaunchScope _ls(K_GEMM_FC1_FWD + MODE, st);
+  if (cs == 1) {
     grouped_gemm_kernel<MODE><<<grid, kThreads, kDynSmem, st>>>(a, b, p);
+    return check_launch("grouped_gemm_kernel");
+  }
+  int clusters = (grid + cs - 1) / cs;
+  if (max_clusters > 0 && clusters > max_clusters) clusters = max_clusters;
+  if (clusters < 1) clusters = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = cs;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(clusters * cs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kDynSmem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, b, p);
+  if (e != cudaSuccess) {
+    set_error("grouped_gemm_kernel cluster launch: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
   }
   return check_launch("grouped_gemm_kernel");
 }
@@ -567,11 +692,11 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
       break;
     case GEMM_WGRAD_W1:
       ok = make_map(&ma, g.A, N, 2 * F, 64) && make_map(&mb, g.B, N, H, 64);
-      ntile_bound = (long long)E * ((2 * F + BM - 1) / BM) * ((H + BN - 1) / BN);
+      ntile_bound = (long long)E * (((2 * F + BM - 1) / BM + 3) / 4 * 4) * ((H + BN - 1) / BN);
       break;
     case GEMM_WGRAD_W2:
       ok = make_map(&ma, g.A, N, H, 64) && make_map(&mb, g.B, N, F, 64);
-      ntile_bound = (long long)E * ((H + BM - 1) / BM) * ((F + BN - 1) / BN);
+      ntile_bound = (long long)E * (((H + BM - 1) / BM + 3) / 4 * 4) * ((F + BN - 1) / BN);
       break;
     default:
       set_error("unknown grouped GEMM mode %d", g.mode);

@@ -135,27 +135,46 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
   float dot[KMAX];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) dot[j] = 0.f;
+  int sj[KMAX];
+  float gj[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    sj[j] = -1;
+    gj[j] = 0.f;
+    if (active && j < k) {
+      const int s = slot[(size_t)m.t * k + j];
+      sj[j] = (s >= 0 && s < N) ? s : -1;
+      gj[j] = gates[(size_t)m.t * k + j];
+    }
+  }
   if (active) {
     for (int c = m.sub; c < cpr; c += tpr) {
       float fy[8];
       unpack8(__ldg(reinterpret_cast<const uint4*>(dy + (size_t)m.t * H) + c), fy);
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
-          const int s = slot[(size_t)m.t * k + j];
-          const float g = gates[(size_t)m.t * k + j];
-          if (s >= 0 && s < N) {
-            float fo[8];
-            unpack8(__ldcs(reinterpret_cast<const uint4*>(o + (size_t)s * H) + c), fo);
-            float prod[8];
+      for (int j0 = 0; j0 < KMAX; j0 += kMaxKBatch) {  // 8 rows of o in flight
+        uint4 ov[kMaxKBatch];
+#pragma unroll
+        for (int u = 0; u < kMaxKBatch; ++u) {
+          const int j = j0 + u;
+          ov[u] = (j < KMAX && sj[j < KMAX ? j : 0] >= 0 && j < k)
+                      ? __ldcs(reinterpret_cast<const uint4*>(o + (size_t)sj[j] * H) + c)
+                      : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kMaxKBatch; ++u) {
+          const int j = j0 + u;
+          if (j < KMAX && j < k && sj[j] >= 0) {
+            float fo[8], prod[8];
+            unpack8(ov[u], fo);
             float d = 0.f;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               d = fmaf(fy[q], fo[q], d);
-              prod[q] = g * fy[q];
+              prod[q] = gj[j] * fy[q];
             }
             dot[j] += d;
-            __stcs(reinterpret_cast<uint4*>(d_o + (size_t)s * H) + c, pack8(prod));
+            __stcs(reinterpret_cast<uint4*>(d_o + (size_t)sj[j] * H) + c, pack8(prod));
           }
         }
       }

@@ -13,91 +13,125 @@ namespace moe {
 
 namespace {
 
-constexpr int kRouteTok = 32;   // tokens per CTA (one per lane)
+constexpr int kRouteTok = 64;   // tokens per CTA: lane owns tokens lane and lane + 32
 constexpr int kRouteEpw = 8;    // experts per warp
-constexpr int kRouteHc = 64;    // hidden elements per shared-memory chunk
-constexpr int kRouteXPitch = kRouteHc + 4;  // floats; 272-byte rows keep LDS.128 conflict-free
+constexpr int kRouteHc = 32;    // hidden elements per chunk
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }
 
-// z[t, e] for a tile of 32 tokens x (warps * 8) experts. Lane <-> token,
-// warp <-> 8 experts. Every accumulator runs over h = 0..H-1 in ascending order
-// with one fmaf per step; since a bf16*bf16 product is exact in fp32, each step
-// is a single fp32 rounding of (acc + x*w), the order both sides of the parity
-// check use.
-__global__ void __launch_bounds__(256) route_logits_kernel(const bf16* __restrict__ x,
-                                                           const bf16* __restrict__ w_r,
-                                                           const float* __restrict__ bias,
-                                                           float* __restrict__ z, int T, int H,
-                                                           int E) {
-  extern __shared__ float4 smem_f4[];
-  float* sm = reinterpret_cast<float*>(smem_f4);
-  const int nwarps = blockDim.x >> 5;
-  const int eb = nwarps * kRouteEpw;  // experts in this CTA
-  float* xs = sm;                                   // [32][kRouteXPitch]
-  float* ws = sm + kRouteTok * kRouteXPitch;        // [eb][kRouteHc]
+__device__ __forceinline__ void unpack8_f32(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    f[2 * q] = __uint_as_float(w[q] << 16);
+    f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+  }
+}
+
+// z[t, e] for a tile of 64 tokens x (NW * 8) experts: lane owns tokens lane and
+// lane+32, warp owns 8 experts, 16 accumulators per thread. Every accumulator
+// runs over h = 0..H-1 in ascending order with one fmaf per step; since a
+// bf16*bf16 product is exact in fp32, each step is a single fp32 rounding of
+// (acc + x*w), the order both sides of the parity check use.
+// Each lane keeps its two tokens' 32-wide x slices in registers (loaded straight
+// from global memory, the next chunk while the current one is consumed); the
+// w_r chunk is staged as fp32 in shared memory (double buffered) and read with
+// warp-uniform broadcast loads, so shared memory serves 1 wavefront per 16
+// FMAs and the loop is bound by the FMA pipe.
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __restrict__ x,
+                                                               const bf16* __restrict__ w_r,
+                                                               const float* __restrict__ bias,
+                                                               float* __restrict__ z, int T,
+                                                               int H, int E) {
+  constexpr int kThreads = NW * 32;
+  constexpr int eb = NW * kRouteEpw;  // experts in this CTA
+  static_assert(eb * (kRouteHc / 8) == kThreads, "one 16-byte w_r piece per thread");
+  __shared__ __align__(16) float ws[2][eb][kRouteHc];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kRouteTok;
   const int e0 = blockIdx.y * eb;
+  const int ta = t0 + lane, tb = t0 + lane + 32;
 
-  float acc[kRouteEpw];
+  float acc[2][kRouteEpw];
 #pragma unroll
-  for (int i = 0; i < kRouteEpw; ++i) acc[i] = 0.f;
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int i = 0; i < kRouteEpw; ++i) acc[u][i] = 0.f;
 
-  const uint16_t* xb = reinterpret_cast<const uint16_t*>(x);
-  const uint16_t* wb = reinterpret_cast<const uint16_t*>(w_r);
-  for (int h0 = 0; h0 < H; h0 += kRouteHc) {
-    // stage x[t0..t0+31][h0..h0+63] and w_r[e0..e0+eb-1][h0..h0+63] as fp32
-    for (int i = threadIdx.x; i < kRouteTok * (kRouteHc / 8); i += blockDim.x) {
-      const int r = i / (kRouteHc / 8), c = (i % (kRouteHc / 8)) * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t0 + r < T) v = __ldg(reinterpret_cast<const uint4*>(xb + (size_t)(t0 + r) * H + h0 + c));
-      float* dst = xs + r * kRouteXPitch + c;
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const uint4* xa = reinterpret_cast<const uint4*>(x + (size_t)min(ta, T - 1) * H);
+  const uint4* xb = reinterpret_cast<const uint4*>(x + (size_t)min(tb, T - 1) * H);
+  const int wr_row = threadIdx.x / (kRouteHc / 8), wr_col = (threadIdx.x % (kRouteHc / 8)) * 8;
+  const bool w_ok = e0 + wr_row < E;
+  const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)(w_ok ? e0 + wr_row : 0) * H);
+
+  uint4 xcur[2][4], xnext[2][4], wnext;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        dst[2 * q] = bf16_bits_to_f32(w[q] & 0xFFFFu);
-        dst[2 * q + 1] = bf16_bits_to_f32(w[q] >> 16);
-      }
-    }
-    for (int i = threadIdx.x; i < eb * (kRouteHc / 8); i += blockDim.x) {
-      const int r = i / (kRouteHc / 8), c = (i % (kRouteHc / 8)) * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (e0 + r < E) v = __ldg(reinterpret_cast<const uint4*>(wb + (size_t)(e0 + r) * H + h0 + c));
-      float* dst = ws + r * kRouteHc + c;
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        dst[2 * q] = bf16_bits_to_f32(w[q] & 0xFFFFu);
-        dst[2 * q + 1] = bf16_bits_to_f32(w[q] >> 16);
-      }
-    }
-    __syncthreads();
-    const float* xr = xs + lane * kRouteXPitch;
-    const float* wr = ws + warp * kRouteEpw * kRouteHc;
-#pragma unroll 4
-    for (int h = 0; h < kRouteHc; h += 4) {
-      const float4 xv = *reinterpret_cast<const float4*>(xr + h);
-#pragma unroll
-      for (int i = 0; i < kRouteEpw; ++i) {
-        const float4 wv = *reinterpret_cast<const float4*>(wr + i * kRouteHc + h);  // broadcast
-        acc[i] = fmaf(xv.x, wv.x, acc[i]);
-        acc[i] = fmaf(xv.y, wv.y, acc[i]);
-        acc[i] = fmaf(xv.z, wv.z, acc[i]);
-        acc[i] = fmaf(xv.w, wv.w, acc[i]);
-      }
-    }
-    __syncthreads();
+  for (int q = 0; q < 4; ++q) {
+    xcur[0][q] = __ldg(xa + q);
+    xcur[1][q] = __ldg(xb + q);
   }
-  const int t = t0 + lane;
-  if (t < T) {
+  wnext = w_ok ? __ldg(wrow + wr_col / 8) : make_uint4(0, 0, 0, 0);
+  const int nchunks = H / kRouteHc;
+  for (int ch = 0; ch < nchunks; ++ch) {
+    {
+      float f[8];
+      unpack8_f32(wnext, f);
+      float4* dst = reinterpret_cast<float4*>(&ws[ch & 1][wr_row][wr_col]);
+      dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+      dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    __syncthreads();
+    if (ch + 1 < nchunks) {
+      const int o = (ch + 1) * (kRouteHc / 8);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xnext[0][q] = __ldg(xa + o + q);
+        xnext[1][q] = __ldg(xb + o + q);
+      }
+      wnext = w_ok ? __ldg(wrow + o + wr_col / 8) : make_uint4(0, 0, 0, 0);
+    }
+    const float* wb = &ws[ch & 1][warp * kRouteEpw][0];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // 8 hidden elements per step
+      float x0[8], x1[8];
+      unpack8_f32(xcur[0][q], x0);
+      unpack8_f32(xcur[1][q], x1);
+#pragma unroll
+      for (int hh = 0; hh < 8; hh += 4) {
+#pragma unroll
+        for (int i = 0; i < kRouteEpw; ++i) {
+          const float4 wv = *reinterpret_cast<const float4*>(wb + i * kRouteHc + q * 8 + hh);
+          acc[0][i] = fmaf(x0[hh + 0], wv.x, acc[0][i]);
+          acc[1][i] = fmaf(x1[hh + 0], wv.x, acc[1][i]);
+          acc[0][i] = fmaf(x0[hh + 1], wv.y, acc[0][i]);
+          acc[1][i] = fmaf(x1[hh + 1], wv.y, acc[1][i]);
+          acc[0][i] = fmaf(x0[hh + 2], wv.z, acc[0][i]);
+          acc[1][i] = fmaf(x1[hh + 2], wv.z, acc[1][i]);
+          acc[0][i] = fmaf(x0[hh + 3], wv.w, acc[0][i]);
+          acc[1][i] = fmaf(x1[hh + 3], wv.w, acc[1][i]);
+        }
+      }
+    }
+    if (ch + 1 < nchunks) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xcur[0][q] = xnext[0][q];
+        xcur[1][q] = xnext[1][q];
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int t = u ? tb : ta;
+    if (t >= T) continue;
 #pragma unroll
     for (int i = 0; i < kRouteEpw; ++i) {
       const int e = e0 + warp * kRouteEpw + i;
       if (e < E) {
-        float v = acc[i];
+        float v = acc[u][i];
         if (bias) v = __fadd_rn(v, __ldg(bias + e));
         z[(size_t)t * E + e] = v;
       }
@@ -186,6 +220,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 // One 256-thread block per group of tokens; each thread owns 16-byte chunks of
 // one token row. dz_j = g_j (dg_j - <g, dg>) on the chosen set;
 // dx = bf16(dx32 + sum_j dz_j * w_r[i_j]).
+template <int KMAX>
 __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     const float* __restrict__ dgates, const float* __restrict__ gates,
     const int32_t* __restrict__ idx, const bf16* __restrict__ w_r, const float* __restrict__ dx32,
@@ -195,24 +230,51 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
   const int t = blockIdx.x * rpb + threadIdx.x / tpr;
   const int sub = threadIdx.x % tpr;
   if (t >= T) return;
+  // dz and the expert of each slot, once per thread (the token's k values are
+  // shared by its threads through L1)
   float inner = 0.f;
-  for (int j = 0; j < k; ++j) inner = fmaf(gates[(size_t)t * k + j], dgates[(size_t)t * k + j], inner);
+  float dzj[KMAX];
+  int ej[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j < k) inner = fmaf(gates[(size_t)t * k + j], dgates[(size_t)t * k + j], inner);
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    dzj[j] = 0.f;
+    ej[j] = -1;
+    if (j < k) {
+      const int e = idx[(size_t)t * k + j];
+      dzj[j] = gates[(size_t)t * k + j] * (dgates[(size_t)t * k + j] - inner);
+      ej[j] = (unsigned)e < (unsigned)E ? e : -1;
+    }
+  }
   const int cpr = H / 8;
   for (int c = sub; c < cpr; c += tpr) {
     const float4* src = reinterpret_cast<const float4*>(dx32 + (size_t)t * H + c * 8);
-    float4 p0 = src[0], p1 = src[1];
+    const float4 p0 = src[0], p1 = src[1];
     float acc[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-    for (int j = 0; j < k; ++j) {
-      const int e = idx[(size_t)t * k + j];
-      if ((unsigned)e >= (unsigned)E) continue;
-      const float g = gates[(size_t)t * k + j];
-      const float dzj = g * (dgates[(size_t)t * k + j] - inner);
-      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)e * H + c * 8));
-      const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[2 * q] = fmaf(dzj, bf16_bits_to_f32(w[q] & 0xFFFFu), acc[2 * q]);
-        acc[2 * q + 1] = fmaf(dzj, bf16_bits_to_f32(w[q] >> 16), acc[2 * q + 1]);
+    for (int j0 = 0; j0 < KMAX; j0 += 8) {  // 8 w_r rows in flight at a time
+      uint4 wv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        wv[u] = (j < k && ej[j] >= 0)
+                    ? __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)ej[j] * H + c * 8))
+                    : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        if (j < k) {
+          const uint32_t w[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[2 * q] = fmaf(dzj[j], bf16_bits_to_f32(w[q] & 0xFFFFu), acc[2 * q]);
+            acc[2 * q + 1] = fmaf(dzj[j], bf16_bits_to_f32(w[q] >> 16), acc[2 * q + 1]);
+          }
+        }
       }
     }
     uint4 out;
@@ -225,10 +287,12 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     *reinterpret_cast<uint4*>(dx + (size_t)t * H + c * 8) = out;
   }
   if (sub == 0) {
-    for (int j = 0; j < k; ++j) {
-      const float g = gates[(size_t)t * k + j];
-      dz[(size_t)t * k + j] = g * (dgates[(size_t)t * k + j] - inner);
-      if ((unsigned)idx[(size_t)t * k + j] >= (unsigned)E) atomicAdd(status + ST_BAD_INDEX, 1);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        dz[(size_t)t * k + j] = dzj[j];
+        if (ej[j] < 0) atomicAdd(status + ST_BAD_INDEX, 1);
+      }
     }
   }
 }
@@ -273,28 +337,49 @@ __device__ int find_chunk(const int32_t* __restrict__ off, int E, int chunk, int
 }
 
 // Pass A: partial[chunk][h] = sum over the chunk's rows s (ascending) of
-// dz[row_src[s]] * x[row_src[s] div k][h].
+// dz[row_src[s]] * x[row_src[s] div k][h]. The chunk's sources and weights are
+// staged in shared memory first, so each thread then has 8 independent x-row
+// loads in flight instead of a chain of dependent loads per row.
 __global__ void __launch_bounds__(256) route_bwd_dwr_partial_kernel(
     const int32_t* __restrict__ off, const int32_t* __restrict__ row_src,
     const float* __restrict__ dz, const bf16* __restrict__ x, float* __restrict__ part, int T,
     int H, int E, int k, int* status) {
   extern __shared__ int s_prefix[];
+  __shared__ int s_tok[kRouteBwdRowsPerChunk];
+  __shared__ float s_w[kRouteBwdRowsPerChunk];
   int e, r0, r1;
   if (!find_chunk(off, E, blockIdx.x, &e, &r0, &r1, s_prefix)) return;
+  const long long N = (long long)T * k;
+  const int n = r1 - r0;
+  if ((int)threadIdx.x < n) {
+    const int src = row_src[r0 + threadIdx.x];
+    const bool ok = src >= 0 && src < N;
+    s_tok[threadIdx.x] = ok ? src / k : -1;
+    s_w[threadIdx.x] = ok ? dz[src] : 0.f;
+  }
+  __syncthreads();
   const int c = blockIdx.y * blockDim.x + threadIdx.x;  // 16-byte chunk of the row
   if (c * 8 >= H) return;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  const long long N = (long long)T * k;
-  for (int s = r0; s < r1; ++s) {
-    const int src = row_src[s];
-    if (src < 0 || src >= N) continue;
-    const float w = dz[src];
-    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(src / k) * H + c * 8));
-    const uint32_t q4[4] = {xv.x, xv.y, xv.z, xv.w};
+  for (int s0 = 0; s0 < n; s0 += 8) {
+    uint4 v[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      acc[2 * q] = fmaf(w, bf16_bits_to_f32(q4[q] & 0xFFFFu), acc[2 * q]);
-      acc[2 * q + 1] = fmaf(w, bf16_bits_to_f32(q4[q] >> 16), acc[2 * q + 1]);
+    for (int u = 0; u < 8; ++u) {
+      const int tok = s0 + u < n ? s_tok[s0 + u] : -1;
+      v[u] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H) + c)
+                      : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (s0 + u < n) {
+        const float w = s_w[s0 + u];
+        const uint32_t q4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = fmaf(w, bf16_bits_to_f32(q4[q] & 0xFFFFu), acc[2 * q]);
+          acc[2 * q + 1] = fmaf(w, bf16_bits_to_f32(q4[q] >> 16), acc[2 * q + 1]);
+        }
+      }
     }
   }
   float4* dst = reinterpret_cast<float4*>(part + (size_t)blockIdx.x * H + c * 8);
@@ -336,13 +421,18 @@ moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* 
                           int* status, cudaStream_t st) {
   (void)status;
   if (d.T == 0) return MOE_OK;
-  const int eb = d.E >= 64 ? 64 : ((d.E + kRouteEpw - 1) / kRouteEpw) * kRouteEpw;
-  const int threads = (eb / kRouteEpw) * 32;
-  const size_t smem = (size_t)(kRouteTok * kRouteXPitch + eb * kRouteHc) * sizeof(float);
+  // warps per CTA: 4 (32 experts) unless E is smaller; 64 tokens per CTA
+  const int nw = d.E > 16 ? 4 : d.E > 8 ? 2 : 1;
+  const int eb = nw * kRouteEpw;
   dim3 grid(ceil_div(d.T, kRouteTok), ceil_div(d.E, eb));
   {
     LaunchScope _ls(K_ROUTE_LOGITS, st);
-    route_logits_kernel<<<grid, threads, smem, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+    if (nw == 4)
+      route_logits_kernel<4><<<grid, 128, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+    else if (nw == 2)
+      route_logits_kernel<2><<<grid, 64, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+    else
+      route_logits_kernel<1><<<grid, 32, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
   }
   moe_status_t s = check_launch("route_logits_kernel");
   if (s != MOE_OK) return s;
@@ -384,8 +474,19 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
   if (d.T > 0) {
     {
       LaunchScope _ls(K_ROUTE_BWD_DX, st);
-      route_bwd_dx_kernel<<<ceil_div(d.T, rpb), 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz,
-                                                              d.T, d.H, d.E, d.k, tpr, status);
+      const dim3 g(ceil_div(d.T, rpb));
+      if (d.k <= 4)
+        route_bwd_dx_kernel<4><<<g, 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz, d.T, d.H,
+                                                  d.E, d.k, tpr, status);
+      else if (d.k <= 8)
+        route_bwd_dx_kernel<8><<<g, 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz, d.T, d.H,
+                                                  d.E, d.k, tpr, status);
+      else if (d.k <= 16)
+        route_bwd_dx_kernel<16><<<g, 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz, d.T, d.H,
+                                                   d.E, d.k, tpr, status);
+      else
+        route_bwd_dx_kernel<32><<<g, 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz, d.T, d.H,
+                                                   d.E, d.k, tpr, status);
     }
     moe_status_t s = check_launch("route_bwd_dx_kernel");
     if (s != MOE_OK) return s;
