@@ -37,17 +37,14 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 128, BN = 256, BK = 64;  // BN: widest tile (per-mode width is kBN)
 constexpr int kStages = 4;
 constexpr int kABytes = BM * BK * 2;   // 16 KB
-constexpr int kBBytes = BN * BK * 2;   // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
+constexpr int kAccCols = 256;          // TMEM columns per accumulator buffer
 constexpr int kTmemCols = 512;
 constexpr int kMaxE = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress -> give up
 constexpr size_t kEpiStageBytes = 8 * 2048;  // one 32x32 bf16 staging buffer per epilogue warp
-constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + kEpiStageBytes + 1024;
 
 struct KParams {
   int E, H, F;
@@ -68,6 +65,17 @@ struct Mode {
   // through L2 dominate; 4 CTAs on consecutive M blocks of one (expert, N block)
   // each load a quarter of the shared B tile and multicast it to all four.
   static constexpr int kCS = kRagK ? 4 : 1;
+  // Tile width. The FC2 dgrad epilogue needs the tile's saved pre-activation
+  // (gate and up) next to the accumulator; at 128 columns that slab (64 KB) is
+  // TMA-loaded into shared memory by a dedicated warp ahead of the epilogue.
+  static constexpr bool kAux = MODE == GEMM_FC2_DGRAD;
+  static constexpr int kBN = kAux ? 128 : 256;
+  static constexpr int kBBytes = kBN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kAuxBytes = kAux ? 4 * 16384 : 0;
+  static constexpr int kWarps = kAux ? 11 : 10;  // producer, MMA, 8 epilogue (+ aux loader)
+  static constexpr size_t kDynSmem =
+      (size_t)kStages * kStageBytes + kAuxBytes + kEpiStageBytes + 1024;
   // reduction depth for the row-ragged modes
   __device__ static int kdim(const KParams& p) {
     return MODE == GEMM_FC1_FWD ? p.H : MODE == GEMM_FC2_FWD ? p.F
@@ -78,7 +86,7 @@ struct Mode {
     switch (MODE) {
       case GEMM_FC1_FWD: return (p.F + 127) / 128;
       case GEMM_FC2_FWD: return (p.H + BN - 1) / BN;
-      case GEMM_FC2_DGRAD: return (p.F + BN - 1) / BN;
+      case GEMM_FC2_DGRAD: return (p.F + kBN - 1) / kBN;
       case GEMM_FC1_DGRAD: return (p.H + BN - 1) / BN;
       case GEMM_WGRAD_W1: return (p.H + BN - 1) / BN;
       default: return (p.F + BN - 1) / BN;
@@ -103,6 +111,8 @@ struct SmemCtl {
   uint64_t tmem_empty[2];
   uint64_t tail;
   uint64_t drain;
+  uint64_t aux_full;
+  uint64_t aux_empty;
   uint32_t tmem_base;
   int abort;
   int tstart[kMaxE + 1];
@@ -129,7 +139,7 @@ __device__ __forceinline__ Tile tile_at(const KParams& p, const SmemCtl& c, int 
   } else {
     const int mt = (cnt + BM - 1) / BM;
     t.m0 = (local % mt) * BM;
-    t.n0 = (local / mt) * (MODE == GEMM_FC1_FWD ? 128 : BN);
+    t.n0 = (local / mt) * (MODE == GEMM_FC1_FWD ? 128 : Mode<MODE>::kBN);
     t.rows = min(BM, cnt - t.m0);
     t.nk = Mode<MODE>::kdim(p) / BK;
   }
@@ -203,9 +213,10 @@ __device__ __forceinline__ float round_bf16(float x) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const KParams p) {
   using M = Mode<MODE>;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ SmemCtl ctl;
@@ -227,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(&ctl.tail, 1);
     ptx::mbar_init(&ctl.drain, 1);
+    ptx::mbar_init(&ctl.aux_full, 1);
+    ptx::mbar_init(&ctl.aux_empty, 256);
     ctl.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -289,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint8_t* sA = smem + stage * kStageBytes;
+        uint8_t* sA = smem + stage * M::kStageBytes;
         uint8_t* sB = sA + kABytes;
         const int k0 = kt * BK;
         const bool tail = M::kRagK && (t.rows - k0 < BK);
@@ -303,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // only after the zeroing below.
             if (tail) {
               ptx::mbar_arrive_expect_tx(&ctl.tail, kABytes);
-              ptx::mbar_expect_tx(&ctl.full[stage], kBBytes);
+              ptx::mbar_expect_tx(&ctl.full[stage], M::kBBytes);
             } else {
-              ptx::mbar_arrive_expect_tx(&ctl.full[stage], kStageBytes);
+              ptx::mbar_arrive_expect_tx(&ctl.full[stage], M::kStageBytes);
             }
             const int r = t.row0 + k0;
             ptx::tma_load_2d(sA, &tmA, bar, t.m0, r);
@@ -319,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            r, cmask);
             }
           } else {
-            ptx::mbar_arrive_expect_tx(bar, kStageBytes);
+            ptx::mbar_arrive_expect_tx(bar, M::kStageBytes);
             ptx::tma_load_2d(sA, &tmA, bar, k0, t.row0 + t.m0);
             if (MODE == GEMM_FC1_FWD) {
               const int base = t.e * 2 * p.F;
@@ -330,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               const int base = MODE == GEMM_FC2_DGRAD ? t.e * p.H : t.e * 2 * p.F;
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
+              for (int i = 0; i < M::kBN / 64; ++i)
                 ptx::tma_load_2d(sB + 8192 * i, &tmB, bar, t.n0 + 64 * i, base + k0);
             }
           }
@@ -363,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, M::kAMn, M::kBMn);
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, M::kBN, M::kAMn, M::kBMn);
       const uint32_t a_lbo = M::kAMn ? 8192 : 16, b_lbo = M::kBMn ? 8192 : 16;
       const uint32_t a_adv = M::kAMn ? (2048 >> 4) : (32 >> 4);
       const uint32_t b_adv = M::kBMn ? (2048 >> 4) : (32 >> 4);
@@ -378,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * kAccCols;
         for (int kt = 0; kt < t.nk; ++kt) {
           if (!ptx::mbar_wait(&ctl.full[stage], phase, &ctl.abort, kWaitLimitNs)) {
             flag_timeout(ctl, p.status, 4);
@@ -386,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a_addr = ptx::smem_u32(smem + stage * kStageBytes);
+          const uint32_t a_addr = ptx::smem_u32(smem + stage * M::kStageBytes);
           const uint32_t b_addr = a_addr + kABytes;
           const uint64_t adesc = ptx::sdesc_sw128(a_addr, a_lbo, 1024);
           const uint64_t bdesc = ptx::sdesc_sw128(b_addr, b_lbo, 1024);
@@ -419,6 +432,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (M::kAux && warp == 10) {
+    // ================================================================ aux loader
+    // Loads each tile's saved pre-activation slab once the epilogue has
+    // released the previous one.
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmC);
+      int cursor = 0;
+      uint32_t ph = 0;
+      for (int tile = first; tile < total; tile += stride) {
+        const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
+        if (!ptx::mbar_wait(&ctl.aux_empty, ph ^ 1, &ctl.abort, kWaitLimitNs)) {
+          flag_timeout(ctl, p.status, 7);
+          break;
+        }
+        ph ^= 1;
+        uint8_t* aux = smem + kStages * M::kStageBytes;
+        const int row = t.row0 + t.m0;
+        ptx::mbar_arrive_expect_tx(&ctl.aux_full, M::kAuxBytes);
+        ptx::tma_load_2d(aux, &tmC, &ctl.aux_full, t.n0, row);
+        ptx::tma_load_2d(aux + 16384, &tmC, &ctl.aux_full, t.n0 + 64, row);
+        ptx::tma_load_2d(aux + 2 * 16384, &tmC, &ctl.aux_full, p.F + t.n0, row);
+        ptx::tma_load_2d(aux + 3 * 16384, &tmC, &ctl.aux_full, p.F + t.n0 + 64, row);
+      }
+    }
+    __syncwarp();
   } else {
     // ================================================================ epilogue
     // 8 warps: warp w reads TMEM lane quarter w % 4 (hardware rule) and owns
@@ -427,12 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int hf = ew >> 2;
     const int r = q * 32 + lane;
-    uint4* stage = reinterpret_cast<uint4*>(smem + kStages * kStageBytes) + ew * 128;
+    uint4* stage = reinterpret_cast<uint4*>(smem + kStages * M::kStageBytes + M::kAuxBytes) + ew * 128;
     int cursor = 0, acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0, aux_phase = 0;
     for (int tile = first; tile < total; tile += stride) {
       const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
-      const int c0 = hf * (BN / 64);  // first 32-column chunk of this warp's half
+      const int c0 = hf * (M::kBN / 64);  // first 32-column chunk of this warp's half
       if (M::kRagK) {
         const int Md = M::wg_mdim(p), Nd = M::wg_ndim(p);
         bf16* outp = (MODE == GEMM_WGRAD_W1 ? p.out0 : p.out1) + (size_t)t.e * Md * Nd;
@@ -451,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
         store_chunks(stage, tbase, c0, slab + t.n0, Nd, t.n0, lane, slab_rows);
       } else {
         if (!ptx::mbar_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
@@ -459,9 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-        const bool row_ok = r < t.rows;
-        const size_t grow = (size_t)t.row0 + t.m0 + r;
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
         // this warp's 32-row slab of the tile, for the coalesced stores
         const size_t slab_row0 = (size_t)t.row0 + t.m0 + q * 32;
         const int slab_rows = min(32, t.rows - q * 32);
@@ -491,29 +527,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                          cols_ok);
           }
         } else if (MODE == GEMM_FC2_DGRAD) {
-          const bf16* arow = p.aux + grow * (size_t)(2 * p.F);
+          // the tile's pre-activation slab: 4 TMA boxes of 128 rows x 64 columns
+          // (gate n0.., gate n0+64.., up n0.., up n0+64..), 128-byte swizzled:
+          // 16-byte chunk j of row r sits at chunk j ^ (r & 7)
+          if (!ptx::mbar_wait(&ctl.aux_full, aux_phase, &ctl.abort, kWaitLimitNs)) {
+            if (lane == 0) flag_timeout(ctl, p.status, 6);
+            break;
+          }
+          aux_phase ^= 1;
+          const uint8_t* aux = smem + kStages * M::kStageBytes;
           bf16* dbase = p.out0 + slab_row0 * (size_t)(2 * p.F);
-          // the saved pre-activation (gate and up) of each chunk
-          uint4 gc[4], uc[4];
-          auto fetch = [&](int f, uint4 (&g)[4], uint4 (&u)[4]) {
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-              g[k2] = make_uint4(0, 0, 0, 0);
-              u[k2] = make_uint4(0, 0, 0, 0);
-            }
-            if (row_ok && f < p.F) {
-#pragma unroll
-              for (int k2 = 0; k2 < 4; ++k2) {
-                g[k2] = reinterpret_cast<const uint4*>(arow + f)[k2];
-                u[k2] = reinterpret_cast<const uint4*>(arow + p.F + f)[k2];
-              }
-            }
-          };
 #pragma unroll 1
-          for (int cc = c0; cc < c0 + BN / 64; ++cc) {
+          for (int cc = c0; cc < c0 + M::kBN / 64; ++cc) {
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
-            fetch(t.n0 + 32 * cc, gc, uc);  // in flight together with the TMEM load
+            const int box = cc >> 1, cb = (cc & 1) * 4;
+            uint4 gc[4], uc[4];
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const int off = r * 128 + (((cb + k2) ^ (r & 7)) * 16);
+              gc[k2] = *reinterpret_cast<const uint4*>(aux + box * 16384 + off);
+              uc[k2] = *reinterpret_cast<const uint4*>(aux + (2 + box) * 16384 + off);
+            }
             ptx::tmem_ld_wait(v);
             const int f = t.n0 + 32 * cc;
             const bool cols_ok = f < p.F;
@@ -532,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             warp_store32(stage, out, dbase + f, 2 * p.F, lane, slab_rows, cols_ok);
           }
+          ptx::mbar_arrive(&ctl.aux_empty);
         } else {
           const int Nd = MODE == GEMM_FC2_FWD || MODE == GEMM_FC1_DGRAD ? p.H : p.F;
           store_chunks(stage, tbase, c0, p.out0 + slab_row0 * (size_t)Nd + t.n0, Nd, t.n0, lane,
@@ -597,7 +633,8 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
 }
 
 template <int MODE>
-moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
+moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                         const KParams& p, int grid,
                          cudaStream_t st) {
   constexpr int cs = Mode<MODE>::kCS;
   static std::once_flag once;
@@ -605,7 +642,8 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KPara
   static int max_clusters = 0;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)Mode<MODE>::kDynSmem);
     if (attr_err == cudaSuccess && cs > 1) {
       // how many clusters of cs CTAs (one per SM) can be resident at once
       cudaLaunchConfig_t cfg = {};
@@ -615,8 +653,8 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KPara
       at[0].val.clusterDim.y = 1;
       at[0].val.clusterDim.z = 1;
       cfg.gridDim = dim3(device_sm_count() / cs * cs);
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = kDynSmem;
+      cfg.blockDim = dim3(Mode<MODE>::kWarps * 32);
+      cfg.dynamicSmemBytes = Mode<MODE>::kDynSmem;
       cfg.attrs = at;
       cfg.numAttrs = 1;
       attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_kernel<MODE>, &cfg);
@@ -628,7 +666,7 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KPara
   }
   LaunchScope _ls(K_GEMM_FC1_FWD + MODE, st);
   if (cs == 1) {
-    grouped_gemm_kernel<MODE><<<grid, kThreads, kDynSmem, st>>>(a, b, p);
+    grouped_gemm_kernel<MODE><<<grid, Mode<MODE>::kWarps * 32, Mode<MODE>::kDynSmem, st>>>(a, b, c, p);
     return check_launch("grouped_gemm_kernel");
   }
   int clusters = (grid + cs - 1) / cs;
@@ -641,12 +679,12 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KPara
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(clusters * cs);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kDynSmem;
+  cfg.blockDim = dim3(Mode<MODE>::kWarps * 32);
+  cfg.dynamicSmemBytes = Mode<MODE>::kDynSmem;
   cfg.stream = st;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, b, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, b, c, p);
   if (e != cudaSuccess) {
     set_error("grouped_gemm_kernel cluster launch: %s", cudaGetErrorString(e));
     return MOE_ERR_CUDA;
@@ -670,7 +708,7 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
     }
     return MOE_OK;
   }
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc;
   bool ok = true;
   long long ntile_bound = 0;  // upper bound on tiles, for the grid size
   switch (g.mode) {
@@ -683,8 +721,9 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
       ntile_bound = (N / BM + E) * ((H + BN - 1) / BN);
       break;
     case GEMM_FC2_DGRAD:
-      ok = make_map(&ma, g.A, N, H, 128) && make_map(&mb, g.B, (long long)E * H, F, 64);
-      ntile_bound = (N / BM + E) * ((F + BN - 1) / BN);
+      ok = make_map(&ma, g.A, N, H, 128) && make_map(&mb, g.B, (long long)E * H, F, 64) &&
+           make_map(&mc, g.aux, N, 2 * F, 128);
+      ntile_bound = (N / BM + E) * ((F + 127) / 128);
       break;
     case GEMM_FC1_DGRAD:
       ok = make_map(&ma, g.A, N, 2 * F, 128) && make_map(&mb, g.B, (long long)E * 2 * F, H, 64);
@@ -703,6 +742,7 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
       return MOE_ERR_INVALID_ARG;
   }
   if (!ok) return MOE_ERR_CUDA;
+  if (g.mode != GEMM_FC2_DGRAD) mc = ma;  // only FC2 dgrad reads a third tensor
   KParams p;
   p.E = E;
   p.H = H;
@@ -717,12 +757,12 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
   if (g.max_ctas > 0 && g.max_ctas < grid) grid = g.max_ctas;
   if (ntile_bound < grid) grid = (int)(ntile_bound > 0 ? ntile_bound : 1);
   switch (g.mode) {
-    case GEMM_FC1_FWD: return launch_mode<GEMM_FC1_FWD>(ma, mb, p, grid, st);
-    case GEMM_FC2_FWD: return launch_mode<GEMM_FC2_FWD>(ma, mb, p, grid, st);
-    case GEMM_FC2_DGRAD: return launch_mode<GEMM_FC2_DGRAD>(ma, mb, p, grid, st);
-    case GEMM_FC1_DGRAD: return launch_mode<GEMM_FC1_DGRAD>(ma, mb, p, grid, st);
-    case GEMM_WGRAD_W1: return launch_mode<GEMM_WGRAD_W1>(ma, mb, p, grid, st);
-    default: return launch_mode<GEMM_WGRAD_W2>(ma, mb, p, grid, st);
+    case GEMM_FC1_FWD: return launch_mode<GEMM_FC1_FWD>(ma, mb, mc, p, grid, st);
+    case GEMM_FC2_FWD: return launch_mode<GEMM_FC2_FWD>(ma, mb, mc, p, grid, st);
+    case GEMM_FC2_DGRAD: return launch_mode<GEMM_FC2_DGRAD>(ma, mb, mc, p, grid, st);
+    case GEMM_FC1_DGRAD: return launch_mode<GEMM_FC1_DGRAD>(ma, mb, mc, p, grid, st);
+    case GEMM_WGRAD_W1: return launch_mode<GEMM_WGRAD_W1>(ma, mb, mc, p, grid, st);
+    default: return launch_mode<GEMM_WGRAD_W2>(ma, mb, mc, p, grid, st);
   }
 }
 

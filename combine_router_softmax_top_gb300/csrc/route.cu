@@ -35,11 +35,14 @@ __device__ __forceinline__ void unpack8_f32(const uint4& v, float (&f)[8]) {
 // runs over h = 0..H-1 in ascending order with one fmaf per step; since a
 // bf16*bf16 product is exact in fp32, each step is a single fp32 rounding of
 // (acc + x*w), the order both sides of the parity check use.
-// Each lane keeps its two tokens' 32-wide x slices in registers (loaded straight
-// from global memory, the next chunk while the current one is consumed); the
-// w_r chunk is staged as fp32 in shared memory (double buffered) and read with
-// warp-uniform broadcast loads, so shared memory serves 1 wavefront per 16
-// FMAs and the loop is bound by the FMA pipe.
+// Per 32-wide chunk of h, x is staged as bf16 (one 16-byte shared load gives a
+// lane 8 values of one token; an 80-byte row pitch keeps the 32 lanes' rows on
+// distinct banks) and w_r as fp32 read with warp-uniform broadcasts: 24 shared
+// wavefronts per 128 FMAs per warp, so the loop is FMA-bound. The next chunk is
+// fetched into registers while the current one is consumed (double buffered,
+// one barrier per chunk).
+constexpr int kRouteXPitchB = 80;  // bytes per staged x row (64 B of data)
+
 template <int NW>
 __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __restrict__ x,
                                                                const bf16* __restrict__ w_r,
@@ -47,13 +50,15 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
                                                                float* __restrict__ z, int T,
                                                                int H, int E) {
   constexpr int kThreads = NW * 32;
-  constexpr int eb = NW * kRouteEpw;  // experts in this CTA
+  constexpr int eb = NW * kRouteEpw;              // experts in this CTA
+  constexpr int nxp = kRouteTok * (kRouteHc / 8);  // 16-byte pieces of an x chunk (256)
+  constexpr int kXP = nxp / kThreads;              // per thread
   static_assert(eb * (kRouteHc / 8) == kThreads, "one 16-byte w_r piece per thread");
+  __shared__ __align__(16) uint8_t xs[2][kRouteTok * kRouteXPitchB];
   __shared__ __align__(16) float ws[2][eb][kRouteHc];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kRouteTok;
   const int e0 = blockIdx.y * eb;
-  const int ta = t0 + lane, tb = t0 + lane + 32;
 
   float acc[2][kRouteEpw];
 #pragma unroll
@@ -61,44 +66,47 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
 #pragma unroll
     for (int i = 0; i < kRouteEpw; ++i) acc[u][i] = 0.f;
 
-  const uint4* xa = reinterpret_cast<const uint4*>(x + (size_t)min(ta, T - 1) * H);
-  const uint4* xb = reinterpret_cast<const uint4*>(x + (size_t)min(tb, T - 1) * H);
   const int wr_row = threadIdx.x / (kRouteHc / 8), wr_col = (threadIdx.x % (kRouteHc / 8)) * 8;
   const bool w_ok = e0 + wr_row < E;
   const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)(w_ok ? e0 + wr_row : 0) * H);
-
-  uint4 xcur[2][4], xnext[2][4], wnext;
+  auto fetch = [&](int ch, uint4 (&rx)[kXP], uint4& rw) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    xcur[0][q] = __ldg(xa + q);
-    xcur[1][q] = __ldg(xb + q);
-  }
-  wnext = w_ok ? __ldg(wrow + wr_col / 8) : make_uint4(0, 0, 0, 0);
+    for (int q = 0; q < kXP; ++q) {
+      const int i = threadIdx.x + q * kThreads;
+      const int row = i / (kRouteHc / 8), col = i % (kRouteHc / 8);
+      const int t = min(t0 + row, T - 1);
+      rx[q] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + ch * (kRouteHc / 8) + col);
+    }
+    rw = w_ok ? __ldg(wrow + ch * (kRouteHc / 8) + wr_col / 8) : make_uint4(0, 0, 0, 0);
+  };
+  uint4 rx[kXP], rw;
+  fetch(0, rx, rw);
   const int nchunks = H / kRouteHc;
   for (int ch = 0; ch < nchunks; ++ch) {
+    const int b = ch & 1;
+#pragma unroll
+    for (int q = 0; q < kXP; ++q) {
+      const int i = threadIdx.x + q * kThreads;
+      const int row = i / (kRouteHc / 8), col = i % (kRouteHc / 8);
+      *reinterpret_cast<uint4*>(&xs[b][row * kRouteXPitchB + col * 16]) = rx[q];
+    }
     {
       float f[8];
-      unpack8_f32(wnext, f);
-      float4* dst = reinterpret_cast<float4*>(&ws[ch & 1][wr_row][wr_col]);
+      unpack8_f32(rw, f);
+      float4* dst = reinterpret_cast<float4*>(&ws[b][wr_row][wr_col]);
       dst[0] = make_float4(f[0], f[1], f[2], f[3]);
       dst[1] = make_float4(f[4], f[5], f[6], f[7]);
     }
     __syncthreads();
-    if (ch + 1 < nchunks) {
-      const int o = (ch + 1) * (kRouteHc / 8);
+    if (ch + 1 < nchunks) fetch(ch + 1, rx, rw);
+    const uint8_t* xa = &xs[b][lane * kRouteXPitchB];
+    const uint8_t* xb = &xs[b][(lane + 32) * kRouteXPitchB];
+    const float* wb = &ws[b][warp * kRouteEpw][0];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xnext[0][q] = __ldg(xa + o + q);
-        xnext[1][q] = __ldg(xb + o + q);
-      }
-      wnext = w_ok ? __ldg(wrow + o + wr_col / 8) : make_uint4(0, 0, 0, 0);
-    }
-    const float* wb = &ws[ch & 1][warp * kRouteEpw][0];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {  // 8 hidden elements per step
+    for (int q = 0; q < kRouteHc / 8; ++q) {  // 8 hidden elements per step
       float x0[8], x1[8];
-      unpack8_f32(xcur[0][q], x0);
-      unpack8_f32(xcur[1][q], x1);
+      unpack8_f32(*reinterpret_cast<const uint4*>(xa + q * 16), x0);
+      unpack8_f32(*reinterpret_cast<const uint4*>(xb + q * 16), x1);
 #pragma unroll
       for (int hh = 0; hh < 8; hh += 4) {
 #pragma unroll
@@ -115,17 +123,10 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
         }
       }
     }
-    if (ch + 1 < nchunks) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xcur[0][q] = xnext[0][q];
-        xcur[1][q] = xnext[1][q];
-      }
-    }
   }
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
-    const int t = u ? tb : ta;
+    const int t = t0 + lane + 32 * u;
     if (t >= T) continue;
 #pragma unroll
     for (int i = 0; i < kRouteEpw; ++i) {
