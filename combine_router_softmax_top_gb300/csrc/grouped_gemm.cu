@@ -6,7 +6,7 @@
 // first so dispatch-backward can start, and the weight gradient later).
 //
 // One persistent kernel per call, one CTA per SM, warp-specialised:
-//   warp 0      TMA producer (4-stage ring of 48 KB A|B stages)
+//   warp 0      TMA producer (ring of A|B stages: 4 x 48 KB, or 6 x 32 KB per CTA in pairs)
 //   warp 1      TMEM allocator + single-thread MMA issuer
 //   warps 2..9  epilogue: TMEM -> registers -> fused math -> coalesced global stores
 //               (two warps per TMEM lane quarter, each owning half the columns)
@@ -33,12 +33,19 @@
 #include "moe_internal.cuh"
 #include "sm100_ptx.cuh"
 
+#ifndef MOE_ROW_CS
+#define MOE_ROW_CS 1
+#endif
+#ifndef MOE_PAIR
+#define MOE_PAIR 1
+#endif
+
 namespace moe {
 
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;  // BN: widest tile (per-mode width is kBN)
-constexpr int kStages = 4;
+constexpr int kStagesMax = 6;
 constexpr int kABytes = BM * BK * 2;   // 16 KB
 constexpr int kAccCols = 256;          // TMEM columns per accumulator buffer
 constexpr int kTmemCols = 512;
@@ -61,21 +68,32 @@ struct Mode {
   static constexpr bool kRagK = MODE == GEMM_WGRAD_W1 || MODE == GEMM_WGRAD_W2;
   static constexpr int kAMn = kRagK ? 1 : 0;
   static constexpr int kBMn = (MODE == GEMM_FC2_DGRAD || MODE == GEMM_FC1_DGRAD || kRagK) ? 1 : 0;
-  // CTAs per cluster. Wgrad tiles are short in K, so their operand reads
-  // through L2 dominate; 4 CTAs on consecutive M blocks of one (expert, N block)
-  // each load a quarter of the shared B tile and multicast it to all four.
-  static constexpr int kCS = kRagK ? 4 : 1;
+  // CTAs per cluster: kCS consecutive M blocks of one (expert, N block) share
+  // the B tile; each CTA loads a slice and multicasts it to all of them.
+  // Wgrad tiles are short in K, so their operand reads through L2 dominate
+  // (4 CTAs); forward and dgrad share the expert's weight tile (MOE_ROW_CS).
+  // CTA pairs (tcgen05 cta_group::2): M = 256 rows per MMA, each CTA loading
+  // its own 128 rows of A and half of B, so a CTA takes in 32 KB per K stage
+  // instead of 48 KB and holds 6 stages.
+  // Measured: pairs speed up FC1/FC2 forward and FC1 dgrad; FC2 dgrad (128-wide
+  // tiles) gains nothing and the short-K wgrad runs twice as slow as with the
+  // 4-CTA multicast, so those two stay unpaired.
+  static constexpr bool kPair = MOE_PAIR && !kRagK && MODE != GEMM_FC2_DGRAD;
+  static constexpr int kCS = kPair ? 2 : kRagK ? 4 : MOE_ROW_CS;
   // Tile width. The FC2 dgrad epilogue needs the tile's saved pre-activation
   // (gate and up) next to the accumulator; at 128 columns that slab (64 KB) is
   // TMA-loaded into shared memory by a dedicated warp ahead of the epilogue.
   static constexpr bool kAux = MODE == GEMM_FC2_DGRAD;
   static constexpr int kBN = kAux ? 128 : 256;
-  static constexpr int kBBytes = kBN * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBBytes = kBN * BK * 2;            // whole B tile per stage
+  static constexpr int kBBytesCta = kPair ? kBBytes / 2 : kBBytes;  // B bytes this CTA loads
+  static constexpr int kStageBytes = kABytes + kBBytesCta;
+  static constexpr int kStages = kPair ? (kAux ? 5 : 6) : 4;
   static constexpr int kAuxBytes = kAux ? 4 * 16384 : 0;
   static constexpr int kWarps = kAux ? 11 : 10;  // producer, MMA, 8 epilogue (+ aux loader)
   static constexpr size_t kDynSmem =
       (size_t)kStages * kStageBytes + kAuxBytes + kEpiStageBytes + 1024;
+  static_assert(kStages <= kStagesMax, "barrier arrays");
   // reduction depth for the row-ragged modes
   __device__ static int kdim(const KParams& p) {
     return MODE == GEMM_FC1_FWD ? p.H : MODE == GEMM_FC2_FWD ? p.F
@@ -105,8 +123,8 @@ struct Tile {
 };
 
 struct SmemCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kStagesMax];
+  uint64_t empty[kStagesMax];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t tail;
@@ -137,10 +155,11 @@ __device__ __forceinline__ Tile tile_at(const KParams& p, const SmemCtl& c, int 
     t.rows = cnt;
     t.nk = (cnt + BK - 1) / BK;
   } else {
-    const int mt = (cnt + BM - 1) / BM;
-    t.m0 = (local % mt) * BM;
-    t.n0 = (local / mt) * (MODE == GEMM_FC1_FWD ? 128 : Mode<MODE>::kBN);
-    t.rows = min(BM, cnt - t.m0);
+    constexpr int cs = Mode<MODE>::kCS;
+    const int mg = ((cnt + BM - 1) / BM + cs - 1) / cs;  // cluster tiles along M
+    t.m0 = ((local % mg) * cs + (int)rank) * BM;
+    t.n0 = (local / mg) * (MODE == GEMM_FC1_FWD ? 128 : Mode<MODE>::kBN);
+    t.rows = min(BM, cnt - t.m0);  // <= 0: this CTA's M block is past the expert
     t.nk = Mode<MODE>::kdim(p) / BK;
   }
   return t;
@@ -228,13 +247,16 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
   // ---- per-CTA setup: offsets, tile prefix, barriers, TMEM
   for (int e = threadIdx.x; e <= E; e += blockDim.x) ctl.off[e] = p.off[e];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < M::kStages; ++s) {
       ptx::mbar_init(&ctl.full[s], 1);
-      ptx::mbar_init(&ctl.empty[s], M::kCS);
+      // multicast B: every CTA of the cluster releases the stage; pair: the
+      // even CTA's MMA releases it in both CTAs
+      ptx::mbar_init(&ctl.empty[s], M::kPair ? 1 : M::kCS);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl.tmem_full[b], 1);
-      ptx::mbar_init(&ctl.tmem_empty[b], 256);
+      // pair: the even CTA's MMA waits for both CTAs' epilogues
+      ptx::mbar_init(&ctl.tmem_empty[b], M::kPair ? 512 : 256);
     }
     ptx::mbar_init(&ctl.tail, 1);
     ptx::mbar_init(&ctl.drain, 1);
@@ -243,7 +265,15 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     ctl.abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 1) {
+  if (M::kPair) {
+    // the pair's TMEM is allocated collectively; barriers must be live in both
+    __syncthreads();
+    ptx::cluster_sync();
+    if (warp == 1) {
+      ptx::tmem_alloc_pair(&ctl.tmem_base, kTmemCols);
+      ptx::tmem_relinquish_pair();
+    }
+  } else if (warp == 1) {
     ptx::tmem_alloc(&ctl.tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -258,7 +288,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         const int cnt = ctl.off[e + 1] - ctl.off[e];
         if (M::kRagK)
           n = (((M::wg_mdim(p) + BM - 1) / BM + M::kCS - 1) / M::kCS) * M::ntiles(p);
-        else n = ((cnt + BM - 1) / BM) * M::ntiles(p);
+        else n = (((cnt + BM - 1) / BM + M::kCS - 1) / M::kCS) * M::ntiles(p);
         if (cnt < 0) n = 0;
       }
       int incl = n;
@@ -277,7 +307,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
   ptx::tc_fence_after();
   // peers multicast into this CTA's shared memory and barriers: all must be
   // initialised first
-  if (M::kCS > 1) ptx::cluster_sync();
+  if (M::kCS > 1 && !M::kPair) ptx::cluster_sync();
   const int total = ctl.tstart[E];
   const uint32_t tmem_base = ctl.tmem_base;
   const uint32_t crank = M::kCS > 1 ? ptx::cluster_ctarank() : 0;
@@ -331,20 +361,44 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
                 ptx::tma_load_2d_multicast(sB + 8192 * i, &tmB, &ctl.full[stage], t.n0 + 64 * i,
                                            r, cmask);
             }
+          } else if (M::kPair) {
+            // both CTAs' loads complete on the even CTA's full[stage]
+            const uint32_t fb = ptx::mapa_shared(&ctl.full[stage], 0);
+            if (crank == 0) ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * M::kStageBytes);
+            ptx::tma_load_2d_pair(sA, &tmA, fb, k0, t.row0 + t.m0);
+            if (MODE == GEMM_FC1_FWD) {  // even CTA: 128 gate rows, odd CTA: 128 up rows
+              ptx::tma_load_2d_pair(sB, &tmB, fb, k0, t.e * 2 * p.F + (crank ? p.F : 0) + t.n0);
+            } else if (MODE == GEMM_FC2_FWD) {
+              ptx::tma_load_2d_pair(sB, &tmB, fb, k0, t.e * p.H + t.n0 + 128 * crank);
+            } else {  // MN-major B: this CTA's half of the N columns
+              const int base = MODE == GEMM_FC2_DGRAD ? t.e * p.H : t.e * 2 * p.F;
+              constexpr int nb = M::kBN / 128;  // 64-wide boxes per CTA
+#pragma unroll
+              for (int i = 0; i < nb; ++i)
+                ptx::tma_load_2d_pair(sB + 8192 * i, &tmB, fb, t.n0 + 64 * (crank * nb + i),
+                                      base + k0);
+            }
           } else {
             ptx::mbar_arrive_expect_tx(bar, M::kStageBytes);
             ptx::tma_load_2d(sA, &tmA, bar, k0, t.row0 + t.m0);
+            // B boxes: box i is loaded by cluster rank i % kCS and multicast
+            auto load_b = [&](int i, void* dst, int c0, int c1) {
+              if (M::kCS == 1)
+                ptx::tma_load_2d(dst, &tmB, bar, c0, c1);
+              else if (i % M::kCS == (int)crank)
+                ptx::tma_load_2d_multicast(dst, &tmB, bar, c0, c1, cmask);
+            };
             if (MODE == GEMM_FC1_FWD) {
               const int base = t.e * 2 * p.F;
-              ptx::tma_load_2d(sB, &tmB, bar, k0, base + t.n0);
-              ptx::tma_load_2d(sB + 16384, &tmB, bar, k0, base + p.F + t.n0);
+              load_b(0, sB, k0, base + t.n0);                 // 128 gate rows
+              load_b(1, sB + 16384, k0, base + p.F + t.n0);   // 128 up rows
             } else if (MODE == GEMM_FC2_FWD) {
-              ptx::tma_load_2d(sB, &tmB, bar, k0, t.e * p.H + t.n0);
+              load_b(0, sB, k0, t.e * p.H + t.n0);
+              load_b(1, sB + 16384, k0, t.e * p.H + t.n0 + 128);
             } else {
               const int base = MODE == GEMM_FC2_DGRAD ? t.e * p.H : t.e * 2 * p.F;
 #pragma unroll
-              for (int i = 0; i < M::kBN / 64; ++i)
-                ptx::tma_load_2d(sB + 8192 * i, &tmB, bar, t.n0 + 64 * i, base + k0);
+              for (int i = 0; i < M::kBN / 64; ++i) load_b(i, sB + 8192 * i, t.n0 + 64 * i, base + k0);
             }
           }
         }
@@ -367,7 +421,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&ctl.full[stage]);
         }
-        if (++stage == kStages) {
+        if (++stage == M::kStages) {
           stage = 0;
           phase ^= 1;
         }
@@ -375,8 +429,9 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, M::kBN, M::kAMn, M::kBMn);
+    // (pair mode: only the even CTA issues, for both CTAs)
+    if (lane == 0 && !(M::kPair && crank != 0)) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(M::kPair ? 2 * BM : BM, M::kBN, M::kAMn, M::kBMn);
       const uint32_t a_lbo = M::kAMn ? 8192 : 16, b_lbo = M::kBMn ? 8192 : 16;
       const uint32_t a_adv = M::kAMn ? (2048 >> 4) : (32 >> 4);
       const uint32_t b_adv = M::kBMn ? (2048 >> 4) : (32 >> 4);
@@ -404,27 +459,35 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
           const uint64_t adesc = ptx::sdesc_sw128(a_addr, a_lbo, 1024);
           const uint64_t bdesc = ptx::sdesc_sw128(b_addr, b_lbo, 1024);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            ptx::umma_bf16(d_tmem, adesc + (uint64_t)(kk * a_adv), bdesc + (uint64_t)(kk * b_adv),
-                           idesc, (kt | kk) != 0);
-          // the stage is free once every CTA that received the multicast B
-          // slices has consumed it
-          if (M::kCS > 1) ptx::umma_commit_multicast(&ctl.empty[stage], cmask);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            if (M::kPair)
+              ptx::umma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * a_adv),
+                                  bdesc + (uint64_t)(kk * b_adv), idesc, (kt | kk) != 0);
+            else
+              ptx::umma_bf16(d_tmem, adesc + (uint64_t)(kk * a_adv), bdesc + (uint64_t)(kk * b_adv),
+                             idesc, (kt | kk) != 0);
+          }
+          // the stage is free once every CTA whose shared memory the MMAs read
+          // (pair) or that received the multicast B slices has consumed it
+          if (M::kPair) ptx::umma_commit_pair(&ctl.empty[stage], 3);
+          else if (M::kCS > 1) ptx::umma_commit_multicast(&ctl.empty[stage], cmask);
           else ptx::umma_commit(&ctl.empty[stage]);
-          if (++stage == kStages) {
+          if (++stage == M::kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        ptx::umma_commit(&ctl.tmem_full[acc]);
+        if (M::kPair) ptx::umma_commit_pair(&ctl.tmem_full[acc], 3);
+        else ptx::umma_commit(&ctl.tmem_full[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
       // make sure no MMA is still running before TMEM is released
-      ptx::umma_commit(&ctl.drain);
+      if (M::kPair) ptx::umma_commit_pair(&ctl.drain, 1);
+      else ptx::umma_commit(&ctl.drain);
       if (!ptx::mbar_wait(&ctl.drain, 0, &ctl.abort, kWaitLimitNs)) {
         // abort already flagged: wait once more with the abort flag ignored
         int dummy = 0;
@@ -447,7 +510,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
           break;
         }
         ph ^= 1;
-        uint8_t* aux = smem + kStages * M::kStageBytes;
+        uint8_t* aux = smem + M::kStages * M::kStageBytes;
         const int row = t.row0 + t.m0;
         ptx::mbar_arrive_expect_tx(&ctl.aux_full, M::kAuxBytes);
         ptx::tma_load_2d(aux, &tmC, &ctl.aux_full, t.n0, row);
@@ -465,7 +528,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     const int q = warp & 3;
     const int hf = ew >> 2;
     const int r = q * 32 + lane;
-    uint4* stage = reinterpret_cast<uint4*>(smem + kStages * M::kStageBytes + M::kAuxBytes) + ew * 128;
+    uint4* stage = reinterpret_cast<uint4*>(smem + M::kStages * M::kStageBytes + M::kAuxBytes) + ew * 128;
     int cursor = 0, acc = 0;
     uint32_t acc_phase = 0, aux_phase = 0;
     for (int tile = first; tile < total; tile += stride) {
@@ -535,7 +598,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
             break;
           }
           aux_phase ^= 1;
-          const uint8_t* aux = smem + kStages * M::kStageBytes;
+          const uint8_t* aux = smem + M::kStages * M::kStageBytes;
           bf16* dbase = p.out0 + slab_row0 * (size_t)(2 * p.F);
 #pragma unroll 1
           for (int cc = c0; cc < c0 + M::kBN / 64; ++cc) {
@@ -575,7 +638,10 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         }
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&ctl.tmem_empty[acc]);
+      if (M::kPair && crank != 0)
+        ptx::mbar_arrive_cluster(ptx::mapa_shared(&ctl.tmem_empty[acc], 0));
+      else
+        ptx::mbar_arrive(&ctl.tmem_empty[acc]);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
@@ -588,7 +654,10 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
   ptx::tc_fence_after();
   // peers may still arrive on this CTA's barriers until they are done
   if (M::kCS > 1) ptx::cluster_sync();
-  if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) {
+    if (M::kPair) ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    else ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -714,20 +783,20 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
   switch (g.mode) {
     case GEMM_FC1_FWD:
       ok = make_map(&ma, g.A, N, H, 128) && make_map(&mb, g.B, (long long)E * 2 * F, H, 128);
-      ntile_bound = (N / BM + E) * ((F + 127) / 128);
+      ntile_bound = (N / BM + 2 * E) * ((F + 127) / 128);
       break;
     case GEMM_FC2_FWD:
-      ok = make_map(&ma, g.A, N, F, 128) && make_map(&mb, g.B, (long long)E * H, F, 256);
-      ntile_bound = (N / BM + E) * ((H + BN - 1) / BN);
+      ok = make_map(&ma, g.A, N, F, 128) && make_map(&mb, g.B, (long long)E * H, F, 128);
+      ntile_bound = (N / BM + 2 * E) * ((H + BN - 1) / BN);
       break;
     case GEMM_FC2_DGRAD:
       ok = make_map(&ma, g.A, N, H, 128) && make_map(&mb, g.B, (long long)E * H, F, 64) &&
            make_map(&mc, g.aux, N, 2 * F, 128);
-      ntile_bound = (N / BM + E) * ((F + 127) / 128);
+      ntile_bound = (N / BM + 2 * E) * ((F + 127) / 128);
       break;
     case GEMM_FC1_DGRAD:
       ok = make_map(&ma, g.A, N, 2 * F, 128) && make_map(&mb, g.B, (long long)E * 2 * F, H, 64);
-      ntile_bound = (N / BM + E) * ((H + BN - 1) / BN);
+      ntile_bound = (N / BM + 2 * E) * ((H + BN - 1) / BN);
       break;
     case GEMM_WGRAD_W1:
       ok = make_map(&ma, g.A, N, 2 * F, 64) && make_map(&mb, g.B, N, H, 64);

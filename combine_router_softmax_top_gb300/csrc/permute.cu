@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const bf16* __restrict__ o
 // d_o[slot[t,j]] = bf16(g[t,j] * dy[t]); dgates[t,j] = <dy[t], o[slot[t,j]]>.
 // The dot product is reduced over the token's threads in a fixed tree order.
 template <int KMAX>
-__global__ void __launch_bounds__(256) combine_bwd_kernel(
+__global__ void __launch_bounds__(256, KMAX <= 8 ? 3 : 1) combine_bwd_kernel(
     const bf16* __restrict__ dy, const bf16* __restrict__ o, const int32_t* __restrict__ slot,
     const float* __restrict__ gates, bf16* __restrict__ d_o, float* __restrict__ dgates, int T,
     int H, int k, long long N, int tpr) {

@@ -14,7 +14,6 @@ namespace moe {
 namespace {
 
 constexpr int kRouteTok = 64;   // tokens per CTA: lane owns tokens lane and lane + 32
-constexpr int kRouteEpw = 8;    // experts per warp
 constexpr int kRouteHc = 32;    // hidden elements per chunk
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
@@ -30,8 +29,8 @@ __device__ __forceinline__ void unpack8_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
-// z[t, e] for a tile of 64 tokens x (NW * 8) experts: lane owns tokens lane and
-// lane+32, warp owns 8 experts, 16 accumulators per thread. Every accumulator
+// z[t, e] for a tile of 64 tokens x (NW * EPW) experts: lane owns tokens lane
+// and lane+32, warp owns EPW experts, 2 x EPW accumulators per thread. Every accumulator
 // runs over h = 0..H-1 in ascending order with one fmaf per step; since a
 // bf16*bf16 product is exact in fp32, each step is a single fp32 rounding of
 // (acc + x*w), the order both sides of the parity check use.
@@ -43,7 +42,7 @@ __device__ __forceinline__ void unpack8_f32(const uint4& v, float (&f)[8]) {
 // one barrier per chunk).
 constexpr int kRouteXPitchB = 80;  // bytes per staged x row (64 B of data)
 
-template <int NW>
+template <int NW, int kRouteEpw>
 __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __restrict__ x,
                                                                const bf16* __restrict__ w_r,
                                                                const float* __restrict__ bias,
@@ -53,7 +52,8 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
   constexpr int eb = NW * kRouteEpw;              // experts in this CTA
   constexpr int nxp = kRouteTok * (kRouteHc / 8);  // 16-byte pieces of an x chunk (256)
   constexpr int kXP = nxp / kThreads;              // per thread
-  static_assert(eb * (kRouteHc / 8) == kThreads, "one 16-byte w_r piece per thread");
+  constexpr int kWP = eb * (kRouteHc / 8);         // 16-byte pieces of a w_r chunk
+  static_assert(kWP <= kThreads && nxp % kThreads == 0, "staging split");
   __shared__ __align__(16) uint8_t xs[2][kRouteTok * kRouteXPitchB];
   __shared__ __align__(16) float ws[2][eb][kRouteHc];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
     for (int i = 0; i < kRouteEpw; ++i) acc[u][i] = 0.f;
 
   const int wr_row = threadIdx.x / (kRouteHc / 8), wr_col = (threadIdx.x % (kRouteHc / 8)) * 8;
-  const bool w_ok = e0 + wr_row < E;
+  const bool w_mine = (int)threadIdx.x < kWP;  // this thread stages a w_r piece
+  const bool w_ok = w_mine && e0 + wr_row < E;
   const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)(w_ok ? e0 + wr_row : 0) * H);
   auto fetch = [&](int ch, uint4 (&rx)[kXP], uint4& rw) {
 #pragma unroll
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
       const int row = i / (kRouteHc / 8), col = i % (kRouteHc / 8);
       *reinterpret_cast<uint4*>(&xs[b][row * kRouteXPitchB + col * 16]) = rx[q];
     }
-    {
+    if (w_mine) {
       float f[8];
       unpack8_f32(rw, f);
       float4* dst = reinterpret_cast<float4*>(&ws[b][wr_row][wr_col]);
@@ -102,25 +103,37 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
     const uint8_t* xa = &xs[b][lane * kRouteXPitchB];
     const uint8_t* xb = &xs[b][(lane + 32) * kRouteXPitchB];
     const float* wb = &ws[b][warp * kRouteEpw][0];
+    // w_r values of the next 4-wide h step are loaded before the FMAs of the
+    // current one, so shared-memory latency overlaps the arithmetic
+    float4 wn[kRouteEpw];
 #pragma unroll
-    for (int q = 0; q < kRouteHc / 8; ++q) {  // 8 hidden elements per step
-      float x0[8], x1[8];
-      unpack8_f32(*reinterpret_cast<const uint4*>(xa + q * 16), x0);
-      unpack8_f32(*reinterpret_cast<const uint4*>(xb + q * 16), x1);
+    for (int i = 0; i < kRouteEpw; ++i) wn[i] = *reinterpret_cast<const float4*>(wb + i * kRouteHc);
+    float x0[8], x1[8];
 #pragma unroll
-      for (int hh = 0; hh < 8; hh += 4) {
+    for (int s4 = 0; s4 < kRouteHc / 4; ++s4) {
+      if ((s4 & 1) == 0) {
+        unpack8_f32(*reinterpret_cast<const uint4*>(xa + (s4 >> 1) * 16), x0);
+        unpack8_f32(*reinterpret_cast<const uint4*>(xb + (s4 >> 1) * 16), x1);
+      }
+      float4 wc[kRouteEpw];
 #pragma unroll
-        for (int i = 0; i < kRouteEpw; ++i) {
-          const float4 wv = *reinterpret_cast<const float4*>(wb + i * kRouteHc + q * 8 + hh);
-          acc[0][i] = fmaf(x0[hh + 0], wv.x, acc[0][i]);
-          acc[1][i] = fmaf(x1[hh + 0], wv.x, acc[1][i]);
-          acc[0][i] = fmaf(x0[hh + 1], wv.y, acc[0][i]);
-          acc[1][i] = fmaf(x1[hh + 1], wv.y, acc[1][i]);
-          acc[0][i] = fmaf(x0[hh + 2], wv.z, acc[0][i]);
-          acc[1][i] = fmaf(x1[hh + 2], wv.z, acc[1][i]);
-          acc[0][i] = fmaf(x0[hh + 3], wv.w, acc[0][i]);
-          acc[1][i] = fmaf(x1[hh + 3], wv.w, acc[1][i]);
-        }
+      for (int i = 0; i < kRouteEpw; ++i) wc[i] = wn[i];
+      if (s4 + 1 < kRouteHc / 4) {
+#pragma unroll
+        for (int i = 0; i < kRouteEpw; ++i)
+          wn[i] = *reinterpret_cast<const float4*>(wb + i * kRouteHc + (s4 + 1) * 4);
+      }
+      const int hh = (s4 & 1) * 4;
+#pragma unroll
+      for (int i = 0; i < kRouteEpw; ++i) {
+        acc[0][i] = fmaf(x0[hh + 0], wc[i].x, acc[0][i]);
+        acc[1][i] = fmaf(x1[hh + 0], wc[i].x, acc[1][i]);
+        acc[0][i] = fmaf(x0[hh + 1], wc[i].y, acc[0][i]);
+        acc[1][i] = fmaf(x1[hh + 1], wc[i].y, acc[1][i]);
+        acc[0][i] = fmaf(x0[hh + 2], wc[i].z, acc[0][i]);
+        acc[1][i] = fmaf(x1[hh + 2], wc[i].z, acc[1][i]);
+        acc[0][i] = fmaf(x0[hh + 3], wc[i].w, acc[0][i]);
+        acc[1][i] = fmaf(x1[hh + 3], wc[i].w, acc[1][i]);
       }
     }
   }
@@ -222,33 +235,34 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 // one token row. dz_j = g_j (dg_j - <g, dg>) on the chosen set;
 // dx = bf16(dx32 + sum_j dz_j * w_r[i_j]).
 template <int KMAX>
-__global__ void __launch_bounds__(256) route_bwd_dx_kernel(
+__global__ void __launch_bounds__(256, KMAX <= 8 ? 4 : 2) route_bwd_dx_kernel(
     const float* __restrict__ dgates, const float* __restrict__ gates,
     const int32_t* __restrict__ idx, const bf16* __restrict__ w_r, const float* __restrict__ dx32,
     bf16* __restrict__ dx, float* __restrict__ dz, int T, int H, int E, int k, int tpr,
     int* status) {
+  // tokens per block = 256 / tpr with tpr >= H/8 >= 8, so at most 32
+  __shared__ float s_dz[32][KMAX];
+  __shared__ int s_e[32][KMAX];
   const int rpb = blockDim.x / tpr;
-  const int t = blockIdx.x * rpb + threadIdx.x / tpr;
+  const int tl = threadIdx.x / tpr;
+  const int t = blockIdx.x * rpb + tl;
   const int sub = threadIdx.x % tpr;
+  // the token's first min(k, tpr) threads work out dz_j and the expert of slot j
+  if (t < T && sub < k) {
+    float inner = 0.f;
+    for (int j = 0; j < k; ++j) inner = fmaf(gates[(size_t)t * k + j], dgates[(size_t)t * k + j], inner);
+    const int e = idx[(size_t)t * k + sub];
+    s_dz[tl][sub] = gates[(size_t)t * k + sub] * (dgates[(size_t)t * k + sub] - inner);
+    s_e[tl][sub] = (unsigned)e < (unsigned)E ? e : -1;
+  }
+  __syncthreads();
   if (t >= T) return;
-  // dz and the expert of each slot, once per thread (the token's k values are
-  // shared by its threads through L1)
-  float inner = 0.f;
   float dzj[KMAX];
   int ej[KMAX];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
-    if (j < k) inner = fmaf(gates[(size_t)t * k + j], dgates[(size_t)t * k + j], inner);
-  }
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    dzj[j] = 0.f;
-    ej[j] = -1;
-    if (j < k) {
-      const int e = idx[(size_t)t * k + j];
-      dzj[j] = gates[(size_t)t * k + j] * (dgates[(size_t)t * k + j] - inner);
-      ej[j] = (unsigned)e < (unsigned)E ? e : -1;
-    }
+    dzj[j] = j < k ? s_dz[tl][j] : 0.f;
+    ej[j] = j < k ? s_e[tl][j] : -1;
   }
   const int cpr = H / 8;
   for (int c = sub; c < cpr; c += tpr) {
@@ -394,12 +408,17 @@ __global__ void __launch_bounds__(256) route_bwd_dwr_reduce_kernel(
     int H, int E) {
   __shared__ int s_first, s_n;
   const int e = blockIdx.x;
-  if (threadIdx.x == 0) {
-    int first = 0;
-    for (int i = 0; i < e; ++i)
-      first += (off[i + 1] - off[i] + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk;
-    s_first = first;
-    s_n = (off[e + 1] - off[e] + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk;
+  if (threadIdx.x < 32) {
+    // chunks of experts 0..e-1, summed by one warp
+    int sum = 0;
+    for (int i = threadIdx.x; i < e; i += 32)
+      sum += (off[i + 1] - off[i] + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (threadIdx.x == 0) {
+      s_first = sum;
+      s_n = (off[e + 1] - off[e] + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk;
+    }
   }
   __syncthreads();
   const int c = blockIdx.y * blockDim.x + threadIdx.x;
@@ -422,18 +441,20 @@ moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* 
                           int* status, cudaStream_t st) {
   (void)status;
   if (d.T == 0) return MOE_OK;
-  // warps per CTA: 4 (32 experts) unless E is smaller; 64 tokens per CTA
-  const int nw = d.E > 16 ? 4 : d.E > 8 ? 2 : 1;
-  const int eb = nw * kRouteEpw;
+  // 4 warps x 4 experts (16 experts, 64 tokens) per CTA: 2 x 4 accumulators per
+  // thread keep the FMA : shared-wavefront ratio at 1 while giving the SMs
+  // enough warps to hide shared-memory latency; small E gets fewer warps.
+  const int nw = d.E > 8 ? 4 : d.E > 4 ? 2 : 1;
+  const int eb = nw * 4;
   dim3 grid(ceil_div(d.T, kRouteTok), ceil_div(d.E, eb));
   {
     LaunchScope _ls(K_ROUTE_LOGITS, st);
     if (nw == 4)
-      route_logits_kernel<4><<<grid, 128, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+      route_logits_kernel<4, 4><<<grid, 128, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
     else if (nw == 2)
-      route_logits_kernel<2><<<grid, 64, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+      route_logits_kernel<2, 4><<<grid, 64, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
     else
-      route_logits_kernel<1><<<grid, 32, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+      route_logits_kernel<1, 4><<<grid, 32, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
   }
   moe_status_t s = check_launch("route_logits_kernel");
   if (s != MOE_OK) return s;
@@ -470,7 +491,7 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
                               cudaStream_t st) {
   const int cpr = d.H / 8;
   int tpr = 1;
-  while (tpr < cpr && tpr < 256) tpr <<= 1;
+  while ((tpr < cpr || tpr < d.k) && tpr < 256) tpr <<= 1;  // >= k threads per token
   const int rpb = 256 / tpr;
   if (d.T > 0) {
     {
