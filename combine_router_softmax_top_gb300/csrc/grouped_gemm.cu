@@ -75,20 +75,19 @@ struct Mode {
   // CTA pairs (tcgen05 cta_group::2): M = 256 rows per MMA, each CTA loading
   // its own 128 rows of A and half of B, so a CTA takes in 32 KB per K stage
   // instead of 48 KB and holds 6 stages.
-  // Measured: pairs speed up FC1/FC2 forward and FC1 dgrad; FC2 dgrad (128-wide
-  // tiles) gains nothing and the short-K wgrad runs twice as slow as with the
-  // 4-CTA multicast, so those two stay unpaired.
-  static constexpr bool kPair = MOE_PAIR && !kRagK && MODE != GEMM_FC2_DGRAD;
+  // Measured: pairs speed up the forward and dgrad GEMMs; the short-K wgrad
+  // runs twice as slow as with the 4-CTA multicast, so it stays unpaired.
+  static constexpr bool kPair = MOE_PAIR && !kRagK;
   static constexpr int kCS = kPair ? 2 : kRagK ? 4 : MOE_ROW_CS;
-  // Tile width. The FC2 dgrad epilogue needs the tile's saved pre-activation
-  // (gate and up) next to the accumulator; at 128 columns that slab (64 KB) is
-  // TMA-loaded into shared memory by a dedicated warp ahead of the epilogue.
+  // The FC2 dgrad epilogue needs the tile's saved pre-activation (gate and up)
+  // next to the accumulator: a dedicated warp TMA-loads it into shared memory
+  // ahead of the epilogue, one 128-column half (64 KB) at a time.
   static constexpr bool kAux = MODE == GEMM_FC2_DGRAD;
-  static constexpr int kBN = kAux ? 128 : 256;
+  static constexpr int kBN = 256;
   static constexpr int kBBytes = kBN * BK * 2;            // whole B tile per stage
   static constexpr int kBBytesCta = kPair ? kBBytes / 2 : kBBytes;  // B bytes this CTA loads
   static constexpr int kStageBytes = kABytes + kBBytesCta;
-  static constexpr int kStages = kPair ? (kAux ? 5 : 6) : 4;
+  static constexpr int kStages = kPair ? (kAux ? 4 : 6) : 4;
   static constexpr int kAuxBytes = kAux ? 4 * 16384 : 0;
   static constexpr int kWarps = kAux ? 11 : 10;  // producer, MMA, 8 epilogue (+ aux loader)
   static constexpr size_t kDynSmem =
@@ -104,7 +103,7 @@ struct Mode {
     switch (MODE) {
       case GEMM_FC1_FWD: return (p.F + 127) / 128;
       case GEMM_FC2_FWD: return (p.H + BN - 1) / BN;
-      case GEMM_FC2_DGRAD: return (p.F + kBN - 1) / kBN;
+      case GEMM_FC2_DGRAD: return (p.F + BN - 1) / BN;
       case GEMM_FC1_DGRAD: return (p.H + BN - 1) / BN;
       case GEMM_WGRAD_W1: return (p.H + BN - 1) / BN;
       default: return (p.F + BN - 1) / BN;
@@ -163,6 +162,18 @@ __device__ __forceinline__ Tile tile_at(const KParams& p, const SmemCtl& c, int 
     t.nk = Mode<MODE>::kdim(p) / BK;
   }
   return t;
+}
+
+// Profiling builds (-DMOE_TRACE) record, for CTA 0, the global time at which
+// each role starts and finishes each of its first 128 tiles, into the bytes
+// after the status words (the router-logits scratch, unused when the caller
+// passes its own logits buffer). Product builds compile this away.
+__device__ __forceinline__ void trace(const KParams& p, int mode, int ev, int i) {
+#ifdef MOE_TRACE
+  if (blockIdx.x == 0 && i < 128)
+    reinterpret_cast<uint64_t*>(reinterpret_cast<char*>(p.status) + 256 + mode * 8192)[i * 8 + ev] =
+        ptx::globaltimer_ns();
+#endif
 }
 
 __device__ __forceinline__ void flag_timeout(SmemCtl& c, int* status, int where) {
@@ -225,6 +236,12 @@ __device__ __forceinline__ void store_chunks(uint4* stage, uint32_t tbase, int c
                  n0 + 32 * cc < ld);
     if (i + 1 < BN / 64) ptx::tmem_ld_wait(nxt);
   }
+}
+
+// Logistic sigmoid with the hardware exponential and reciprocal (a few ulp;
+// the epilogue rounds its results to bf16 anyway).
+__device__ __forceinline__ float fast_sigmoid(float x) {
+  return __frcp_rn(1.f + __expf(-x));
 }
 
 __device__ __forceinline__ float round_bf16(float x) {
@@ -324,8 +341,10 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     int stage = 0, cursor = 0;
     uint32_t phase = 0, tail_phase = 0;
     bool ok = true;
-    for (int tile = first; tile < total && ok; tile += stride) {
+    int ti = 0;
+    for (int tile = first; tile < total && ok; tile += stride, ++ti) {
       const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
+      if (lane == 0) trace(p, MODE, 0, ti);
       for (int kt = 0; kt < t.nk; ++kt) {
         if (!ptx::mbar_wait(&ctl.empty[stage], phase ^ 1, &ctl.abort, kWaitLimitNs)) {
           if (lane == 0) flag_timeout(ctl, p.status, 1);
@@ -426,6 +445,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
           phase ^= 1;
         }
       }
+      if (lane == 0) trace(p, MODE, 1, ti);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
@@ -438,14 +458,17 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
       int stage = 0, cursor = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
+      int ti = -1;
       for (int tile = first; tile < total && ok; tile += stride) {
         const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
+        ++ti;
         if (t.nk == 0) continue;
         if (!ptx::mbar_wait(&ctl.tmem_empty[acc], acc_phase ^ 1, &ctl.abort, kWaitLimitNs)) {
           flag_timeout(ctl, p.status, 3);
           break;
         }
         ptx::tc_fence_after();
+        trace(p, MODE, 2, ti);
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
         for (int kt = 0; kt < t.nk; ++kt) {
           if (!ptx::mbar_wait(&ctl.full[stage], phase, &ctl.abort, kWaitLimitNs)) {
@@ -478,6 +501,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
           }
         }
         if (!ok) break;
+        trace(p, MODE, 3, ti);
         if (M::kPair) ptx::umma_commit_pair(&ctl.tmem_full[acc], 3);
         else ptx::umma_commit(&ctl.tmem_full[acc]);
         if (++acc == 2) {
@@ -497,8 +521,8 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     __syncwarp();
   } else if (M::kAux && warp == 10) {
     // ================================================================ aux loader
-    // Loads each tile's saved pre-activation slab once the epilogue has
-    // released the previous one.
+    // Loads each tile's saved pre-activation, a 128-column half at a time, each
+    // once the epilogue has released the previous half.
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmC);
       int cursor = 0;
@@ -512,11 +536,19 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         ph ^= 1;
         uint8_t* aux = smem + M::kStages * M::kStageBytes;
         const int row = t.row0 + t.m0;
-        ptx::mbar_arrive_expect_tx(&ctl.aux_full, M::kAuxBytes);
-        ptx::tma_load_2d(aux, &tmC, &ctl.aux_full, t.n0, row);
-        ptx::tma_load_2d(aux + 16384, &tmC, &ctl.aux_full, t.n0 + 64, row);
-        ptx::tma_load_2d(aux + 2 * 16384, &tmC, &ctl.aux_full, p.F + t.n0, row);
-        ptx::tma_load_2d(aux + 3 * 16384, &tmC, &ctl.aux_full, p.F + t.n0 + 64, row);
+        for (int half = 0; half < 2; ++half) {
+          if (half == 1 && !ptx::mbar_wait(&ctl.aux_empty, ph ^ 1, &ctl.abort, kWaitLimitNs)) {
+            flag_timeout(ctl, p.status, 7);
+            break;
+          }
+          if (half == 1) ph ^= 1;
+          const int c = t.n0 + 128 * half;
+          ptx::mbar_arrive_expect_tx(&ctl.aux_full, M::kAuxBytes);
+          ptx::tma_load_2d(aux, &tmC, &ctl.aux_full, c, row);
+          ptx::tma_load_2d(aux + 16384, &tmC, &ctl.aux_full, c + 64, row);
+          ptx::tma_load_2d(aux + 2 * 16384, &tmC, &ctl.aux_full, p.F + c, row);
+          ptx::tma_load_2d(aux + 3 * 16384, &tmC, &ctl.aux_full, p.F + c + 64, row);
+        }
       }
     }
     __syncwarp();
@@ -531,8 +563,11 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     uint4* stage = reinterpret_cast<uint4*>(smem + M::kStages * M::kStageBytes + M::kAuxBytes) + ew * 128;
     int cursor = 0, acc = 0;
     uint32_t acc_phase = 0, aux_phase = 0;
+    int ti = -1;
     for (int tile = first; tile < total; tile += stride) {
       const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
+      ++ti;
+      const bool tr = lane == 0 && (ew == 0 || ew == 4);
       const int c0 = hf * (M::kBN / 64);  // first 32-column chunk of this warp's half
       if (M::kRagK) {
         const int Md = M::wg_mdim(p), Nd = M::wg_ndim(p);
@@ -552,6 +587,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
           break;
         }
         ptx::tc_fence_after();
+        if (tr) trace(p, MODE, ew == 0 ? 4 : 6, ti);
         const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
         store_chunks(stage, tbase, c0, slab + t.n0, Nd, t.n0, lane, slab_rows);
       } else {
@@ -560,6 +596,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
           break;
         }
         ptx::tc_fence_after();
+        if (tr) trace(p, MODE, ew == 0 ? 4 : 6, ti);
         const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
         // this warp's 32-row slab of the tile, for the coalesced stores
         const size_t slab_row0 = (size_t)t.row0 + t.m0 + q * 32;
@@ -581,7 +618,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
             for (int i = 0; i < 32; ++i) {
               ag[i] = round_bf16(ag[i]);
               au[i] = round_bf16(au[i]);
-              hv[i] = ag[i] / (1.f + __expf(-ag[i])) * au[i];
+              hv[i] = ag[i] * fast_sigmoid(ag[i]) * au[i];
             }
             bf16* abase = p.out0 + slab_row0 * (size_t)(2 * p.F);
             warp_store32(stage, ag, abase + f, 2 * p.F, lane, slab_rows, cols_ok);
@@ -590,53 +627,62 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
                          cols_ok);
           }
         } else if (MODE == GEMM_FC2_DGRAD) {
-          // the tile's pre-activation slab: 4 TMA boxes of 128 rows x 64 columns
-          // (gate n0.., gate n0+64.., up n0.., up n0+64..), 128-byte swizzled:
-          // 16-byte chunk j of row r sits at chunk j ^ (r & 7)
-          if (!ptx::mbar_wait(&ctl.aux_full, aux_phase, &ctl.abort, kWaitLimitNs)) {
-            if (lane == 0) flag_timeout(ctl, p.status, 6);
-            break;
-          }
-          aux_phase ^= 1;
+          // the pre-activation slab arrives one 128-column half at a time: 4 TMA
+          // boxes of 128 rows x 64 columns (gate c.., gate c+64.., up c..,
+          // up c+64..), 128-byte swizzled: 16-byte chunk j of row r sits at
+          // chunk j ^ (r & 7). Each half is 4 chunks of 32 columns, 2 per warp.
           const uint8_t* aux = smem + M::kStages * M::kStageBytes;
           bf16* dbase = p.out0 + slab_row0 * (size_t)(2 * p.F);
+          bool ok_aux = true;
+          for (int half = 0; half < 2 && ok_aux; ++half) {
+            if (!ptx::mbar_wait(&ctl.aux_full, aux_phase, &ctl.abort, kWaitLimitNs)) {
+              if (lane == 0) flag_timeout(ctl, p.status, 6);
+              ok_aux = false;
+              break;
+            }
+            aux_phase ^= 1;
 #pragma unroll 1
-          for (int cc = c0; cc < c0 + M::kBN / 64; ++cc) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
-            const int box = cc >> 1, cb = (cc & 1) * 4;
-            uint4 gc[4], uc[4];
+            for (int j = 0; j < 2; ++j) {
+              const int ch = 2 * hf + j;   // chunk within the half
+              const int cc = 4 * half + ch;  // chunk within the tile
+              uint32_t v[32];
+              ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
+              const int box = ch >> 1, cb = (ch & 1) * 4;
+              uint4 gc[4], uc[4];
 #pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-              const int off = r * 128 + (((cb + k2) ^ (r & 7)) * 16);
-              gc[k2] = *reinterpret_cast<const uint4*>(aux + box * 16384 + off);
-              uc[k2] = *reinterpret_cast<const uint4*>(aux + (2 + box) * 16384 + off);
-            }
-            ptx::tmem_ld_wait(v);
-            const int f = t.n0 + 32 * cc;
-            const bool cols_ok = f < p.F;
-            float out[32];
+              for (int k2 = 0; k2 < 4; ++k2) {
+                const int off = r * 128 + (((cb + k2) ^ (r & 7)) * 16);
+                gc[k2] = *reinterpret_cast<const uint4*>(aux + box * 16384 + off);
+                uc[k2] = *reinterpret_cast<const uint4*>(aux + (2 + box) * 16384 + off);
+              }
+              ptx::tmem_ld_wait(v);
+              const int f = t.n0 + 32 * cc;
+              const bool cols_ok = f < p.F;
+              float out[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {  // da_up = dh * silu(a_g)
-              const float ag = bf16_at(gc, i);
-              out[i] = __uint_as_float(v[i]) * ag / (1.f + __expf(-ag));
-            }
-            warp_store32(stage, out, dbase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
+              for (int i = 0; i < 32; ++i) {  // da_up = dh * silu(a_g)
+                const float ag = bf16_at(gc, i);
+                out[i] = __uint_as_float(v[i]) * ag * fast_sigmoid(ag);
+              }
+              warp_store32(stage, out, dbase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {  // da_gate = dh * a_u * silu'(a_g)
-              const float ag = bf16_at(gc, i);
-              const float sg = 1.f / (1.f + __expf(-ag));
-              out[i] = __uint_as_float(v[i]) * bf16_at(uc, i) * sg * (1.f + ag * (1.f - sg));
+              for (int i = 0; i < 32; ++i) {  // da_gate = dh * a_u * silu'(a_g)
+                const float ag = bf16_at(gc, i);
+                const float sg = fast_sigmoid(ag);
+                out[i] = __uint_as_float(v[i]) * bf16_at(uc, i) * sg * (1.f + ag * (1.f - sg));
+              }
+              warp_store32(stage, out, dbase + f, 2 * p.F, lane, slab_rows, cols_ok);
             }
-            warp_store32(stage, out, dbase + f, 2 * p.F, lane, slab_rows, cols_ok);
+            ptx::mbar_arrive(&ctl.aux_empty);
           }
-          ptx::mbar_arrive(&ctl.aux_empty);
+          if (!ok_aux) break;
         } else {
           const int Nd = MODE == GEMM_FC2_FWD || MODE == GEMM_FC1_DGRAD ? p.H : p.F;
           store_chunks(stage, tbase, c0, p.out0 + slab_row0 * (size_t)Nd + t.n0, Nd, t.n0, lane,
                        slab_rows);
         }
       }
+      if (tr) trace(p, MODE, ew == 0 ? 5 : 7, ti);
       ptx::tc_fence_before();
       if (M::kPair && crank != 0)
         ptx::mbar_arrive_cluster(ptx::mapa_shared(&ctl.tmem_empty[acc], 0));
