@@ -394,6 +394,59 @@ def run_reference(args, rank, world):
                   "d2h_bytes_per_step": 0}})
 
 
+# ----------------------------------------------------------------------------- schedule
+def run_schedule(args):
+    """Two micro-batches through the scheduler: serial vs overlapped step time and
+    the communication time hidden behind the expert GEMMs (interval analysis)."""
+    import moe_synth
+    import combine_router_softmax_top_gb300 as moe
+    from combine_router_softmax_top_gb300 import build
+
+    build.build()
+    wl = "two_microbatch"
+    i0, i1 = moe_synth.workload(wl, 0), moe_synth.workload(wl, 1)
+    d = moe.LayerDesc.of(**i0.shape_dict())
+    b0 = moe.LayerBuffers(d)
+    b0.load_inputs(i0)
+    b1 = moe.LayerBuffers(d, weights=b0)
+    b1.load_inputs(i1, weights=False)
+    sc = torch.cuda.Stream(priority=-1)
+    sg = torch.cuda.Stream()
+    res = {}
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for name, overlap, defer, cap in (("serial", 0, 0, 0), ("overlap", 1, 0, 0),
+                                      ("overlap_defer", 1, 1, 0),
+                                      ("overlap_defer_gemm136", 1, 1, sms - 16),
+                                      ("overlap_defer_gemm120", 1, 1, sms - 32)):
+        s = moe.Scheduler(d, sc, sg, gemm_sms=cap)
+        for _ in range(args.warmup):
+            s.step(b0, b1, overlap=bool(overlap), defer_wgrad=bool(defer))
+        s.flush()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(sc)
+        for _ in range(args.steps):
+            s.step(b0, b1, overlap=bool(overlap), defer_wgrad=bool(defer))
+        e1.record(sc)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        tm = s.timings()
+        comm, gemm, hidden = moe.interval_overlap(tm)
+        s.flush()
+        torch.cuda.synchronize()
+        s.close()
+        res[name] = {"ms_per_step": round(ms, 4), "comm_union_ms": round(comm, 4),
+                     "gemm_union_ms": round(gemm, 4), "hidden_comm_ms": round(hidden, 4),
+                     "gemm_sms": cap or sms}
+    for b in (b0, b1):
+        assert moe.moe_device_status(d, b.ws) == moe.MOE_OK
+    emit({"metric": "two-micro-batch MoE layer step, serial vs two-stream overlap",
+          "unit": "ms", "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+          "config": {"workload": wl, **i0.shape_dict(), "micro_batches": 2},
+          "schedules": res,
+          "tokens_per_s_best": round(2 * i0.T / (min(v["ms_per_step"] for v in res.values()) / 1e3), 1)})
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -404,10 +457,14 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
     ap.add_argument("--ref-sample-tokens", type=int, default=64)
+    ap.add_argument("--schedule", action="store_true",
+                    help="time the two-micro-batch scheduler (serial vs overlap) instead")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps, always
     rank, world, local = dist_setup()
-    if args.impl == "reference":
+    if args.schedule:
+        run_schedule(args)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)

@@ -345,8 +345,9 @@ class Scheduler:
 
 
 def interval_overlap(timings):
-    """Union of comm-stream intervals, union of GEMM-stream intervals, and the
-    length of their intersection (the hidden communication), in ms, measured
+    """Union of the dispatch/combine (communication) phase intervals, union of
+    the expert-GEMM phase intervals, and the length of their intersection (the
+    hidden communication), in ms, measured
     as the EP-overlap skill card's profiling section prescribes (interval
     unions and their intersection, never a sum of kernel durations)."""
     def union(iv):
@@ -359,8 +360,9 @@ def interval_overlap(timings):
                 out.append([s, e])
         return out
 
-    comm = union([(t["start_ms"], t["end_ms"]) for t in timings if t["stream"] == 0])
-    gemm = union([(t["start_ms"], t["end_ms"]) for t in timings if t["stream"] == 1])
+    gemm_phases = ("ffn_fwd", "dgrad", "wgrad")
+    comm = union([(t["start_ms"], t["end_ms"]) for t in timings if t["phase"] not in gemm_phases])
+    gemm = union([(t["start_ms"], t["end_ms"]) for t in timings if t["phase"] in gemm_phases])
     inter = 0.0
     for a0, a1 in comm:
         for b0, b1 in gemm:

@@ -81,14 +81,14 @@ struct Mode {
   static constexpr int kCS = kPair ? 2 : kRagK ? 4 : MOE_ROW_CS;
   // The FC2 dgrad epilogue needs the tile's saved pre-activation (gate and up)
   // next to the accumulator: a dedicated warp TMA-loads it into shared memory
-  // ahead of the epilogue, one 128-column half (64 KB) at a time.
+  // ahead of the epilogue, one 64-column quarter (gate and up, 32 KB) at a time.
   static constexpr bool kAux = MODE == GEMM_FC2_DGRAD;
   static constexpr int kBN = 256;
   static constexpr int kBBytes = kBN * BK * 2;            // whole B tile per stage
   static constexpr int kBBytesCta = kPair ? kBBytes / 2 : kBBytes;  // B bytes this CTA loads
   static constexpr int kStageBytes = kABytes + kBBytesCta;
-  static constexpr int kStages = kPair ? (kAux ? 4 : 6) : 4;
-  static constexpr int kAuxBytes = kAux ? 4 * 16384 : 0;
+  static constexpr int kStages = kPair ? (kAux ? 5 : 6) : 4;
+  static constexpr int kAuxBytes = kAux ? 2 * 16384 : 0;
   static constexpr int kWarps = kAux ? 11 : 10;  // producer, MMA, 8 epilogue (+ aux loader)
   static constexpr size_t kDynSmem =
       (size_t)kStages * kStageBytes + kAuxBytes + kEpiStageBytes + 1024;
@@ -238,10 +238,13 @@ __device__ __forceinline__ void store_chunks(uint4* stage, uint32_t tbase, int c
   }
 }
 
-// Logistic sigmoid with the hardware exponential and reciprocal (a few ulp;
-// the epilogue rounds its results to bf16 anyway).
+// Logistic sigmoid from the identity s(x) = (1 + tanh(x/2)) / 2, with the
+// hardware tanh approximation (one MUFU op; relative error ~2^-11, below the
+// bf16 rounding the epilogue applies to its results).
 __device__ __forceinline__ float fast_sigmoid(float x) {
-  return __frcp_rn(1.f + __expf(-x));
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return fmaf(0.5f, t, 0.5f);
 }
 
 __device__ __forceinline__ float round_bf16(float x) {
@@ -521,8 +524,8 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     __syncwarp();
   } else if (M::kAux && warp == 10) {
     // ================================================================ aux loader
-    // Loads each tile's saved pre-activation, a 128-column half at a time, each
-    // once the epilogue has released the previous half.
+    // Loads each tile's saved pre-activation, a 64-column quarter at a time,
+    // each once the epilogue has released the previous quarter.
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmC);
       int cursor = 0;
@@ -536,18 +539,16 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         ph ^= 1;
         uint8_t* aux = smem + M::kStages * M::kStageBytes;
         const int row = t.row0 + t.m0;
-        for (int half = 0; half < 2; ++half) {
-          if (half == 1 && !ptx::mbar_wait(&ctl.aux_empty, ph ^ 1, &ctl.abort, kWaitLimitNs)) {
+        for (int qt = 0; qt < M::kBN / 64; ++qt) {
+          if (qt > 0 && !ptx::mbar_wait(&ctl.aux_empty, ph ^ 1, &ctl.abort, kWaitLimitNs)) {
             flag_timeout(ctl, p.status, 7);
             break;
           }
-          if (half == 1) ph ^= 1;
-          const int c = t.n0 + 128 * half;
+          if (qt > 0) ph ^= 1;
+          const int c = t.n0 + 64 * qt;
           ptx::mbar_arrive_expect_tx(&ctl.aux_full, M::kAuxBytes);
-          ptx::tma_load_2d(aux, &tmC, &ctl.aux_full, c, row);
-          ptx::tma_load_2d(aux + 16384, &tmC, &ctl.aux_full, c + 64, row);
-          ptx::tma_load_2d(aux + 2 * 16384, &tmC, &ctl.aux_full, p.F + c, row);
-          ptx::tma_load_2d(aux + 3 * 16384, &tmC, &ctl.aux_full, p.F + c + 64, row);
+          ptx::tma_load_2d(aux, &tmC, &ctl.aux_full, c, row);                  // gate
+          ptx::tma_load_2d(aux + 16384, &tmC, &ctl.aux_full, p.F + c, row);    // up
         }
       }
     }
@@ -627,53 +628,49 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
                          cols_ok);
           }
         } else if (MODE == GEMM_FC2_DGRAD) {
-          // the pre-activation slab arrives one 128-column half at a time: 4 TMA
-          // boxes of 128 rows x 64 columns (gate c.., gate c+64.., up c..,
-          // up c+64..), 128-byte swizzled: 16-byte chunk j of row r sits at
-          // chunk j ^ (r & 7). Each half is 4 chunks of 32 columns, 2 per warp.
+          // the pre-activation slab arrives one 64-column quarter at a time: a
+          // gate box and an up box of 128 rows x 64 columns, 128-byte swizzled
+          // (16-byte chunk j of row r sits at chunk j ^ (r & 7)). A quarter is
+          // 2 chunks of 32 columns; each warp takes one.
           const uint8_t* aux = smem + M::kStages * M::kStageBytes;
           bf16* dbase = p.out0 + slab_row0 * (size_t)(2 * p.F);
           bool ok_aux = true;
-          for (int half = 0; half < 2 && ok_aux; ++half) {
+          for (int qt = 0; qt < M::kBN / 64 && ok_aux; ++qt) {
             if (!ptx::mbar_wait(&ctl.aux_full, aux_phase, &ctl.abort, kWaitLimitNs)) {
               if (lane == 0) flag_timeout(ctl, p.status, 6);
               ok_aux = false;
               break;
             }
             aux_phase ^= 1;
-#pragma unroll 1
-            for (int j = 0; j < 2; ++j) {
-              const int ch = 2 * hf + j;   // chunk within the half
-              const int cc = 4 * half + ch;  // chunk within the tile
-              uint32_t v[32];
-              ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
-              const int box = ch >> 1, cb = (ch & 1) * 4;
-              uint4 gc[4], uc[4];
+            const int cc = 2 * qt + hf;  // chunk within the tile
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
+            const int cb = hf * 4;
+            uint4 gc[4], uc[4];
 #pragma unroll
-              for (int k2 = 0; k2 < 4; ++k2) {
-                const int off = r * 128 + (((cb + k2) ^ (r & 7)) * 16);
-                gc[k2] = *reinterpret_cast<const uint4*>(aux + box * 16384 + off);
-                uc[k2] = *reinterpret_cast<const uint4*>(aux + (2 + box) * 16384 + off);
-              }
-              ptx::tmem_ld_wait(v);
-              const int f = t.n0 + 32 * cc;
-              const bool cols_ok = f < p.F;
-              float out[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {  // da_up = dh * silu(a_g)
-                const float ag = bf16_at(gc, i);
-                out[i] = __uint_as_float(v[i]) * ag * fast_sigmoid(ag);
-              }
-              warp_store32(stage, out, dbase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {  // da_gate = dh * a_u * silu'(a_g)
-                const float ag = bf16_at(gc, i);
-                const float sg = fast_sigmoid(ag);
-                out[i] = __uint_as_float(v[i]) * bf16_at(uc, i) * sg * (1.f + ag * (1.f - sg));
-              }
-              warp_store32(stage, out, dbase + f, 2 * p.F, lane, slab_rows, cols_ok);
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const int off = r * 128 + (((cb + k2) ^ (r & 7)) * 16);
+              gc[k2] = *reinterpret_cast<const uint4*>(aux + off);
+              uc[k2] = *reinterpret_cast<const uint4*>(aux + 16384 + off);
             }
-            ptx::mbar_arrive(&ctl.aux_empty);
+            ptx::tmem_ld_wait(v);
+            const int f = t.n0 + 32 * cc;
+            const bool cols_ok = f < p.F;
+            float out[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {  // da_up = dh * silu(a_g)
+              const float ag = bf16_at(gc, i);
+              out[i] = __uint_as_float(v[i]) * ag * fast_sigmoid(ag);
+            }
+            ptx::mbar_arrive(&ctl.aux_empty);  // the quarter is in registers now
+            warp_store32(stage, out, dbase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {  // da_gate = dh * a_u * silu'(a_g)
+              const float ag = bf16_at(gc, i);
+              const float sg = fast_sigmoid(ag);
+              out[i] = __uint_as_float(v[i]) * bf16_at(uc, i) * sg * (1.f + ag * (1.f - sg));
+            }
+            warp_store32(stage, out, dbase + f, 2 * p.F, lane, slab_rows, cols_ok);
           }
           if (!ok_aux) break;
         } else {

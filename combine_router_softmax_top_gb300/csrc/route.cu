@@ -9,11 +9,14 @@
 
 #include "moe_internal.cuh"
 
+#ifndef MOE_ROUTE_TPL
+#define MOE_ROUTE_TPL 4
+#endif
+
 namespace moe {
 
 namespace {
 
-constexpr int kRouteTok = 64;   // tokens per CTA: lane owns tokens lane and lane + 32
 constexpr int kRouteHc = 32;    // hidden elements per chunk
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
@@ -42,12 +45,13 @@ __device__ __forceinline__ void unpack8_f32(const uint4& v, float (&f)[8]) {
 // one barrier per chunk).
 constexpr int kRouteXPitchB = 80;  // bytes per staged x row (64 B of data)
 
-template <int NW, int kRouteEpw>
+template <int NW, int kRouteEpw, int TPL>
 __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __restrict__ x,
                                                                const bf16* __restrict__ w_r,
                                                                const float* __restrict__ bias,
                                                                float* __restrict__ z, int T,
                                                                int H, int E) {
+  constexpr int kRouteTok = 32 * TPL;  // tokens per CTA: lane owns tokens lane + 32u
   constexpr int kThreads = NW * 32;
   constexpr int eb = NW * kRouteEpw;              // experts in this CTA
   constexpr int nxp = kRouteTok * (kRouteHc / 8);  // 16-byte pieces of an x chunk (256)
@@ -60,9 +64,9 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
   const int t0 = blockIdx.x * kRouteTok;
   const int e0 = blockIdx.y * eb;
 
-  float acc[2][kRouteEpw];
+  float acc[TPL][kRouteEpw];
 #pragma unroll
-  for (int u = 0; u < 2; ++u)
+  for (int u = 0; u < TPL; ++u)
 #pragma unroll
     for (int i = 0; i < kRouteEpw; ++i) acc[u][i] = 0.f;
 
@@ -100,20 +104,21 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
     }
     __syncthreads();
     if (ch + 1 < nchunks) fetch(ch + 1, rx, rw);
-    const uint8_t* xa = &xs[b][lane * kRouteXPitchB];
-    const uint8_t* xb = &xs[b][(lane + 32) * kRouteXPitchB];
     const float* wb = &ws[b][warp * kRouteEpw][0];
     // w_r values of the next 4-wide h step are loaded before the FMAs of the
     // current one, so shared-memory latency overlaps the arithmetic
     float4 wn[kRouteEpw];
 #pragma unroll
     for (int i = 0; i < kRouteEpw; ++i) wn[i] = *reinterpret_cast<const float4*>(wb + i * kRouteHc);
-    float x0[8], x1[8];
+    float xv[TPL][8];
 #pragma unroll
     for (int s4 = 0; s4 < kRouteHc / 4; ++s4) {
       if ((s4 & 1) == 0) {
-        unpack8_f32(*reinterpret_cast<const uint4*>(xa + (s4 >> 1) * 16), x0);
-        unpack8_f32(*reinterpret_cast<const uint4*>(xb + (s4 >> 1) * 16), x1);
+#pragma unroll
+        for (int u = 0; u < TPL; ++u)
+          unpack8_f32(*reinterpret_cast<const uint4*>(&xs[b][(lane + 32 * u) * kRouteXPitchB] +
+                                                      (s4 >> 1) * 16),
+                      xv[u]);
       }
       float4 wc[kRouteEpw];
 #pragma unroll
@@ -126,19 +131,18 @@ __global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __res
       const int hh = (s4 & 1) * 4;
 #pragma unroll
       for (int i = 0; i < kRouteEpw; ++i) {
-        acc[0][i] = fmaf(x0[hh + 0], wc[i].x, acc[0][i]);
-        acc[1][i] = fmaf(x1[hh + 0], wc[i].x, acc[1][i]);
-        acc[0][i] = fmaf(x0[hh + 1], wc[i].y, acc[0][i]);
-        acc[1][i] = fmaf(x1[hh + 1], wc[i].y, acc[1][i]);
-        acc[0][i] = fmaf(x0[hh + 2], wc[i].z, acc[0][i]);
-        acc[1][i] = fmaf(x1[hh + 2], wc[i].z, acc[1][i]);
-        acc[0][i] = fmaf(x0[hh + 3], wc[i].w, acc[0][i]);
-        acc[1][i] = fmaf(x1[hh + 3], wc[i].w, acc[1][i]);
+#pragma unroll
+        for (int u = 0; u < TPL; ++u) {
+          acc[u][i] = fmaf(xv[u][hh + 0], wc[i].x, acc[u][i]);
+          acc[u][i] = fmaf(xv[u][hh + 1], wc[i].y, acc[u][i]);
+          acc[u][i] = fmaf(xv[u][hh + 2], wc[i].z, acc[u][i]);
+          acc[u][i] = fmaf(xv[u][hh + 3], wc[i].w, acc[u][i]);
+        }
       }
     }
   }
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
+  for (int u = 0; u < TPL; ++u) {
     const int t = t0 + lane + 32 * u;
     if (t >= T) continue;
 #pragma unroll
@@ -441,20 +445,21 @@ moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* 
                           int* status, cudaStream_t st) {
   (void)status;
   if (d.T == 0) return MOE_OK;
-  // 4 warps x 4 experts (16 experts, 64 tokens) per CTA: 2 x 4 accumulators per
-  // thread keep the FMA : shared-wavefront ratio at 1 while giving the SMs
-  // enough warps to hide shared-memory latency; small E gets fewer warps.
+  // 4 warps x 4 experts per CTA, ROUTE_TPL tokens per lane: 2 x 4 or 4 x 4
+  // accumulators per thread keep the FMA : shared-wavefront ratio at or above 1
+  // while giving the SMs enough warps to hide shared-memory latency.
+  constexpr int tpl = MOE_ROUTE_TPL;
   const int nw = d.E > 8 ? 4 : d.E > 4 ? 2 : 1;
   const int eb = nw * 4;
-  dim3 grid(ceil_div(d.T, kRouteTok), ceil_div(d.E, eb));
+  dim3 grid(ceil_div(d.T, 32 * tpl), ceil_div(d.E, eb));
   {
     LaunchScope _ls(K_ROUTE_LOGITS, st);
     if (nw == 4)
-      route_logits_kernel<4, 4><<<grid, 128, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+      route_logits_kernel<4, 4, tpl><<<grid, 128, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
     else if (nw == 2)
-      route_logits_kernel<2, 4><<<grid, 64, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+      route_logits_kernel<2, 4, tpl><<<grid, 64, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
     else
-      route_logits_kernel<1, 4><<<grid, 32, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+      route_logits_kernel<1, 4, tpl><<<grid, 32, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
   }
   moe_status_t s = check_launch("route_logits_kernel");
   if (s != MOE_OK) return s;
