@@ -305,3 +305,14 @@ def test_oracle_regression_fixture():
     for key, val in stored.items():
         np.testing.assert_allclose(np.asarray(now[key], np.float64), np.asarray(val, np.float64),
                                    rtol=1e-12, atol=0, err_msg=key)
+
+
+def test_logit_summation_order_is_ascending_h():
+    """The fp32 router sum adds h = 0, 1, 2, ... in turn: 1 + 2^-24 + 2^-24 rounds
+    to 1 at each step (ties to even), while the reverse order first makes 2^-23
+    and then lands on 1 + 2^-23. Any other order gives a different bit pattern."""
+    x = np.array([[1.0, 2.0 ** -24, 2.0 ** -24]])
+    w = np.ones((1, 3))
+    assert O.router_logits_fp32(x, w)[0, 0] == np.float32(1.0)
+    x_rev = x[:, ::-1].copy()
+    assert O.router_logits_fp32(x_rev, w)[0, 0] == np.float32(1.0 + 2.0 ** -23)
