@@ -90,6 +90,12 @@ struct Mode {
   static constexpr int kStages = kPair ? (kAux ? 5 : 6) : 4;
   static constexpr int kAuxBytes = kAux ? 2 * 16384 : 0;
   static constexpr int kWarps = kAux ? 11 : 10;  // producer, MMA, 8 epilogue (+ aux loader)
+  // Plain bf16 outputs leave through TMA tensor stores of 32 x 32 boxes (the
+  // staging buffer is the box): 2D [rows, cols] maps for the forward FC2 and
+  // FC1 dgrad outputs, 3D [expert, rows, cols] maps for the weight gradients,
+  // whose clipping at the matrix edge makes every wgrad box storable. 0: none.
+  static constexpr int kStoreDims =
+      (MODE == GEMM_FC2_FWD || MODE == GEMM_FC1_DGRAD) ? 2 : kRagK ? 3 : 0;
   static constexpr size_t kDynSmem =
       (size_t)kStages * kStageBytes + kAuxBytes + kEpiStageBytes + 1024;
   static_assert(kStages <= kStagesMax, "barrier arrays");
@@ -221,8 +227,17 @@ __device__ __forceinline__ float bf16_at(const uint4 (&u)[4], int i) {
 // Stores this warp's half of a plain fp32 accumulator tile (BN/64 chunks of 32
 // columns starting at chunk c0) as bf16; the TMEM load of the next chunk is in
 // flight while the current one is written out.
+//
+// With a store map (dims 2 or 3) each 32 x 32 chunk goes out as one TMA store
+// of the staging buffer at box (x0 + 32 * chunk, y0[, z0]); lane 0 issues it
+// and, before the buffer is rewritten, waits until the previous store has read
+// it. A 2D map spans all rows of the output, so a slab with fewer than 32 valid
+// rows (the rows past it belong to the next expert) takes the plain stores.
 __device__ __forceinline__ void store_chunks(uint4* stage, uint32_t tbase, int c0, bf16* slab,
-                                             int ld, int n0, int lane, int slab_rows) {
+                                             int ld, int n0, int lane, int slab_rows,
+                                             const CUtensorMap* tm, int dims, int x0, int y0,
+                                             int z0) {
+  const bool tma = dims == 3 || (dims == 2 && slab_rows == 32);
   uint32_t va[32], vb[32];
   ptx::tmem_ld_32x32b_x32(tbase + 32 * c0, va);
   ptx::tmem_ld_wait(va);
@@ -232,8 +247,33 @@ __device__ __forceinline__ void store_chunks(uint4* stage, uint32_t tbase, int c
     uint32_t(&cur)[32] = (i & 1) ? vb : va;
     uint32_t(&nxt)[32] = (i & 1) ? va : vb;
     if (i + 1 < BN / 64) ptx::tmem_ld_32x32b_x32(tbase + 32 * (cc + 1), nxt);
-    warp_store32(stage, reinterpret_cast<float*>(cur), slab + 32 * cc, ld, lane, slab_rows,
-                 n0 + 32 * cc < ld);
+    const bool cols_ok = n0 + 32 * cc < ld;
+    if (tma) {
+      if (slab_rows > 0 && cols_ok) {
+        if (lane == 0) ptx::bulk_wait_group_read0();
+        __syncwarp();
+        const float* v = reinterpret_cast<const float*>(cur);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          stage[lane * 4 + (q ^ ((lane >> 1) & 3))] = make_uint4(
+              pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+              pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (dims == 3) ptx::tma_store_3d(tm, stage, x0 + 32 * cc, y0, z0);
+          else ptx::tma_store_2d(tm, stage, x0 + 32 * cc, y0);
+          ptx::bulk_commit_group();
+        }
+      }
+    } else {
+      if (dims) {
+        if (lane == 0) ptx::bulk_wait_group_read0();
+        __syncwarp();
+      }
+      warp_store32(stage, reinterpret_cast<float*>(cur), slab + 32 * cc, ld, lane, slab_rows,
+                   cols_ok);
+    }
     if (i + 1 < BN / 64) ptx::tmem_ld_wait(nxt);
   }
 }
@@ -255,7 +295,8 @@ template <int MODE>
 __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmC,
+                        const __grid_constant__ CUtensorMap tmD, const KParams p) {
   using M = Mode<MODE>;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ SmemCtl ctl;
@@ -576,9 +617,13 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         const int slab_rows = min(32, Md - (t.m0 + q * 32));
         bf16* slab = outp + (size_t)(t.m0 + q * 32) * Nd;
         if (t.nk == 0) {
+          // an expert with no rows: zero weight gradient (plain stores, after
+          // the last TMA store has finished reading the staging buffer)
           float z[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) z[i] = 0.f;
+          if (lane == 0) ptx::bulk_wait_group_read0();
+          __syncwarp();
           for (int cc = c0; cc < c0 + BN / 64; ++cc)
             warp_store32(stage, z, slab + t.n0 + 32 * cc, Nd, lane, slab_rows, t.n0 + 32 * cc < Nd);
           continue;
@@ -590,7 +635,8 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         ptx::tc_fence_after();
         if (tr) trace(p, MODE, ew == 0 ? 4 : 6, ti);
         const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-        store_chunks(stage, tbase, c0, slab + t.n0, Nd, t.n0, lane, slab_rows);
+        store_chunks(stage, tbase, c0, slab + t.n0, Nd, t.n0, lane, slab_rows, &tmD, M::kStoreDims,
+                     t.n0, t.m0 + q * 32, t.e);
       } else {
         if (!ptx::mbar_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
           if (lane == 0) flag_timeout(ctl, p.status, 5);
@@ -676,7 +722,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         } else {
           const int Nd = MODE == GEMM_FC2_FWD || MODE == GEMM_FC1_DGRAD ? p.H : p.F;
           store_chunks(stage, tbase, c0, p.out0 + slab_row0 * (size_t)Nd + t.n0, Nd, t.n0, lane,
-                       slab_rows);
+                       slab_rows, &tmD, M::kStoreDims, t.n0, (int)slab_row0, 0);
         }
       }
       if (tr) trace(p, MODE, ew == 0 ? 5 : 7, ti);
@@ -690,6 +736,9 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         acc_phase ^= 1;
       }
     }
+    // the staging buffers and the outputs must outlive the TMA stores
+    if (M::kStoreDims && lane == 0) ptx::bulk_wait_group0();
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -744,9 +793,34 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
   return true;
 }
 
+// Store map of a bf16 output: 2D [rows, cols] or 3D [experts, rows, cols],
+// row-major, box 32 columns x 32 rows (x 1 expert), 64-byte swizzle (the
+// staging buffer's layout: 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)).
+bool make_store_map(CUtensorMap* m, void* base, long long experts, long long rows, long long cols,
+                    int dims) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return false;
+  }
+  cuuint64_t dim[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)experts};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(rows * cols * 2)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dims, base, dim, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d) for a %lld x %lld x %lld store map", (int)r,
+              experts, rows, cols);
+    return false;
+  }
+  return true;
+}
+
 template <int MODE>
 moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                         const KParams& p, int grid,
+                         const CUtensorMap& dmap, const KParams& p, int grid,
                          cudaStream_t st) {
   constexpr int cs = Mode<MODE>::kCS;
   static std::once_flag once;
@@ -778,7 +852,7 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUten
   }
   LaunchScope _ls(K_GEMM_FC1_FWD + MODE, st);
   if (cs == 1) {
-    grouped_gemm_kernel<MODE><<<grid, Mode<MODE>::kWarps * 32, Mode<MODE>::kDynSmem, st>>>(a, b, c, p);
+    grouped_gemm_kernel<MODE><<<grid, Mode<MODE>::kWarps * 32, Mode<MODE>::kDynSmem, st>>>(a, b, c, dmap, p);
     return check_launch("grouped_gemm_kernel");
   }
   int clusters = (grid + cs - 1) / cs;
@@ -796,7 +870,7 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUten
   cfg.stream = st;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, b, c, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, b, c, dmap, p);
   if (e != cudaSuccess) {
     set_error("grouped_gemm_kernel cluster launch: %s", cudaGetErrorString(e));
     return MOE_ERR_CUDA;
@@ -820,7 +894,7 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
     }
     return MOE_OK;
   }
-  CUtensorMap ma, mb, mc;
+  CUtensorMap ma, mb, mc, md;
   bool ok = true;
   long long ntile_bound = 0;  // upper bound on tiles, for the grid size
   switch (g.mode) {
@@ -855,6 +929,14 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
   }
   if (!ok) return MOE_ERR_CUDA;
   if (g.mode != GEMM_FC2_DGRAD) mc = ma;  // only FC2 dgrad reads a third tensor
+  switch (g.mode) {  // the outputs written by TMA stores
+    case GEMM_FC2_FWD:
+    case GEMM_FC1_DGRAD: ok = make_store_map(&md, g.out0, 1, N, H, 2); break;
+    case GEMM_WGRAD_W1: ok = make_store_map(&md, g.out0, E, 2 * F, H, 3); break;
+    case GEMM_WGRAD_W2: ok = make_store_map(&md, g.out1, E, H, F, 3); break;
+    default: md = ma;
+  }
+  if (!ok) return MOE_ERR_CUDA;
   KParams p;
   p.E = E;
   p.H = H;
@@ -869,12 +951,12 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
   if (g.max_ctas > 0 && g.max_ctas < grid) grid = g.max_ctas;
   if (ntile_bound < grid) grid = (int)(ntile_bound > 0 ? ntile_bound : 1);
   switch (g.mode) {
-    case GEMM_FC1_FWD: return launch_mode<GEMM_FC1_FWD>(ma, mb, mc, p, grid, st);
-    case GEMM_FC2_FWD: return launch_mode<GEMM_FC2_FWD>(ma, mb, mc, p, grid, st);
-    case GEMM_FC2_DGRAD: return launch_mode<GEMM_FC2_DGRAD>(ma, mb, mc, p, grid, st);
-    case GEMM_FC1_DGRAD: return launch_mode<GEMM_FC1_DGRAD>(ma, mb, mc, p, grid, st);
-    case GEMM_WGRAD_W1: return launch_mode<GEMM_WGRAD_W1>(ma, mb, mc, p, grid, st);
-    default: return launch_mode<GEMM_WGRAD_W2>(ma, mb, mc, p, grid, st);
+    case GEMM_FC1_FWD: return launch_mode<GEMM_FC1_FWD>(ma, mb, mc, md, p, grid, st);
+    case GEMM_FC2_FWD: return launch_mode<GEMM_FC2_FWD>(ma, mb, mc, md, p, grid, st);
+    case GEMM_FC2_DGRAD: return launch_mode<GEMM_FC2_DGRAD>(ma, mb, mc, md, p, grid, st);
+    case GEMM_FC1_DGRAD: return launch_mode<GEMM_FC1_DGRAD>(ma, mb, mc, md, p, grid, st);
+    case GEMM_WGRAD_W1: return launch_mode<GEMM_WGRAD_W1>(ma, mb, mc, md, p, grid, st);
+    default: return launch_mode<GEMM_WGRAD_W2>(ma, mb, mc, md, p, grid, st);
   }
 }
 
