@@ -37,6 +37,10 @@ METRIC = "MoE layer fwd+bwd tokens/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 FMA lanes x 2 flop x 2.07 GHz (max SM clock)
+FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# kernels whose floor is fp32 FMA arithmetic, not memory (fixed-order fp32 router sums)
+ALU_BOUND = ("route_logits",)
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -59,7 +63,9 @@ def algorithmic(d) -> dict:
     N = T * k
     b2, b4 = 2, 4
     out = {
-        "route_logits": (T * H * b2 + E * H * b2 + T * E * b4, 2.0 * T * H * E),
+        # with E <= 128 the routing (top-k, gates) is fused into the logits kernel
+        "route_logits": (T * H * b2 + E * H * b2 + T * E * b4 + (2 * N * b4 if E <= 128 else 0),
+                         2.0 * T * H * E),
         "route_topk": (T * E * b4 + 2 * N * b4, 0.0),
         "layout_count": (N * b4, 0.0),
         "layout_assign": (N * b4 + 2 * N * b4, 0.0),
@@ -68,6 +74,8 @@ def algorithmic(d) -> dict:
         "combine_bwd": (T * H * b2 + N * H * b2 + 2 * N * b4 + N * H * b2 + N * b4, 3.0 * N * H),
         "permute_bwd": (N * H * b2 + N * b4 + T * H * b4, 1.0 * N * H),
         "route_bwd_dx": (T * H * b4 + E * H * b2 + 3 * N * b4 + T * H * b2, 2.0 * N * H),
+        # permute backward fused with the router's dx pass (the layer path)
+        "dispatch_bwd": (N * H * b2 + 4 * N * b4 + E * H * b2 + T * H * b2, 3.0 * N * H),
         "route_bwd_dwr_partial": (T * H * b2 + 2 * N * b4, 2.0 * N * H),
         "route_bwd_dwr_reduce": (E * H * b4, 0.0),
         "gemm_fc1_fwd": (N * H * b2 + E * 2 * F * H * b2 + N * 2 * F * b2 + N * F * b2,
@@ -87,6 +95,7 @@ KERNEL_SOURCES = {  # the files each kernel family is built from
     "layout": ("layout.cu", "moe_internal.cuh"),
     "permute": ("permute.cu", "moe_internal.cuh"),
     "combine": ("permute.cu", "moe_internal.cuh"),
+    "dispatch": ("route.cu", "moe_internal.cuh"),
 }
 
 
@@ -289,8 +298,12 @@ def run_ours(args, rank, world, local):
         tfl = fl / (avg_ms * 1e-3) / 1e12 if avg_ms > 0 else 0.0
         t_hbm = by / (pk["hbm_gbs"] * 1e9)
         t_tc = fl / (pk["bf16_tflops_sustained"] * 1e12) if name.startswith("gemm") else 0.0
+        t_alu = fl / (FP32_TFLOPS * 1e12) if name in ALU_BOUND else 0.0
         bound = "tensor" if t_tc > t_hbm else "hbm"
-        frac = (t_tc if bound == "tensor" else t_hbm) / (avg_ms * 1e-3) if avg_ms > 0 else 0.0
+        if t_alu > max(t_tc, t_hbm):
+            bound = "alu"
+        t_bound = {"tensor": t_tc, "hbm": t_hbm, "alu": t_alu}[bound]
+        frac = t_bound / (avg_ms * 1e-3) if avg_ms > 0 else 0.0
         kernels[name] = {"launches": n, "avg_us": round(avg_ms * 1e3, 2),
                          "share": None, "GB_s": round(gbs, 1), "TFLOP_s": round(tfl, 1),
                          "bound": bound, "roofline_frac": round(frac, 3),
@@ -303,6 +316,9 @@ def run_ours(args, rank, world, local):
     if kd["bound"] == "tensor":
         roof = {"bound": "tensor", "achieved": kd["TFLOP_s"], "peak": pk["bf16_tflops_sustained"],
                 "unit": "TFLOP/s"}
+    elif kd["bound"] == "alu":
+        roof = {"bound": "alu", "achieved": kd["TFLOP_s"], "peak": round(FP32_TFLOPS, 1),
+                "unit": "TFLOP/s"}
     else:
         roof = {"bound": "hbm", "achieved": kd["GB_s"], "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
@@ -312,7 +328,8 @@ def run_ours(args, rank, world, local):
     gemm_names = [n for n in kernels if n.startswith("gemm")]
     gemm_ms = sum(agg[n][1] for n in gemm_names) / args.steps
     gemm_fl = sum(algo[n][1] for n in gemm_names)
-    pc_names = [n for n in ("permute", "combine", "combine_bwd", "permute_bwd") if n in agg]
+    pc_names = [n for n in ("permute", "combine", "combine_bwd", "permute_bwd", "dispatch_bwd")
+                if n in agg]
     pc_ms = sum(agg[n][1] for n in pc_names) / args.steps
     pc_bytes = sum(algo[n][0] for n in pc_names)
 

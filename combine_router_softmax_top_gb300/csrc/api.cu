@@ -193,11 +193,13 @@ moe_status_t op_wgrad(const moe_layer_desc_t& d, const bf16* x_perm, const bf16*
 
 moe_status_t op_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,
                           const int32_t* idx, const bf16* x, const bf16* w_r,
-                          const int32_t* row_src, const int32_t* off, const float* dx32, bf16* dx,
-                          float* dw_r, void* ws, cudaStream_t st) {
+                          const int32_t* row_src, const int32_t* off, const float* dx32,
+                          const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dw_r,
+                          void* ws, cudaStream_t st) {
   const WsLayout w = ws_layout(d);
-  return launch_route_bwd(d, dgates, gates, idx, x, w_r, row_src, off, dx32, dx, dw_r,
-                          ws_at<float>(ws, w.dz), ws_at<float>(ws, w.dwr_part), status_of(ws), st);
+  return launch_route_bwd(d, dgates, gates, idx, x, w_r, row_src, off, dx32, dx_perm, slot, dx,
+                          dw_r, ws_at<float>(ws, w.dz), ws_at<float>(ws, w.dwr_part),
+                          status_of(ws), st);
 }
 
 moe_status_t op_dispatch(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st) {
@@ -239,9 +241,11 @@ moe_status_t op_dgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int 
 
 moe_status_t op_dispatch_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b,
                                 cudaStream_t st) {
-  MOE_CHECK(launch_permute_bwd(d, reinterpret_cast<const bf16*>(b->dx_perm), b->slot, b->dx32, st));
+  // the dispatch backward (row sums of dx_perm) is fused into the router's
+  // dx pass; dx32 is not written on this path
   return op_route_bwd(d, b->dgates, b->gates, b->idx, reinterpret_cast<const bf16*>(b->x),
-                      reinterpret_cast<const bf16*>(b->w_r), b->row_src, b->off, b->dx32,
+                      reinterpret_cast<const bf16*>(b->w_r), b->row_src, b->off, nullptr,
+                      reinterpret_cast<const bf16*>(b->dx_perm), b->slot,
                       reinterpret_cast<bf16*>(b->dx), b->dw_r, b->ws, st);
 }
 
@@ -401,8 +405,8 @@ moe_status_t moe_route_bwd(const moe_layer_desc_t* d, const float* dgates, const
   MOE_PTR(dgates); MOE_PTR(gates); MOE_PTR(idx); MOE_PTR(x); MOE_PTR(w_r); MOE_PTR(row_src);
   MOE_PTR(off); MOE_PTR(dx32); MOE_PTR(dx); MOE_PTR(dw_r);
   MOE_CHECK(check_ws(*d, ws, ws_bytes));
-  return op_route_bwd(*d, dgates, gates, idx, BF(x), BF(w_r), row_src, off, dx32, BFW(dx), dw_r,
-                      ws, S(stream));
+  return op_route_bwd(*d, dgates, gates, idx, BF(x), BF(w_r), row_src, off, dx32, nullptr,
+                      nullptr, BFW(dx), dw_r, ws, S(stream));
 }
 
 moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b, void* stream) {

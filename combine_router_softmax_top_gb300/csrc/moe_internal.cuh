@@ -35,7 +35,7 @@ enum KernelId {
   K_ROUTE_LOGITS = 0, K_ROUTE_TOPK, K_LAYOUT_COUNT, K_LAYOUT_ASSIGN, K_PERMUTE, K_COMBINE,
   K_COMBINE_BWD, K_PERMUTE_BWD, K_ROUTE_BWD_DX, K_ROUTE_BWD_DWR_PARTIAL, K_ROUTE_BWD_DWR_REDUCE,
   K_GEMM_FC1_FWD, K_GEMM_FC2_FWD, K_GEMM_FC2_DGRAD, K_GEMM_FC1_DGRAD, K_GEMM_WGRAD_W1,
-  K_GEMM_WGRAD_W2, K_NUM
+  K_GEMM_WGRAD_W2, K_DISPATCH_BWD, K_NUM
 };
 
 // Wraps one kernel launch: counts it and, while profiling is on, brackets it
@@ -75,11 +75,14 @@ moe_status_t launch_combine_bwd(const moe_layer_desc_t& d, const bf16* dy, const
                                 float* dgates, cudaStream_t st);
 moe_status_t launch_permute_bwd(const moe_layer_desc_t& d, const bf16* dx_perm,
                                 const int32_t* slot, float* dx32, cudaStream_t st);
+// Router backward. With dx_perm (and slot) given, the dispatch backward is
+// fused in: dx32 is not read and the row sums of dx_perm are formed in
+// registers (the layer path); otherwise dx32 comes from launch_permute_bwd.
 moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,
                               const int32_t* idx, const bf16* x, const bf16* w_r,
                               const int32_t* row_src, const int32_t* off, const float* dx32,
-                              bf16* dx, float* dw_r, float* dz, float* dwr_part, int* status,
-                              cudaStream_t st);
+                              const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dw_r,
+                              float* dz, float* dwr_part, int* status, cudaStream_t st);
 
 enum GemmMode {
   GEMM_FC1_FWD = 0,   // a, h = SwiGLU(x_perm @ W1^T)

@@ -9,15 +9,10 @@
 
 #include "moe_internal.cuh"
 
-#ifndef MOE_ROUTE_TPL
-#define MOE_ROUTE_TPL 4
-#endif
-
 namespace moe {
 
 namespace {
 
-constexpr int kRouteHc = 32;    // hidden elements per chunk
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
@@ -32,145 +27,16 @@ __device__ __forceinline__ void unpack8_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
-// z[t, e] for a tile of 64 tokens x (NW * EPW) experts: lane owns tokens lane
-// and lane+32, warp owns EPW experts, 2 x EPW accumulators per thread. Every accumulator
-// runs over h = 0..H-1 in ascending order with one fmaf per step; since a
-// bf16*bf16 product is exact in fp32, each step is a single fp32 rounding of
-// (acc + x*w), the order both sides of the parity check use.
-// Per 32-wide chunk of h, x is staged as bf16 (one 16-byte shared load gives a
-// lane 8 values of one token; an 80-byte row pitch keeps the 32 lanes' rows on
-// distinct banks) and w_r as fp32 read with warp-uniform broadcasts: 24 shared
-// wavefronts per 128 FMAs per warp, so the loop is FMA-bound. The next chunk is
-// fetched into registers while the current one is consumed (double buffered,
-// one barrier per chunk).
-constexpr int kRouteXPitchB = 80;  // bytes per staged x row (64 B of data)
-
-template <int NW, int kRouteEpw, int TPL>
-__global__ void __launch_bounds__(NW * 32) route_logits_kernel(const bf16* __restrict__ x,
-                                                               const bf16* __restrict__ w_r,
-                                                               const float* __restrict__ bias,
-                                                               float* __restrict__ z, int T,
-                                                               int H, int E) {
-  constexpr int kRouteTok = 32 * TPL;  // tokens per CTA: lane owns tokens lane + 32u
-  constexpr int kThreads = NW * 32;
-  constexpr int eb = NW * kRouteEpw;              // experts in this CTA
-  constexpr int nxp = kRouteTok * (kRouteHc / 8);  // 16-byte pieces of an x chunk (256)
-  constexpr int kXP = nxp / kThreads;              // per thread
-  constexpr int kWP = eb * (kRouteHc / 8);         // 16-byte pieces of a w_r chunk
-  static_assert(kWP <= kThreads && nxp % kThreads == 0, "staging split");
-  __shared__ __align__(16) uint8_t xs[2][kRouteTok * kRouteXPitchB];
-  __shared__ __align__(16) float ws[2][eb][kRouteHc];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * kRouteTok;
-  const int e0 = blockIdx.y * eb;
-
-  float acc[TPL][kRouteEpw];
-#pragma unroll
-  for (int u = 0; u < TPL; ++u)
-#pragma unroll
-    for (int i = 0; i < kRouteEpw; ++i) acc[u][i] = 0.f;
-
-  const int wr_row = threadIdx.x / (kRouteHc / 8), wr_col = (threadIdx.x % (kRouteHc / 8)) * 8;
-  const bool w_mine = (int)threadIdx.x < kWP;  // this thread stages a w_r piece
-  const bool w_ok = w_mine && e0 + wr_row < E;
-  const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)(w_ok ? e0 + wr_row : 0) * H);
-  auto fetch = [&](int ch, uint4 (&rx)[kXP], uint4& rw) {
-#pragma unroll
-    for (int q = 0; q < kXP; ++q) {
-      const int i = threadIdx.x + q * kThreads;
-      const int row = i / (kRouteHc / 8), col = i % (kRouteHc / 8);
-      const int t = min(t0 + row, T - 1);
-      rx[q] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + ch * (kRouteHc / 8) + col);
-    }
-    rw = w_ok ? __ldg(wrow + ch * (kRouteHc / 8) + wr_col / 8) : make_uint4(0, 0, 0, 0);
-  };
-  uint4 rx[kXP], rw;
-  fetch(0, rx, rw);
-  const int nchunks = H / kRouteHc;
-  for (int ch = 0; ch < nchunks; ++ch) {
-    const int b = ch & 1;
-#pragma unroll
-    for (int q = 0; q < kXP; ++q) {
-      const int i = threadIdx.x + q * kThreads;
-      const int row = i / (kRouteHc / 8), col = i % (kRouteHc / 8);
-      *reinterpret_cast<uint4*>(&xs[b][row * kRouteXPitchB + col * 16]) = rx[q];
-    }
-    if (w_mine) {
-      float f[8];
-      unpack8_f32(rw, f);
-      float4* dst = reinterpret_cast<float4*>(&ws[b][wr_row][wr_col]);
-      dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-      dst[1] = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    __syncthreads();
-    if (ch + 1 < nchunks) fetch(ch + 1, rx, rw);
-    const float* wb = &ws[b][warp * kRouteEpw][0];
-    // w_r values of the next 4-wide h step are loaded before the FMAs of the
-    // current one, so shared-memory latency overlaps the arithmetic
-    float4 wn[kRouteEpw];
-#pragma unroll
-    for (int i = 0; i < kRouteEpw; ++i) wn[i] = *reinterpret_cast<const float4*>(wb + i * kRouteHc);
-    float xv[TPL][8];
-#pragma unroll
-    for (int s4 = 0; s4 < kRouteHc / 4; ++s4) {
-      if ((s4 & 1) == 0) {
-#pragma unroll
-        for (int u = 0; u < TPL; ++u)
-          unpack8_f32(*reinterpret_cast<const uint4*>(&xs[b][(lane + 32 * u) * kRouteXPitchB] +
-                                                      (s4 >> 1) * 16),
-                      xv[u]);
-      }
-      float4 wc[kRouteEpw];
-#pragma unroll
-      for (int i = 0; i < kRouteEpw; ++i) wc[i] = wn[i];
-      if (s4 + 1 < kRouteHc / 4) {
-#pragma unroll
-        for (int i = 0; i < kRouteEpw; ++i)
-          wn[i] = *reinterpret_cast<const float4*>(wb + i * kRouteHc + (s4 + 1) * 4);
-      }
-      const int hh = (s4 & 1) * 4;
-#pragma unroll
-      for (int i = 0; i < kRouteEpw; ++i) {
-#pragma unroll
-        for (int u = 0; u < TPL; ++u) {
-          acc[u][i] = fmaf(xv[u][hh + 0], wc[i].x, acc[u][i]);
-          acc[u][i] = fmaf(xv[u][hh + 1], wc[i].y, acc[u][i]);
-          acc[u][i] = fmaf(xv[u][hh + 2], wc[i].z, acc[u][i]);
-          acc[u][i] = fmaf(xv[u][hh + 3], wc[i].w, acc[u][i]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < TPL; ++u) {
-    const int t = t0 + lane + 32 * u;
-    if (t >= T) continue;
-#pragma unroll
-    for (int i = 0; i < kRouteEpw; ++i) {
-      const int e = e0 + warp * kRouteEpw + i;
-      if (e < E) {
-        float v = acc[u][i];
-        if (bias) v = __fadd_rn(v, __ldg(bias + e));
-        z[(size_t)t * E + e] = v;
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
   return v1 > v2 || (v1 == v2 && e1 < e2);
 }
 
-// One warp per token: top-k (or the forced set), softmax over all E, gates.
+// Top-k (or the forced set), softmax over all E and renormalised gates of one
+// token, by one warp; zt is the token's row of logits (global or shared).
 template <int EPL>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ z,
-                                                         int32_t* __restrict__ idx,
-                                                         float* __restrict__ gates, int T, int E,
-                                                         int k, int forced) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* zt = z + (size_t)t * E;
+__device__ __forceinline__ void topk_row(const float* zt, int t, int32_t* __restrict__ idx,
+                                         float* __restrict__ gates, int E, int k, int forced,
+                                         int lane) {
   float v[EPL];
   float m = -FLT_MAX;
 #pragma unroll
@@ -234,65 +100,285 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
 }
 
+// z[t, e] for a tile of 4*TPL tokens x 128 experts, one block of kRouteNw
+// warps. Every logit runs over h = 0..H-1 in ascending order with one fused
+// multiply-add per step; since a bf16*bf16 product is exact in fp32, each step
+// is a single fp32 rounding of (acc + x*w), the order both sides of the parity
+// check use.
+//
+// Lane (tg, eg) = (lane / 8, lane % 8) of warp w owns tokens tg + 4u (u < TPL)
+// and experts EW*w + eg + 8i (i < EW/8, EW = 128/kRouteNw experts per warp).
+// The host sizes TPL so that the grid is about one wave of the SMs. The block
+// is limited by shared-memory wavefronts per FMA: a warp-wide 16-byte shared
+// load costs about one wavefront per 4 bytes a lane receives, broadcast or
+// not, so operands stay bf16 in shared memory (8 steps of h per 16-byte load)
+// and each step is one mixed-precision fma.rn.f32.bf16: the bf16 factors
+// widen exactly and the sum is rounded once, the same bits as fmaf on the
+// widened values, with no unpacking instructions.
+// Chunks of 64 h are copied with cp.async into a 3-stage ring (rows padded to
+// 144 bytes: the 4 token rows and 8 expert rows a warp reads at once sit on
+// distinct banks).
+//
+// With FUSE (E <= 128: the block holds every expert of its tokens), the block
+// then parks its logits in shared memory and each warp routes its tokens
+// (topk_row), which saves the logits round trip and a launch.
+constexpr int kRouteEb = 128;  // experts per block
+constexpr int kRouteNw = 8;    // warps per block
+constexpr int kRouteHc = 64;                  // h per chunk
+constexpr int kRoutePitchB = kRouteHc * 2 + 16;  // bytes per staged row
+constexpr int kRouteStages = 3;
+
+__device__ __forceinline__ void fma_bf16_lo(float& acc, uint32_t x, uint32_t w) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\tmov.b32 {xl, xh}, %1;\n\tmov.b32 {wl, wh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(x), "r"(w));
+}
+__device__ __forceinline__ void fma_bf16_hi(float& acc, uint32_t x, uint32_t w) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\tmov.b32 {xl, xh}, %1;\n\tmov.b32 {wl, wh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(x), "r"(w));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int TPL, bool FUSE>
+__global__ void __launch_bounds__(kRouteNw * 32, 1) route_logits_kernel(
+    const bf16* __restrict__ x, const bf16* __restrict__ w_r, const float* __restrict__ bias,
+    float* __restrict__ z, int32_t* __restrict__ idx, float* __restrict__ gates, int T, int H,
+    int E, int k, int forced) {
+  constexpr int NW = kRouteNw, NT = NW * 32;
+  constexpr int TB = 4 * TPL;
+  constexpr int EW = kRouteEb / NW;  // experts per warp
+  constexpr int EPL = EW / 8;        // experts per lane
+  constexpr int ROWS = TB + kRouteEb;
+  constexpr int STAGE_B = ROWS * kRoutePitchB;
+  constexpr int PIECES = ROWS * (kRouteHc / 8);  // 16-byte pieces per chunk
+  static_assert(EPL >= 1, "route tile");
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tg = lane >> 3, eg = lane & 7;
+  const int t0 = blockIdx.x * TB;
+  const int e0 = blockIdx.y * kRouteEb;
+  const int nchunks = H / kRouteHc;
+
+  // rows 0..TB-1 of a stage: x (tokens, clamped to T-1); rows TB..: w_r
+  // (experts; rows past E are zero-filled)
+  auto issue = [&](int ch) {
+    if (ch < nchunks) {
+      uint8_t* stage = route_smem + (ch % kRouteStages) * STAGE_B;
+      for (int pc = threadIdx.x; pc < PIECES; pc += NT) {
+        const int row = pc >> 3, piece = pc & 7;
+        const bf16* src;
+        bool valid = true;
+        if (row < TB) {
+          src = x + (size_t)min(t0 + row, T - 1) * H;
+        } else {
+          const int e = e0 + row - TB;
+          valid = e < E;
+          src = w_r + (size_t)(valid ? e : 0) * H;
+        }
+        cp_async16(stage + row * kRoutePitchB + piece * 16, src + ch * kRouteHc + piece * 8,
+                   valid);
+      }
+    }
+    cp_async_commit();
+  };
+
+  float acc[TPL][EPL];
+#pragma unroll
+  for (int u = 0; u < TPL; ++u)
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[u][i] = 0.f;
+
+#pragma unroll
+  for (int s0 = 0; s0 < kRouteStages - 1; ++s0) issue(s0);
+  for (int ch = 0; ch < nchunks; ++ch) {
+    cp_async_wait<kRouteStages - 2>();
+    __syncthreads();  // chunk ch landed for every thread; chunk ch-1 fully consumed
+    issue(ch + kRouteStages - 1);
+    const uint8_t* stage = route_smem + (ch % kRouteStages) * STAGE_B;
+    const uint8_t* xrow = stage + tg * kRoutePitchB;
+    const uint8_t* wrow = stage + (TB + EW * warp + eg) * kRoutePitchB;
+#pragma unroll
+    for (int s8 = 0; s8 < kRouteHc / 8; ++s8) {
+      uint4 xv[TPL], wv[EPL];
+#pragma unroll
+      for (int u = 0; u < TPL; ++u)
+        xv[u] = *reinterpret_cast<const uint4*>(xrow + 4 * u * kRoutePitchB + 16 * s8);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        wv[i] = *reinterpret_cast<const uint4*>(wrow + 8 * i * kRoutePitchB + 16 * s8);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int u = 0; u < TPL; ++u) {
+          const uint32_t xq = q == 0 ? xv[u].x : q == 1 ? xv[u].y : q == 2 ? xv[u].z : xv[u].w;
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) {
+            const uint32_t wq = q == 0 ? wv[i].x : q == 1 ? wv[i].y : q == 2 ? wv[i].z : wv[i].w;
+            fma_bf16_lo(acc[u][i], xq, wq);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < TPL; ++u) {
+          const uint32_t xq = q == 0 ? xv[u].x : q == 1 ? xv[u].y : q == 2 ? xv[u].z : xv[u].w;
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) {
+            const uint32_t wq = q == 0 ? wv[i].x : q == 1 ? wv[i].y : q == 2 ? wv[i].z : wv[i].w;
+            fma_bf16_hi(acc[u][i], xq, wq);
+          }
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  float* zs = reinterpret_cast<float*>(route_smem);  // TB x 128 floats
+  if (FUSE) __syncthreads();
+#pragma unroll
+  for (int u = 0; u < TPL; ++u) {
+    const int tl = tg + 4 * u, t = t0 + tl;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int el = EW * warp + eg + 8 * i, e = e0 + el;
+      if (e < E) {
+        float v = acc[u][i];
+        if (bias) v = __fadd_rn(v, __ldg(bias + e));
+        if (t < T) z[(size_t)t * E + e] = v;
+        if (FUSE) zs[tl * kRouteEb + el] = v;
+      }
+    }
+  }
+  if (FUSE) {
+    __syncthreads();
+    for (int tl = warp; tl < TB; tl += NW)
+      if (t0 + tl < T) topk_row<kRouteEb / 32>(zs + tl * kRouteEb, t0 + tl, idx, gates, E, k, forced, lane);
+  }
+}
+
+// One warp per token, logits from global memory (E > 128).
+template <int EPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ z,
+                                                         int32_t* __restrict__ idx,
+                                                         float* __restrict__ gates, int T, int E,
+                                                         int k, int forced) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  topk_row<EPL>(z + (size_t)t * E, t, idx, gates, E, k, forced, lane);
+}
+
 // ------------------------------------------------------------------ backward
-// One 256-thread block per group of tokens; each thread owns 16-byte chunks of
-// one token row. dz_j = g_j (dg_j - <g, dg>) on the chosen set;
-// dx = bf16(dx32 + sum_j dz_j * w_r[i_j]).
-template <int KMAX>
-__global__ void __launch_bounds__(256, KMAX <= 8 ? 4 : 2) route_bwd_dx_kernel(
+// dz_j = g_j (dg_j - <g, dg>) on the chosen set;
+// dx = bf16(dx32 + sum_j dz_j * w_r[i_j]), j ascending.
+// A block owns kDxTok tokens x one 64-column slice of the row: the slice of
+// w_r (E x 64) is staged in shared memory once, so the k expert rows a token
+// adds come from shared memory instead of k gathers through L2. Thread
+// (token lane, chunk) = (tid / 8, tid % 8) handles one 16-byte chunk of the
+// slice for 32 tokens at a time; the 8 threads of a token read its routing
+// state (the same addresses, from L1) and each works out dz itself.
+// FUSED: the dispatch backward is done in the same pass and dx32 is never
+// stored: the row sum dx32[t] = sum_j dx_perm[slot[t,j]] (fp32, j ascending,
+// from 0) is formed in registers exactly as the standalone permute backward
+// forms it, then the router term is added in the same order as above, so the
+// two paths give the same bits.
+constexpr int kDxTok = 128;                 // tokens per block
+constexpr int kDxPitchB = 64 * 2 + 16;      // bytes per staged w_r slice row
+
+template <int KMAX, bool FUSED>
+__global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     const float* __restrict__ dgates, const float* __restrict__ gates,
     const int32_t* __restrict__ idx, const bf16* __restrict__ w_r, const float* __restrict__ dx32,
-    bf16* __restrict__ dx, float* __restrict__ dz, int T, int H, int E, int k, int tpr,
-    int* status) {
-  // tokens per block = 256 / tpr with tpr >= H/8 >= 8, so at most 32
-  __shared__ float s_dz[32][KMAX];
-  __shared__ int s_e[32][KMAX];
-  const int rpb = blockDim.x / tpr;
-  const int tl = threadIdx.x / tpr;
-  const int t = blockIdx.x * rpb + tl;
-  const int sub = threadIdx.x % tpr;
-  // the token's first min(k, tpr) threads work out dz_j and the expert of slot j
-  if (t < T && sub < k) {
-    float inner = 0.f;
-    for (int j = 0; j < k; ++j) inner = fmaf(gates[(size_t)t * k + j], dgates[(size_t)t * k + j], inner);
-    const int e = idx[(size_t)t * k + sub];
-    s_dz[tl][sub] = gates[(size_t)t * k + sub] * (dgates[(size_t)t * k + sub] - inner);
-    s_e[tl][sub] = (unsigned)e < (unsigned)E ? e : -1;
+    const bf16* __restrict__ dx_perm, const int32_t* __restrict__ slot, bf16* __restrict__ dx,
+    float* __restrict__ dz, int T, int H, int E, int k, int* status) {
+  constexpr int KB = KMAX < 8 ? KMAX : 8;  // rows in flight per batch
+  extern __shared__ __align__(16) uint8_t s_wr[];  // [E][kDxPitchB]
+  const int c = blockIdx.y * 8 + (threadIdx.x & 7);  // 16-byte chunk of the row
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) {
+    const int e = i >> 3, q = i & 7;
+    *reinterpret_cast<uint4*>(s_wr + e * kDxPitchB + q * 16) =
+        __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)e * H) + blockIdx.y * 8 + q);
   }
   __syncthreads();
-  if (t >= T) return;
-  float dzj[KMAX];
-  int ej[KMAX];
+  const long long N = (long long)T * k;
+  const bool writer = blockIdx.y == 0 && (threadIdx.x & 7) == 0;
+  for (int tl = threadIdx.x >> 3; tl < kDxTok; tl += 32) {
+    const int t = blockIdx.x * kDxTok + tl;
+    if (t >= T) break;
+    const size_t tk = (size_t)t * k;
+    float dzj[KMAX];
+    int ej[KMAX], sj[KMAX];
+    float inner = 0.f;
 #pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    dzj[j] = j < k ? s_dz[tl][j] : 0.f;
-    ej[j] = j < k ? s_e[tl][j] : -1;
-  }
-  const int cpr = H / 8;
-  for (int c = sub; c < cpr; c += tpr) {
-    const float4* src = reinterpret_cast<const float4*>(dx32 + (size_t)t * H + c * 8);
-    const float4 p0 = src[0], p1 = src[1];
-    float acc[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-    for (int j0 = 0; j0 < KMAX; j0 += 8) {  // 8 w_r rows in flight at a time
-      uint4 wv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u;
-        wv[u] = (j < k && ej[j] >= 0)
-                    ? __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)ej[j] * H + c * 8))
-                    : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < KMAX; ++j) {
+      ej[j] = -1;
+      sj[j] = -1;
+      if (j < k) {
+        const int e = __ldg(idx + tk + j);
+        ej[j] = (unsigned)e < (unsigned)E ? e : -1;
+        if (FUSED) {
+          const int sv = __ldg(slot + tk + j);
+          sj[j] = sv >= 0 && sv < N ? sv : -1;
+        }
+        inner = fmaf(__ldg(gates + tk + j), __ldg(dgates + tk + j), inner);
       }
+    }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u;
-        if (j < k) {
-          const uint32_t w[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+    for (int j = 0; j < KMAX; ++j)
+      dzj[j] = j < k ? __ldg(gates + tk + j) * (__ldg(dgates + tk + j) - inner) : 0.f;
+
+    float acc[8];
+    if (FUSED) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc[2 * q] = fmaf(dzj[j], bf16_bits_to_f32(w[q] & 0xFFFFu), acc[2 * q]);
-            acc[2 * q + 1] = fmaf(dzj[j], bf16_bits_to_f32(w[q] >> 16), acc[2 * q + 1]);
+      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll
+      for (int j0 = 0; j0 < KMAX; j0 += KB) {
+        uint4 v[KB];
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          const int j = j0 + u;
+          v[u] = (j < k && sj[j] >= 0)
+                     ? __ldcs(reinterpret_cast<const uint4*>(dx_perm + (size_t)sj[j] * H) + c)
+                     : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          if (j0 + u < k) {
+            float f[8];
+            unpack8_f32(v[u], f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] += f[q];
           }
+        }
+      }
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(dx32 + (size_t)t * H + c * 8);
+      const float4 p0 = src[0], p1 = src[1];
+      acc[0] = p0.x; acc[1] = p0.y; acc[2] = p0.z; acc[3] = p0.w;
+      acc[4] = p1.x; acc[5] = p1.y; acc[6] = p1.z; acc[7] = p1.w;
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k && ej[j] >= 0) {
+        const uint4 wv =
+            *reinterpret_cast<const uint4*>(s_wr + ej[j] * kDxPitchB + (threadIdx.x & 7) * 16);
+        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = fmaf(dzj[j], bf16_bits_to_f32(w[q] & 0xFFFFu), acc[2 * q]);
+          acc[2 * q + 1] = fmaf(dzj[j], bf16_bits_to_f32(w[q] >> 16), acc[2 * q + 1]);
         }
       }
     }
@@ -304,13 +390,13 @@ __global__ void __launch_bounds__(256, KMAX <= 8 ? 4 : 2) route_bwd_dx_kernel(
       o[q] = *reinterpret_cast<uint32_t*>(&b2);
     }
     *reinterpret_cast<uint4*>(dx + (size_t)t * H + c * 8) = out;
-  }
-  if (sub == 0) {
+    if (writer) {
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      if (j < k) {
-        dz[(size_t)t * k + j] = dzj[j];
-        if (ej[j] < 0) atomicAdd(status + ST_BAD_INDEX, 1);
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          dz[tk + j] = dzj[j];
+          if (ej[j] < 0) atomicAdd(status + ST_BAD_INDEX, 1);
+        }
       }
     }
   }
@@ -440,80 +526,104 @@ __global__ void __launch_bounds__(256) route_bwd_dwr_reduce_kernel(
 
 }  // namespace
 
+template <int TPL, bool FUSE>
+cudaError_t launch_logits_t(const moe_layer_desc_t& d, dim3 grid, const bf16* x, const bf16* w_r,
+                            const float* bias, float* logits, int32_t* idx, float* gates,
+                            cudaStream_t st) {
+  const int forced = d.mode == MOE_ROUTE_FORCED_BALANCED;
+  constexpr size_t smem = (size_t)kRouteStages * (4 * TPL + kRouteEb) * kRoutePitchB;
+  static cudaError_t attr = cudaFuncSetAttribute(
+      route_logits_kernel<TPL, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (attr != cudaSuccess) return attr;
+  route_logits_kernel<TPL, FUSE><<<grid, kRouteNw * 32, smem, st>>>(x, w_r, bias, logits, idx,
+                                                                    gates, d.T, d.H, d.E, d.k,
+                                                                    forced);
+  return cudaSuccess;
+}
+
+template <int TPL>
+cudaError_t launch_logits(const moe_layer_desc_t& d, dim3 grid, bool fuse, const bf16* x,
+                          const bf16* w_r, const float* bias, float* logits, int32_t* idx,
+                          float* gates, cudaStream_t st) {
+  return fuse ? launch_logits_t<TPL, true>(d, grid, x, w_r, bias, logits, idx, gates, st)
+              : launch_logits_t<TPL, false>(d, grid, x, w_r, bias, logits, idx, gates, st);
+}
+
 moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
                           const float* bias, float* logits, int32_t* idx, float* gates,
                           int* status, cudaStream_t st) {
   (void)status;
   if (d.T == 0) return MOE_OK;
-  // 4 warps x 4 experts per CTA, ROUTE_TPL tokens per lane: 2 x 4 or 4 x 4
-  // accumulators per thread keep the FMA : shared-wavefront ratio at or above 1
-  // while giving the SMs enough warps to hide shared-memory latency.
-  constexpr int tpl = MOE_ROUTE_TPL;
-  const int nw = d.E > 8 ? 4 : d.E > 4 ? 2 : 1;
-  const int eb = nw * 4;
-  dim3 grid(ceil_div(d.T, 32 * tpl), ceil_div(d.E, eb));
+  // tokens per lane: the smallest TPL (<= 7) that covers the tokens in about
+  // one wave of one block per SM
+  const int gy = ceil_div(d.E, kRouteEb);
+  const int per_sm = ceil_div(d.T * gy, 4 * device_sm_count());
+  const int tpl = per_sm < 1 ? 1 : per_sm > 7 ? 7 : per_sm;
+  const dim3 grid(ceil_div(d.T, 4 * tpl), gy);
+  const bool fuse = gy == 1;
+  cudaError_t ae;
   {
     LaunchScope _ls(K_ROUTE_LOGITS, st);
-    if (nw == 4)
-      route_logits_kernel<4, 4, tpl><<<grid, 128, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
-    else if (nw == 2)
-      route_logits_kernel<2, 4, tpl><<<grid, 64, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
-    else
-      route_logits_kernel<1, 4, tpl><<<grid, 32, 0, st>>>(x, w_r, bias, logits, d.T, d.H, d.E);
+    switch (tpl) {
+      case 1: ae = launch_logits<1>(d, grid, fuse, x, w_r, bias, logits, idx, gates, st); break;
+      case 2: ae = launch_logits<2>(d, grid, fuse, x, w_r, bias, logits, idx, gates, st); break;
+      case 3: ae = launch_logits<3>(d, grid, fuse, x, w_r, bias, logits, idx, gates, st); break;
+      case 4: ae = launch_logits<4>(d, grid, fuse, x, w_r, bias, logits, idx, gates, st); break;
+      case 5: ae = launch_logits<5>(d, grid, fuse, x, w_r, bias, logits, idx, gates, st); break;
+      case 6: ae = launch_logits<6>(d, grid, fuse, x, w_r, bias, logits, idx, gates, st); break;
+      default: ae = launch_logits<7>(d, grid, fuse, x, w_r, bias, logits, idx, gates, st); break;
+    }
+  }
+  if (ae != cudaSuccess) {
+    set_error("route_logits_kernel attribute setup: %s", cudaGetErrorString(ae));
+    return MOE_ERR_CUDA;
   }
   moe_status_t s = check_launch("route_logits_kernel");
-  if (s != MOE_OK) return s;
+  if (s != MOE_OK || fuse) return s;
   const int tpb = 256, warps = tpb / 32;
-  dim3 g2(ceil_div(d.T, warps));
   const int forced = d.mode == MOE_ROUTE_FORCED_BALANCED;
-  if (d.E <= 32)
-    {
-      LaunchScope _ls(K_ROUTE_TOPK, st);
-      route_topk_kernel<1><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
-    }
-  else if (d.E <= 64)
-    {
-      LaunchScope _ls(K_ROUTE_TOPK, st);
-      route_topk_kernel<2><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
-    }
-  else if (d.E <= 128)
-    {
-      LaunchScope _ls(K_ROUTE_TOPK, st);
-      route_topk_kernel<4><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
-    }
-  else
-    {
-      LaunchScope _ls(K_ROUTE_TOPK, st);
-      route_topk_kernel<8><<<g2, tpb, 0, st>>>(logits, idx, gates, d.T, d.E, d.k, forced);
-    }
+  {
+    LaunchScope _ls(K_ROUTE_TOPK, st);
+    route_topk_kernel<8><<<dim3(ceil_div(d.T, warps)), tpb, 0, st>>>(logits, idx, gates, d.T, d.E,
+                                                                     d.k, forced);
+  }
   return check_launch("route_topk_kernel");
+}
+
+template <bool FUSED>
+void launch_dx(const moe_layer_desc_t& d, const float* dgates, const float* gates,
+               const int32_t* idx, const bf16* w_r, const float* dx32, const bf16* dx_perm,
+               const int32_t* slot, bf16* dx, float* dz, int* status, cudaStream_t st) {
+  const dim3 g(ceil_div(d.T, kDxTok), d.H / 64);
+  const size_t smem = (size_t)d.E * kDxPitchB;
+  if (d.k <= 4)
+    route_bwd_dx_kernel<4, FUSED><<<g, 256, smem, st>>>(dgates, gates, idx, w_r, dx32, dx_perm,
+                                                        slot, dx, dz, d.T, d.H, d.E, d.k, status);
+  else if (d.k <= 8)
+    route_bwd_dx_kernel<8, FUSED><<<g, 256, smem, st>>>(dgates, gates, idx, w_r, dx32, dx_perm,
+                                                        slot, dx, dz, d.T, d.H, d.E, d.k, status);
+  else if (d.k <= 16)
+    route_bwd_dx_kernel<16, FUSED><<<g, 256, smem, st>>>(dgates, gates, idx, w_r, dx32, dx_perm,
+                                                         slot, dx, dz, d.T, d.H, d.E, d.k, status);
+  else
+    route_bwd_dx_kernel<32, FUSED><<<g, 256, smem, st>>>(dgates, gates, idx, w_r, dx32, dx_perm,
+                                                         slot, dx, dz, d.T, d.H, d.E, d.k, status);
 }
 
 moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,
                               const int32_t* idx, const bf16* x, const bf16* w_r,
                               const int32_t* row_src, const int32_t* off, const float* dx32,
-                              bf16* dx, float* dw_r, float* dz, float* dwr_part, int* status,
-                              cudaStream_t st) {
+                              const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dw_r,
+                              float* dz, float* dwr_part, int* status, cudaStream_t st) {
+  const bool fused = dx_perm != nullptr;
   const int cpr = d.H / 8;
-  int tpr = 1;
-  while ((tpr < cpr || tpr < d.k) && tpr < 256) tpr <<= 1;  // >= k threads per token
-  const int rpb = 256 / tpr;
   if (d.T > 0) {
     {
-      LaunchScope _ls(K_ROUTE_BWD_DX, st);
-      const dim3 g(ceil_div(d.T, rpb));
-      if (d.k <= 4)
-        route_bwd_dx_kernel<4><<<g, 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz, d.T, d.H,
-                                                  d.E, d.k, tpr, status);
-      else if (d.k <= 8)
-        route_bwd_dx_kernel<8><<<g, 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz, d.T, d.H,
-                                                  d.E, d.k, tpr, status);
-      else if (d.k <= 16)
-        route_bwd_dx_kernel<16><<<g, 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz, d.T, d.H,
-                                                   d.E, d.k, tpr, status);
+      LaunchScope _ls(fused ? K_DISPATCH_BWD : K_ROUTE_BWD_DX, st);
+      if (fused)
+        launch_dx<true>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status, st);
       else
-        route_bwd_dx_kernel<32><<<g, 256, 0, st>>>(dgates, gates, idx, w_r, dx32, dx, dz, d.T, d.H,
-                                                   d.E, d.k, tpr, status);
+        launch_dx<false>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status, st);
     }
     moe_status_t s = check_launch("route_bwd_dx_kernel");
     if (s != MOE_OK) return s;

@@ -170,3 +170,24 @@ def test_host_step_matches_device_path():
     moe.moe_layer_step_host(d, b, hx, hdy, hy, hdx)
     assert np.array_equal(np64(hy), g["y"])
     assert np.array_equal(np64(hdx), g["dx"])
+
+
+@pytest.mark.parametrize("k", [3, 8, 12])
+def test_fused_dispatch_bwd_matches_two_calls(k):
+    """The layer path fuses the permute backward into the router's dx pass; it
+    must give the same bits as moe_permute_bwd followed by moe_route_bwd."""
+    inp = moe_synth.make_inputs(T=300, H=192, E=16, k=k, F=128, seed=30 + k)
+    d = desc_of(inp)
+    b = moe.LayerBuffers(d)
+    b.load_inputs(inp)
+    moe.moe_layer_forward(d, b)
+    moe.moe_layer_backward(d, b, run_wgrad=False)
+    dx32 = torch.empty_like(b.dx32)
+    dx = torch.empty_like(b.dx)
+    dw_r = torch.empty_like(b.dw_r)
+    moe.moe_permute_bwd(d, b.dx_perm, b.slot, dx32)
+    moe.moe_route_bwd(d, b.dgates, b.gates, b.idx, b.x, b.w_r, b.row_src, b.off, dx32, dx, dw_r,
+                      b.ws)
+    assert moe.moe_device_status(d, b.ws) == moe.MOE_OK
+    assert torch.equal(dx.view(torch.int16), b.dx.view(torch.int16))
+    assert torch.equal(dw_r.view(torch.int32), b.dw_r.view(torch.int32))
