@@ -259,25 +259,32 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     per_step_launches = moe.moe_kernel_launches() - l0
 
-    # ---- timed region
+    # ---- timed region (no per-launch events inside: they would sit between
+    # the kernels and break programmatic dependent launch)
     barrier(world)
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(local)
     time.sleep(0.25)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = moe.moe_kernel_launches()
-    moe.moe_profile_start(per_step_launches * args.steps + 8)
     e0.record(st)
     for _ in range(args.steps):
         step()
     e1.record(st)
     torch.cuda.synchronize(dev)
-    prof = moe.moe_profile_stop(per_step_launches * args.steps + 8)
     launches = moe.moe_kernel_launches() - launches0
     barrier(world)
     clk = clocks.stop()
     ms_local = e0.elapsed_time(e1) / args.steps
     ms = max_over_ranks(ms_local, world)
+
+    # ---- per-kernel durations: the same steps again, each launch bracketed by
+    # CUDA events on its own stream
+    moe.moe_profile_start(per_step_launches * args.steps + 8)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    prof = moe.moe_profile_stop(per_step_launches * args.steps + 8)
     status = moe.moe_device_status(d, b.ws, st)
     if status != moe.MOE_OK:
         raise RuntimeError(f"device status {status}: {moe.lib().moe_last_error()}")

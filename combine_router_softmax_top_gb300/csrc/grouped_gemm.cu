@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
 
-  // ---- per-CTA setup: offsets, tile prefix, barriers, TMEM
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) ctl.off[e] = p.off[e];
+  // ---- per-CTA setup: barriers, TMEM, then (once the previous kernel on the
+  // stream has completed) offsets and the tile prefix
   if (threadIdx.x == 0) {
     for (int s = 0; s < M::kStages; ++s) {
       ptx::mbar_init(&ctl.full[s], 1);
@@ -340,6 +340,12 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     ptx::tmem_alloc(&ctl.tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  pdl_wait();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) ctl.off[e] = p.off[e];
   __syncthreads();
   if (warp == 0) {
     // tiles per expert -> exclusive prefix
@@ -380,10 +386,6 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
 
   if (warp == 0) {
     // ================================================================ producer
-    if (lane == 0) {
-      ptx::tma_prefetch_desc(&tmA);
-      ptx::tma_prefetch_desc(&tmB);
-    }
     int stage = 0, cursor = 0;
     uint32_t phase = 0, tail_phase = 0;
     bool ok = true;
@@ -854,24 +856,27 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUten
   }
   LaunchScope _ls(K_GEMM_FC1_FWD + MODE, st);
   if (cs == 1) {
-    grouped_gemm_kernel<MODE><<<grid, Mode<MODE>::kWarps * 32, Mode<MODE>::kDynSmem, st>>>(a, b, c, dmap, p);
+    launch_k(grouped_gemm_kernel<MODE>, grid, Mode<MODE>::kWarps * 32, Mode<MODE>::kDynSmem, st, a,
+             b, c, dmap, p);
     return check_launch("grouped_gemm_kernel");
   }
   int clusters = (grid + cs - 1) / cs;
   if (max_clusters > 0 && clusters > max_clusters) clusters = max_clusters;
   if (clusters < 1) clusters = 1;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = cs;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = MOE_PDL;
   cfg.gridDim = dim3(clusters * cs);
   cfg.blockDim = dim3(Mode<MODE>::kWarps * 32);
   cfg.dynamicSmemBytes = Mode<MODE>::kDynSmem;
   cfg.stream = st;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, b, c, dmap, p);
   if (e != cudaSuccess) {
     set_error("grouped_gemm_kernel cluster launch: %s", cudaGetErrorString(e));

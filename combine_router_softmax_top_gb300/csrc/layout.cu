@@ -22,6 +22,7 @@ constexpr int kWarps = kTok / 32;
 __global__ void __launch_bounds__(kTok) layout_count_kernel(const int32_t* __restrict__ idx,
                                                             int* __restrict__ hist, int T, int E,
                                                             int k, int* status) {
+  pdl_wait();
   extern __shared__ int s_hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
   __syncthreads();
@@ -42,6 +43,7 @@ __global__ void __launch_bounds__(kTok) layout_assign_kernel(
     int32_t* __restrict__ off, int32_t* __restrict__ slot, int32_t* __restrict__ row_src,
     int32_t* __restrict__ cnt_re, int32_t* __restrict__ rank_off, int T, int E, int k, int R,
     int nblocks) {
+  pdl_wait();
   extern __shared__ int smem[];
   int* s_base = smem;                              // [E]  first row of this block's entries
   int* s_cnt = s_base + E;                         // [E]
@@ -137,15 +139,16 @@ moe_status_t launch_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_
   const int nb = d.T > 0 ? ceil_div(d.T, kTok) : 1;
   {
     LaunchScope _ls(K_LAYOUT_COUNT, st);
-    layout_count_kernel<<<nb, kTok, d.E * sizeof(int), st>>>(idx, hist, d.T, d.E, d.k, status);
+    launch_k(layout_count_kernel, nb, kTok, d.E * sizeof(int), st, idx, hist, d.T, d.E, d.k,
+             status);
   }
   moe_status_t s = check_launch("layout_count_kernel");
   if (s != MOE_OK) return s;
   const size_t smem = (size_t)d.E * (2 + 2 * kWarps) * sizeof(int);
   {
     LaunchScope _ls(K_LAYOUT_ASSIGN, st);
-    layout_assign_kernel<<<nb, kTok, smem, st>>>(idx, hist, cnt, off, slot, row_src, cnt_re,
-                                                 rank_off, d.T, d.E, d.k, d.R, nb);
+    launch_k(layout_assign_kernel, nb, kTok, smem, st, idx, hist, cnt, off, slot, row_src, cnt_re,
+             rank_off, d.T, d.E, d.k, d.R, nb);
   }
   return check_launch("layout_assign_kernel");
 }

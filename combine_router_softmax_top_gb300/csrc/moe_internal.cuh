@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 
 namespace moe {
@@ -58,6 +60,38 @@ void set_error(const char* fmt, ...);
 moe_status_t check_launch(const char* what);
 
 int device_sm_count();
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel is launched with programmatic stream serialisation: the next
+// kernel on the stream is launched as the blocks of this one exit, runs its
+// set-up (shared memory, barriers, TMEM, descriptor prefetch), then blocks in
+// pdl_wait() until this grid has completed and its writes are visible. Each
+// kernel calls pdl_wait() before its first global memory access (read or
+// write). Kernels do not signal an earlier launch (griddepcontrol.
+// launch_dependents): measured on the layer step, that made the dependent
+// grids resident too early and cost 0.10 ms per step, while the launch at
+// block exit saves 0.04 ms over plain stream order. Without the launch
+// attribute pdl_wait() is a no-op, so the order of work is the same either way.
+#ifndef MOE_PDL
+#define MOE_PDL 1
+#endif
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- launchers
 moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,

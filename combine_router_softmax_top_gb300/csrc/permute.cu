@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const bf16* __restrict__ x
                                                       const int32_t* __restrict__ row_src,
                                                       bf16* __restrict__ x_perm, int T, int H,
                                                       int k, long long N) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const int cpr = H / 8;
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const bf16* __restrict__ o
                                                       const float* __restrict__ gates,
                                                       bf16* __restrict__ y, int T, int H, int k,
                                                       long long N, int tpr) {
+  pdl_wait();
   const RowMap m = row_map(tpr);
   if (m.t >= T) return;
   const int cpr = H / 8;
@@ -128,6 +130,7 @@ __global__ void __launch_bounds__(256, KMAX <= 8 ? 3 : 1) combine_bwd_kernel(
     const bf16* __restrict__ dy, const bf16* __restrict__ o, const int32_t* __restrict__ slot,
     const float* __restrict__ gates, bf16* __restrict__ d_o, float* __restrict__ dgates, int T,
     int H, int k, long long N, int tpr) {
+  pdl_wait();
   __shared__ float s_part[8][KMAX];
   const RowMap m = row_map(tpr);
   const bool active = m.t < T;
@@ -216,6 +219,7 @@ __global__ void __launch_bounds__(256) permute_bwd_kernel(const bf16* __restrict
                                                           const int32_t* __restrict__ slot,
                                                           float* __restrict__ dx32, int T, int H,
                                                           int k, long long N, int tpr) {
+  pdl_wait();
   const RowMap m = row_map(tpr);
   if (m.t >= T) return;
   const int cpr = H / 8;
@@ -267,7 +271,7 @@ moe_status_t launch_permute(const moe_layer_desc_t& d, const bf16* x, const int3
   if (blocks > cap) blocks = cap;
   {
     LaunchScope _ls(K_PERMUTE, st);
-    permute_kernel<<<(int)blocks, 256, 0, st>>>(x, row_src, x_perm, d.T, d.H, d.k, N);
+    launch_k(permute_kernel, (int)blocks, 256, 0, st, x, row_src, x_perm, d.T, d.H, d.k, N);
   }
   return check_launch("permute_kernel");
 }
@@ -278,8 +282,8 @@ moe_status_t launch_combine(const moe_layer_desc_t& d, const bf16* o, const int3
   const int tpr = threads_per_row(d.H);
   {
     LaunchScope _ls(K_COMBINE, st);
-    combine_kernel<<<ceil_div(d.T, 256 / tpr), 256, 0, st>>>(o, slot, gates, y, d.T, d.H, d.k,
-                                                             (long long)d.T * d.k, tpr);
+    launch_k(combine_kernel, ceil_div(d.T, 256 / tpr), 256, 0, st, o, slot, gates, y, d.T, d.H, d.k,
+             (long long)d.T * d.k, tpr);
   }
   return check_launch("combine_kernel");
 }
@@ -294,27 +298,32 @@ moe_status_t launch_combine_bwd(const moe_layer_desc_t& d, const bf16* dy, const
   if (d.k <= 2)
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
-      combine_bwd_kernel<2><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+      launch_k(combine_bwd_kernel<2>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
+               d.k, N, tpr);
     }
   else if (d.k <= 4)
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
-      combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+      launch_k(combine_bwd_kernel<4>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
+               d.k, N, tpr);
     }
   else if (d.k <= 8)
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
-      combine_bwd_kernel<8><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+      launch_k(combine_bwd_kernel<8>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
+               d.k, N, tpr);
     }
   else if (d.k <= 16)
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
-      combine_bwd_kernel<16><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+      launch_k(combine_bwd_kernel<16>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
+               d.k, N, tpr);
     }
   else
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
-      combine_bwd_kernel<32><<<grid, 256, 0, st>>>(dy, o, slot, gates, d_o, dgates, d.T, d.H, d.k, N, tpr);
+      launch_k(combine_bwd_kernel<32>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
+               d.k, N, tpr);
     }
   return check_launch("combine_bwd_kernel");
 }
@@ -325,8 +334,8 @@ moe_status_t launch_permute_bwd(const moe_layer_desc_t& d, const bf16* dx_perm,
   const int tpr = threads_per_row(d.H);
   {
     LaunchScope _ls(K_PERMUTE_BWD, st);
-    permute_bwd_kernel<<<ceil_div(d.T, 256 / tpr), 256, 0, st>>>(dx_perm, slot, dx32, d.T, d.H,
-                                                                 d.k, (long long)d.T * d.k, tpr);
+    launch_k(permute_bwd_kernel, ceil_div(d.T, 256 / tpr), 256, 0, st, dx_perm, slot, dx32, d.T,
+             d.H, d.k, (long long)d.T * d.k, tpr);
   }
   return check_launch("permute_bwd_kernel");
 }

@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) route_logits_kernel(
     const bf16* __restrict__ x, const bf16* __restrict__ w_r, const float* __restrict__ bias,
     float* __restrict__ z, int32_t* __restrict__ idx, float* __restrict__ gates, int T, int H,
     int E, int k, int forced) {
+  pdl_wait();
   constexpr int NW = kRouteNw, NT = NW * 32;
   constexpr int TB = 4 * TPL;
   constexpr int EW = kRouteEb / NW;  // experts per warp
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                                                          int32_t* __restrict__ idx,
                                                          float* __restrict__ gates, int T, int E,
                                                          int k, int forced) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -303,6 +305,7 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     const int32_t* __restrict__ idx, const bf16* __restrict__ w_r, const float* __restrict__ dx32,
     const bf16* __restrict__ dx_perm, const int32_t* __restrict__ slot, bf16* __restrict__ dx,
     float* __restrict__ dz, int T, int H, int E, int k, int* status) {
+  pdl_wait();
   constexpr int KB = KMAX < 8 ? KMAX : 8;  // rows in flight per batch
   extern __shared__ __align__(16) uint8_t s_wr[];  // [E][kDxPitchB]
   const int c = blockIdx.y * 8 + (threadIdx.x & 7);  // 16-byte chunk of the row
@@ -449,6 +452,7 @@ __global__ void __launch_bounds__(256) route_bwd_dwr_partial_kernel(
     const int32_t* __restrict__ off, const int32_t* __restrict__ row_src,
     const float* __restrict__ dz, const bf16* __restrict__ x, float* __restrict__ part, int T,
     int H, int E, int k, int* status) {
+  pdl_wait();
   extern __shared__ int s_prefix[];
   __shared__ int s_tok[kRouteBwdRowsPerChunk];
   __shared__ float s_w[kRouteBwdRowsPerChunk];
@@ -496,6 +500,7 @@ __global__ void __launch_bounds__(256) route_bwd_dwr_partial_kernel(
 __global__ void __launch_bounds__(256) route_bwd_dwr_reduce_kernel(
     const int32_t* __restrict__ off, const float* __restrict__ part, float* __restrict__ dw_r,
     int H, int E) {
+  pdl_wait();
   __shared__ int s_first, s_n;
   const int e = blockIdx.x;
   if (threadIdx.x < 32) {
@@ -535,9 +540,8 @@ cudaError_t launch_logits_t(const moe_layer_desc_t& d, dim3 grid, const bf16* x,
   static cudaError_t attr = cudaFuncSetAttribute(
       route_logits_kernel<TPL, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return attr;
-  route_logits_kernel<TPL, FUSE><<<grid, kRouteNw * 32, smem, st>>>(x, w_r, bias, logits, idx,
-                                                                    gates, d.T, d.H, d.E, d.k,
-                                                                    forced);
+  launch_k(route_logits_kernel<TPL, FUSE>, grid, kRouteNw * 32, smem, st, x, w_r, bias, logits, idx,
+           gates, d.T, d.H, d.E, d.k, forced);
   return cudaSuccess;
 }
 
@@ -584,8 +588,8 @@ moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* 
   const int forced = d.mode == MOE_ROUTE_FORCED_BALANCED;
   {
     LaunchScope _ls(K_ROUTE_TOPK, st);
-    route_topk_kernel<8><<<dim3(ceil_div(d.T, warps)), tpb, 0, st>>>(logits, idx, gates, d.T, d.E,
-                                                                     d.k, forced);
+    launch_k(route_topk_kernel<8>, dim3(ceil_div(d.T, warps)), tpb, 0, st, logits, idx, gates, d.T,
+             d.E, d.k, forced);
   }
   return check_launch("route_topk_kernel");
 }
@@ -597,17 +601,17 @@ void launch_dx(const moe_layer_desc_t& d, const float* dgates, const float* gate
   const dim3 g(ceil_div(d.T, kDxTok), d.H / 64);
   const size_t smem = (size_t)d.E * kDxPitchB;
   if (d.k <= 4)
-    route_bwd_dx_kernel<4, FUSED><<<g, 256, smem, st>>>(dgates, gates, idx, w_r, dx32, dx_perm,
-                                                        slot, dx, dz, d.T, d.H, d.E, d.k, status);
+    launch_k(route_bwd_dx_kernel<4, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
+             dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
   else if (d.k <= 8)
-    route_bwd_dx_kernel<8, FUSED><<<g, 256, smem, st>>>(dgates, gates, idx, w_r, dx32, dx_perm,
-                                                        slot, dx, dz, d.T, d.H, d.E, d.k, status);
+    launch_k(route_bwd_dx_kernel<8, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
+             dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
   else if (d.k <= 16)
-    route_bwd_dx_kernel<16, FUSED><<<g, 256, smem, st>>>(dgates, gates, idx, w_r, dx32, dx_perm,
-                                                         slot, dx, dz, d.T, d.H, d.E, d.k, status);
+    launch_k(route_bwd_dx_kernel<16, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
+             dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
   else
-    route_bwd_dx_kernel<32, FUSED><<<g, 256, smem, st>>>(dgates, gates, idx, w_r, dx32, dx_perm,
-                                                         slot, dx, dz, d.T, d.H, d.E, d.k, status);
+    launch_k(route_bwd_dx_kernel<32, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
+             dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
 }
 
 moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,
@@ -634,8 +638,8 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
     dim3 ga(max_chunks, ceil_div(cpr, 256));
     {
       LaunchScope _ls(K_ROUTE_BWD_DWR_PARTIAL, st);
-      route_bwd_dwr_partial_kernel<<<ga, 256, (d.E + 1) * sizeof(int), st>>>(
-          off, row_src, dz, x, dwr_part, d.T, d.H, d.E, d.k, status);
+      launch_k(route_bwd_dwr_partial_kernel, ga, 256, (d.E + 1) * sizeof(int), st, off, row_src, dz,
+               x, dwr_part, d.T, d.H, d.E, d.k, status);
     }
     moe_status_t s = check_launch("route_bwd_dwr_partial_kernel");
     if (s != MOE_OK) return s;
@@ -643,7 +647,7 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
   dim3 gb(d.E, ceil_div(d.H / 4, 256));
   {
     LaunchScope _ls(K_ROUTE_BWD_DWR_REDUCE, st);
-    route_bwd_dwr_reduce_kernel<<<gb, 256, 0, st>>>(off, dwr_part, dw_r, d.H, d.E);
+    launch_k(route_bwd_dwr_reduce_kernel, gb, 256, 0, st, off, dwr_part, dw_r, d.H, d.E);
   }
   return check_launch("route_bwd_dwr_reduce_kernel");
 }
