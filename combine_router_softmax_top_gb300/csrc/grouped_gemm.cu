@@ -39,6 +39,12 @@
 #ifndef MOE_PAIR
 #define MOE_PAIR 1
 #endif
+#ifndef MOE_WG1_CS
+#define MOE_WG1_CS 2
+#endif
+#ifndef MOE_WG2_CS
+#define MOE_WG2_CS 2
+#endif
 
 namespace moe {
 
@@ -74,13 +80,17 @@ struct Mode {
   // its own 128 rows of A and half of B, so a CTA takes in 32 KB per K stage
   // instead of 48 KB and holds 6 stages. Pairs speed up the forward and dgrad
   // GEMMs. The short-K wgrad tiles (4 K stages per expert at 256 rows) stay
-  // unpaired and share B across 4 CTAs by multicast (kCS = 4): a paired wgrad
-  // (each CTA loading its own A and half of B, 128 KB per 128 x 256 output
-  // instead of 192 KB received) was measured 1.6x slower, its producer taking
-  // 4.0 us per tile to land 128 KB against 2.1 us for the multicast layout's
-  // 96 KB of loads.
+  // unpaired and share B across a cluster by multicast. Measured on the
+  // 256-rows-per-expert layer, clusters of 2 are fastest (W1 201 us against
+  // 208 us unclustered and 220 to 223 us with 3, 4 or 6 CTAs; W2 115 us with
+  // 2 to 4, 129 us with 8). A paired wgrad (each CTA loading its own A and
+  // half of B, 128 KB per 128 x 256 output instead of 192 KB received) was
+  // measured 1.6x slower: its producer took 4.0 us per tile to land 128 KB,
+  // against 2.1 us in 4-CTA clusters (96 KB of loads per CTA).
   static constexpr bool kPair = MOE_PAIR && !kRagK;
-  static constexpr int kCS = kPair ? 2 : kRagK ? 4 : MOE_ROW_CS;
+  static constexpr int kCS = kPair ? 2
+                            : MODE == GEMM_WGRAD_W1 ? MOE_WG1_CS
+                            : MODE == GEMM_WGRAD_W2 ? MOE_WG2_CS : MOE_ROW_CS;
   // The FC2 dgrad epilogue needs the tile's saved pre-activation (gate and up)
   // next to the accumulator: a dedicated warp TMA-loads it into shared memory
   // ahead of the epilogue, one 64-column quarter (gate and up, 32 KB) at a time.
@@ -924,11 +934,13 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
       break;
     case GEMM_WGRAD_W1:
       ok = make_map(&ma, g.A, N, 2 * F, 64) && make_map(&mb, g.B, N, H, 64);
-      ntile_bound = (long long)E * (((2 * F + BM - 1) / BM + 3) / 4 * 4) * ((H + BN - 1) / BN);
+      ntile_bound = (long long)E * ceil_div(ceil_div(2 * F, BM), Mode<GEMM_WGRAD_W1>::kCS) *
+                    Mode<GEMM_WGRAD_W1>::kCS * ((H + BN - 1) / BN);
       break;
     case GEMM_WGRAD_W2:
       ok = make_map(&ma, g.A, N, H, 64) && make_map(&mb, g.B, N, F, 64);
-      ntile_bound = (long long)E * (((H + BM - 1) / BM + 3) / 4 * 4) * ((F + BN - 1) / BN);
+      ntile_bound = (long long)E * ceil_div(ceil_div(H, BM), Mode<GEMM_WGRAD_W2>::kCS) *
+                    Mode<GEMM_WGRAD_W2>::kCS * ((F + BN - 1) / BN);
       break;
     default:
       set_error("unknown grouped GEMM mode %d", g.mode);
