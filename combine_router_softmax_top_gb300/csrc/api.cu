@@ -4,6 +4,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "moe_internal.cuh"
 #include "moe_layer_ops.h"
 
@@ -31,6 +33,37 @@ moe_status_t check_launch(const char* what) {
     return MOE_ERR_CUDA;
   }
   return MOE_OK;
+}
+
+// Per-device copy stream and events for moe_layer_step_host, created on first
+// use with that device current and kept until exit.
+struct CopyLane {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t start = nullptr, dy_in = nullptr, fwd_done = nullptr, y_out = nullptr;
+};
+
+CopyLane* copy_lane() {
+  constexpr int kMaxDevices = 64;
+  static CopyLane lanes[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    set_error("no usable current device for the copy stream");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  CopyLane& l = lanes[dev];
+  if (!l.stream) {
+    cudaError_t e = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&l.start, &l.dy_in, &l.fwd_done, &l.y_out})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      set_error("copy stream setup: %s", cudaGetErrorString(e));
+      l.stream = nullptr;
+      return nullptr;
+    }
+  }
+  return &l;
 }
 
 int device_sm_count() {
@@ -429,8 +462,8 @@ moe_status_t moe_layer_backward(const moe_layer_desc_t* d, const moe_mb_bufs_t* 
 }
 
 moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
-                                 const moe_bf16* host_x, const moe_bf16* host_dy, moe_bf16* host_y,
-                                 moe_bf16* host_dx, void* stream) {
+                                 const moe_bf16* host_x, const moe_bf16* host_dy,
+                                 moe_bf16* host_y, moe_bf16* host_dx, void* stream) {
   MOE_CHECK(validate(d));
   MOE_CHECK(check_mb(*d, b, true));
   if (!host_x || !host_dy || !host_y || !host_dx) {
@@ -439,16 +472,42 @@ moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t*
   }
   const size_t bytes = (size_t)d->T * d->H * sizeof(moe_bf16);
   cudaStream_t st = S(stream);
-  cudaError_t e = cudaMemcpyAsync(const_cast<moe_bf16*>(b->x), host_x, bytes, cudaMemcpyHostToDevice, st);
+  CopyLane* cl = copy_lane();
+  if (!cl) return MOE_ERR_CUDA;
+  // x goes in first on the compute stream. dy goes in on the copy stream while
+  // the forward runs. y comes out on the copy stream while the backward runs.
+  // dx comes out last.
+  cudaError_t e = cudaEventRecord(cl->start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cl->stream, cl->start, 0);
   if (e == cudaSuccess)
-    e = cudaMemcpyAsync(const_cast<moe_bf16*>(b->dy), host_dy, bytes, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) { set_error("host to device copy: %s", cudaGetErrorString(e)); return MOE_ERR_CUDA; }
+    e = cudaMemcpyAsync(const_cast<moe_bf16*>(b->x), host_x, bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<moe_bf16*>(b->dy), host_dy, bytes, cudaMemcpyHostToDevice,
+                        cl->stream);
+  if (e == cudaSuccess) e = cudaEventRecord(cl->dy_in, cl->stream);
+  if (e != cudaSuccess) {
+    set_error("host to device copy: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
   MOE_CHECK(moe_layer_forward(d, b, stream));
+  e = cudaEventRecord(cl->fwd_done, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cl->stream, cl->fwd_done, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(host_y, b->y, bytes, cudaMemcpyDeviceToHost, cl->stream);
+  if (e == cudaSuccess) e = cudaEventRecord(cl->y_out, cl->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, cl->dy_in, 0);
+  if (e != cudaSuccess) {
+    set_error("copy stream: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
   MOE_CHECK(moe_layer_backward(d, b, 1, stream));
-  e = cudaMemcpyAsync(host_y, b->y, bytes, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(host_dx, b->dx, bytes, cudaMemcpyDeviceToHost, st);
+  e = cudaMemcpyAsync(host_dx, b->dx, bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, cl->y_out, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) { set_error("device to host copy: %s", cudaGetErrorString(e)); return MOE_ERR_CUDA; }
+  if (e != cudaSuccess) {
+    set_error("device to host copy: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
   return MOE_OK;
 }
 
