@@ -84,9 +84,12 @@ struct Mode {
   // 256-rows-per-expert layer, clusters of 2 are fastest (W1 201 us against
   // 208 us unclustered and 220 to 223 us with 3, 4 or 6 CTAs; W2 115 us with
   // 2 to 4, 129 us with 8). A paired wgrad (each CTA loading its own A and
-  // half of B, 128 KB per 128 x 256 output instead of 192 KB received) was
-  // measured 1.6x slower: its producer took 4.0 us per tile to land 128 KB,
-  // against 2.1 us in 4-CTA clusters (96 KB of loads per CTA).
+  // half of B, 128 KB per 128 x 256 output instead of 192 KB received) stays
+  // slower even with the pair handshakes trimmed (one arrival per stage, the
+  // odd CTA's accumulator release forwarded once per tile): W1 222 us, W2
+  // 130 us. A trace shows each short tile's MMA resuming 1.3 to 1.6 us after
+  // both epilogues released the accumulator, a latency two accumulators do
+  // not hide when a tile's MMAs take 1.2 us.
   static constexpr bool kPair = MOE_PAIR && !kRagK;
   static constexpr int kCS = kPair ? 2
                             : MODE == GEMM_WGRAD_W1 ? MOE_WG1_CS
@@ -144,6 +147,7 @@ struct SmemCtl {
   uint64_t empty[kStagesMax];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
+  uint64_t epi_done[2];  // pair, odd CTA: its epilogue warps released the accumulator
   uint64_t tail;
   uint64_t drain;
   uint64_t aux_full;
@@ -328,8 +332,10 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl.tmem_full[b], 1);
-      // pair: the even CTA's MMA waits for both CTAs' epilogues
-      ptx::mbar_init(&ctl.tmem_empty[b], M::kPair ? 512 : 256);
+      // one arrival per epilogue warp; pair: the even CTA's MMA also waits
+      // for the odd CTA's epilogue, reported by one forwarded arrival
+      ptx::mbar_init(&ctl.tmem_empty[b], M::kPair ? 9 : 8);
+      ptx::mbar_init(&ctl.epi_done[b], 8);
     }
     ptx::mbar_init(&ctl.tail, 1);
     ptx::mbar_init(&ctl.drain, 1);
@@ -575,6 +581,25 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         int dummy = 0;
         ptx::mbar_wait(&ctl.drain, 0, &dummy, kWaitLimitNs);
       }
+    } else if (lane == 0 && M::kPair) {
+      // odd CTA of a pair: forward "accumulator free" to the even CTA's MMA
+      // issuer, one cluster arrival per tile once all 8 epilogue warps have
+      // arrived locally (fewer cluster-scope arrivals than one per warp).
+      int cursor = 0, acc = 0;
+      uint32_t acc_phase = 0;
+      for (int tile = first; tile < total; tile += stride) {
+        const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
+        if (t.nk == 0) continue;
+        if (!ptx::mbar_wait(&ctl.epi_done[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
+          flag_timeout(ctl, p.status, 9);
+          break;
+        }
+        ptx::mbar_arrive_cluster(ptx::mapa_shared(&ctl.tmem_empty[acc], 0));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
     }
     __syncwarp();
   } else if (M::kAux && warp == 10) {
@@ -740,11 +765,12 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
         }
       }
       if (tr) trace(p, MODE, ew == 0 ? 5 : 7, ti);
+      // one arrival per epilogue warp once all its lanes' TMEM reads are done
+      // (in the odd CTA of a pair, on the local barrier its MMA warp forwards)
       ptx::tc_fence_before();
-      if (M::kPair && crank != 0)
-        ptx::mbar_arrive_cluster(ptx::mapa_shared(&ctl.tmem_empty[acc], 0));
-      else
-        ptx::mbar_arrive(&ctl.tmem_empty[acc]);
+      __syncwarp();
+      if (lane == 0)
+        ptx::mbar_arrive(M::kPair && crank != 0 ? &ctl.epi_done[acc] : &ctl.tmem_empty[acc]);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
