@@ -54,39 +54,56 @@ def peaks():
 
 
 def algorithmic(d) -> dict:
-    """Minimum bytes moved and flops per launch of each kernel for shape d.
+    """Minimum bytes read, bytes written and flops per launch of each kernel.
 
-    Bytes count each tensor the kernel must read or write once (x re-reads of
-    the gathers are served by L2 and not counted); flops count multiply-adds
-    as 2."""
+    Bytes count each tensor the kernel must read or write once (the k-fold
+    re-reads of x in the gathers are served by L2 and not counted); flops count
+    multiply-adds as 2. Returns {kernel: (read_bytes, write_bytes, flops)}."""
     T, H, E, k, F = d["T"], d["H"], d["E"], d["k"], d["F"]
     N = T * k
     b2, b4 = 2, 4
+    fused_topk = E <= 128  # the routing is fused into the logits kernel
     out = {
-        # with E <= 128 the routing (top-k, gates) is fused into the logits kernel
-        "route_logits": (T * H * b2 + E * H * b2 + T * E * b4 + (2 * N * b4 if E <= 128 else 0),
-                         2.0 * T * H * E),
-        "route_topk": (T * E * b4 + 2 * N * b4, 0.0),
-        "layout_count": (N * b4, 0.0),
-        "layout_assign": (N * b4 + 2 * N * b4, 0.0),
-        "permute": (T * H * b2 + N * b4 + N * H * b2, 0.0),
-        "combine": (N * H * b2 + 2 * N * b4 + T * H * b2, 2.0 * N * H),
-        "combine_bwd": (T * H * b2 + N * H * b2 + 2 * N * b4 + N * H * b2 + N * b4, 3.0 * N * H),
-        "permute_bwd": (N * H * b2 + N * b4 + T * H * b4, 1.0 * N * H),
-        "route_bwd_dx": (T * H * b4 + E * H * b2 + 3 * N * b4 + T * H * b2, 2.0 * N * H),
+        "route_logits": (T * H * b2 + E * H * b2,
+                         T * E * b4 + (2 * N * b4 if fused_topk else 0), 2.0 * T * H * E),
+        "route_topk": (T * E * b4, 2 * N * b4, 0.0),
+        "layout_count": (N * b4, 0, 0.0),
+        "layout_assign": (N * b4, 2 * N * b4, 0.0),
+        "permute": (T * H * b2 + N * b4, N * H * b2, 0.0),
+        "combine": (N * H * b2 + 2 * N * b4, T * H * b2, 2.0 * N * H),
+        "combine_bwd": (T * H * b2 + N * H * b2 + 2 * N * b4, N * H * b2 + N * b4, 3.0 * N * H),
+        "permute_bwd": (N * H * b2 + N * b4, T * H * b4, 1.0 * N * H),
+        "route_bwd_dx": (T * H * b4 + E * H * b2 + 3 * N * b4, T * H * b2, 2.0 * N * H),
         # permute backward fused with the router's dx pass (the layer path)
-        "dispatch_bwd": (N * H * b2 + 4 * N * b4 + E * H * b2 + T * H * b2, 3.0 * N * H),
-        "route_bwd_dwr_partial": (T * H * b2 + 2 * N * b4, 2.0 * N * H),
-        "route_bwd_dwr_reduce": (E * H * b4, 0.0),
-        "gemm_fc1_fwd": (N * H * b2 + E * 2 * F * H * b2 + N * 2 * F * b2 + N * F * b2,
+        "dispatch_bwd": (N * H * b2 + 3 * N * b4 + E * H * b2, T * H * b2 + N * b4, 3.0 * N * H),
+        "route_bwd_dwr_partial": (T * H * b2 + 2 * N * b4, 0, 2.0 * N * H),
+        "route_bwd_dwr_reduce": (E * H * b4, 0, 0.0),
+        "gemm_fc1_fwd": (N * H * b2 + E * 2 * F * H * b2, N * 2 * F * b2 + N * F * b2,
                          2.0 * N * H * 2 * F),
-        "gemm_fc2_fwd": (N * F * b2 + E * H * F * b2 + N * H * b2, 2.0 * N * F * H),
-        "gemm_fc2_dgrad": (N * H * b2 + E * H * F * b2 + 2 * N * 2 * F * b2, 2.0 * N * H * F),
-        "gemm_fc1_dgrad": (N * 2 * F * b2 + E * 2 * F * H * b2 + N * H * b2, 2.0 * N * 2 * F * H),
-        "gemm_wgrad_w1": (N * 2 * F * b2 + N * H * b2 + E * 2 * F * H * b2, 2.0 * N * 2 * F * H),
-        "gemm_wgrad_w2": (N * H * b2 + N * F * b2 + E * H * F * b2, 2.0 * N * H * F),
+        "gemm_fc2_fwd": (N * F * b2 + E * H * F * b2, N * H * b2, 2.0 * N * F * H),
+        "gemm_fc2_dgrad": (N * H * b2 + E * H * F * b2 + N * 2 * F * b2, N * 2 * F * b2,
+                           2.0 * N * H * F),
+        "gemm_fc1_dgrad": (N * 2 * F * b2 + E * 2 * F * H * b2, N * H * b2, 2.0 * N * 2 * F * H),
+        "gemm_wgrad_w1": (N * 2 * F * b2 + N * H * b2, E * 2 * F * H * b2, 2.0 * N * 2 * F * H),
+        "gemm_wgrad_w2": (N * H * b2 + N * F * b2, E * H * F * b2, 2.0 * N * H * F),
     }
     return out
+
+
+def hbm_write_gbs(dev) -> float:
+    """Write-only HBM bandwidth, measured live: best of 5 zero-fills of 1 GiB."""
+    buf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    best = float("inf")
+    for i in range(8):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        buf.zero_()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        if i >= 3:
+            best = min(best, e0.elapsed_time(e1))
+    del buf
+    return (1 << 30) / (best * 1e-3) / 1e9
 
 
 KERNEL_SOURCES = {  # the files each kernel family is built from
@@ -297,10 +314,15 @@ def run_ours(args, rank, world, local):
         a = agg.setdefault(name, [0, 0.0])
         a[0] += 1
         a[1] += t
+    wr_gbs = hbm_write_gbs(dev)
     kernels = {}
     for name, (n, tot) in agg.items():
         avg_ms = tot / n
-        by, fl = algo.get(name, (0.0, 0.0))
+        rd, wr, fl = algo.get(name, (0.0, 0.0, 0.0))
+        by = rd + wr
+        # HBM floor with writes counted at the write-only rate: a kernel that
+        # mostly writes (the weight gradients) cannot reach the copy bandwidth
+        t_floor = max(by / (pk["hbm_gbs"] * 1e9), wr / (wr_gbs * 1e9))
         gbs = by / (avg_ms * 1e-3) / 1e9 if avg_ms > 0 else 0.0
         tfl = fl / (avg_ms * 1e-3) / 1e12 if avg_ms > 0 else 0.0
         t_hbm = by / (pk["hbm_gbs"] * 1e9)
@@ -314,7 +336,9 @@ def run_ours(args, rank, world, local):
         kernels[name] = {"launches": n, "avg_us": round(avg_ms * 1e3, 2),
                          "share": None, "GB_s": round(gbs, 1), "TFLOP_s": round(tfl, 1),
                          "bound": bound, "roofline_frac": round(frac, 3),
-                         "algo_bytes": int(by), "algo_flops": fl}
+                         "hbm_floor_us": round(t_floor * 1e6, 1),
+                         "hbm_floor_frac": round(t_floor / (avg_ms * 1e-3), 3) if avg_ms > 0 else None,
+                         "algo_bytes": int(by), "algo_write_bytes": int(wr), "algo_flops": fl}
     total = sum(v[1] for v in agg.values())
     for name in kernels:
         kernels[name]["share"] = round(agg[name][1] / total, 4) if total else None
@@ -329,16 +353,19 @@ def run_ours(args, rank, world, local):
     else:
         roof = {"bound": "hbm", "achieved": kd["GB_s"], "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    # the same kernel against its HBM floor with writes at the write-only rate
+    roof["write_aware"] = {"hbm_write_gbs_live": round(wr_gbs, 1), "floor_us": kd["hbm_floor_us"],
+                           "frac": kd["hbm_floor_frac"]}
     roof["traffic"] = traffic_for(dom, args.workload)
     roof["kernel"] = dom
     roof["peak_kind"] = pk_kind
     gemm_names = [n for n in kernels if n.startswith("gemm")]
     gemm_ms = sum(agg[n][1] for n in gemm_names) / args.steps
-    gemm_fl = sum(algo[n][1] for n in gemm_names)
+    gemm_fl = sum(algo[n][2] for n in gemm_names)
     pc_names = [n for n in ("permute", "combine", "combine_bwd", "permute_bwd", "dispatch_bwd")
                 if n in agg]
     pc_ms = sum(agg[n][1] for n in pc_names) / args.steps
-    pc_bytes = sum(algo[n][0] for n in pc_names)
+    pc_bytes = sum(algo[n][0] + algo[n][1] for n in pc_names)
 
     # ---- end to end through the host-buffer C-ABI call
     hx = inp.x.clone().pin_memory()

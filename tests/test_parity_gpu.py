@@ -43,6 +43,11 @@ CASES = {
     "one_token": lambda: moe_synth.make_inputs(T=1, H=64, E=8, k=2, F=64, seed=17),
     # wide layer, deep K: several K stages and wide rows
     "wide": lambda: moe_synth.make_inputs(T=256, H=1024, E=8, k=2, F=512, seed=18),
+    # the maximum expert count: two 128-expert router blocks, the separate top-k
+    # kernel, 256-entry layout tables and tile prefixes
+    "max_experts": lambda: moe_synth.make_inputs(T=200, H=128, E=256, k=8, F=64, seed=26),
+    # k above 16: the 32-slot variants of the combine and router backward
+    "large_k": lambda: moe_synth.make_inputs(T=150, H=192, E=32, k=20, F=64, seed=27),
 }
 
 
