@@ -89,6 +89,8 @@ WsLayout ws_layout(const moe_layer_desc_t& d) {
   o = align256(o + (size_t)N * sizeof(float));
   w.dwr_part = o;
   o = align256(o + (size_t)chunks * d.H * sizeof(float));
+  w.dep = o;
+  o = align256(o + (size_t)d.E * sizeof(int));
   w.total = o;
   return w;
 }
@@ -174,13 +176,15 @@ moe_status_t op_ffn_fwd(const moe_layer_desc_t& d, const bf16* x_perm, const int
   g.out1 = h;
   g.status = status_of(ws);
   g.max_ctas = max_ctas;
-  MOE_CHECK(launch_grouped_gemm(d, g, st));
-  g.mode = GEMM_FC2_FWD;
-  g.A = h;
-  g.B = w2;
-  g.out0 = o;
-  g.out1 = nullptr;
-  return launch_grouped_gemm(d, g, st);
+  g.dep = ws_at<int>(ws, ws_layout(d).dep);
+  GemmArgs g2 = g;
+  g2.mode = GEMM_FC2_FWD;
+  g2.A = h;
+  g2.B = w2;
+  g2.out0 = o;
+  g2.out1 = nullptr;
+  // FC2 tiles of an expert start as soon as its FC1 tiles are stored
+  return launch_grouped_gemm_chain(d, g, g2, st);
 }
 
 moe_status_t op_dgrad(const moe_layer_desc_t& d, const bf16* d_o, const bf16* a,
@@ -195,13 +199,15 @@ moe_status_t op_dgrad(const moe_layer_desc_t& d, const bf16* d_o, const bf16* a,
   g.aux = a;
   g.status = status_of(ws);
   g.max_ctas = max_ctas;
-  MOE_CHECK(launch_grouped_gemm(d, g, st));
-  g.mode = GEMM_FC1_DGRAD;
-  g.A = da;
-  g.B = w1;
-  g.out0 = dx_perm;
-  g.aux = nullptr;
-  return launch_grouped_gemm(d, g, st);
+  g.dep = ws_at<int>(ws, ws_layout(d).dep);
+  GemmArgs g2 = g;
+  g2.mode = GEMM_FC1_DGRAD;
+  g2.A = da;
+  g2.B = w1;
+  g2.out0 = dx_perm;
+  g2.aux = nullptr;
+  // FC1 dgrad tiles of an expert start as soon as its da is stored
+  return launch_grouped_gemm_chain(d, g, g2, st);
 }
 
 moe_status_t op_wgrad(const moe_layer_desc_t& d, const bf16* x_perm, const bf16* h,

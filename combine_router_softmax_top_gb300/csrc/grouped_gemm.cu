@@ -67,6 +67,7 @@ struct KParams {
   bf16* out1;
   const bf16* aux;
   int* status;
+  int* dep;  // fused launches: per-expert count of first-mode epilogue warps done
 };
 
 template <int MODE>
@@ -102,17 +103,16 @@ struct Mode {
   static constexpr int kBBytes = kBN * BK * 2;            // whole B tile per stage
   static constexpr int kBBytesCta = kPair ? kBBytes / 2 : kBBytes;  // B bytes this CTA loads
   static constexpr int kStageBytes = kABytes + kBBytesCta;
+  // stages of the operand ring (with the aux buffer a launch fits 5 pair stages);
+  // the warps are a producer, the MMA issuer, 8 epilogue warps and, for kAux,
+  // the aux loader (see Fuse below, which sizes a launch)
   static constexpr int kStages = kPair ? (kAux ? 5 : 6) : 4;
-  static constexpr int kAuxBytes = kAux ? 2 * 16384 : 0;
-  static constexpr int kWarps = kAux ? 11 : 10;  // producer, MMA, 8 epilogue (+ aux loader)
   // Plain bf16 outputs leave through TMA tensor stores of 32 x 32 boxes (the
   // staging buffer is the box): 2D [rows, cols] maps for the forward FC2 and
   // FC1 dgrad outputs, 3D [expert, rows, cols] maps for the weight gradients,
   // whose clipping at the matrix edge makes every wgrad box storable. 0: none.
   static constexpr int kStoreDims =
       (MODE == GEMM_FC2_FWD || MODE == GEMM_FC1_DGRAD) ? 2 : kRagK ? 3 : 0;
-  static constexpr size_t kDynSmem =
-      (size_t)kStages * kStageBytes + kAuxBytes + kEpiStageBytes + 1024;
   static_assert(kStages <= kStagesMax, "barrier arrays");
   // reduction depth for the row-ragged modes
   __device__ static int kdim(const KParams& p) {
@@ -154,19 +154,20 @@ struct SmemCtl {
   uint64_t aux_empty;
   uint32_t tmem_base;
   int abort;
-  int tstart[kMaxE + 1];
+  int tstart[kMaxE + 1];   // tile prefix of the (first) mode
+  int tstart2[kMaxE + 1];  // tile prefix of the second mode of a fused launch
   int off[kMaxE + 1];
 };
 
 template <int MODE>
-__device__ __forceinline__ Tile tile_at(const KParams& p, const SmemCtl& c, int tile, int& cursor,
-                                       uint32_t rank = 0) {
-  while (c.tstart[cursor + 1] <= tile) ++cursor;
+__device__ __forceinline__ Tile tile_at(const KParams& p, const int* tstart, const int* off,
+                                       int tile, int& cursor, uint32_t rank = 0) {
+  while (tstart[cursor + 1] <= tile) ++cursor;
   Tile t;
   t.e = cursor;
-  t.row0 = c.off[t.e];
-  const int cnt = c.off[t.e + 1] - t.row0;
-  const int local = tile - c.tstart[t.e];
+  t.row0 = off[t.e];
+  const int cnt = off[t.e + 1] - t.row0;
+  const int local = tile - tstart[t.e];
   if (Mode<MODE>::kRagK) {
     // one cluster tile = kCS consecutive M blocks of one (expert, N block)
     constexpr int cs = Mode<MODE>::kCS;
@@ -307,13 +308,456 @@ __device__ __forceinline__ float round_bf16(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// Launch-wide constants of a kernel that runs the tiles of MODE and then, when
+// MODE2 >= 0, those of MODE2 in the same persistent launch. MODE2's tiles of
+// expert e wait until every tile of expert e of MODE has stored its output
+// (per-expert counters), so one grid works through both GEMMs and the second
+// fills the last, partial round of tiles of the first.
+template <int MODE, int MODE2>
+struct Fuse {
+  using A = Mode<MODE>;
+  using B = Mode<(MODE2 >= 0 ? MODE2 : MODE)>;
+  static constexpr bool kHas2 = MODE2 >= 0;
+  static constexpr bool kAux = A::kAux || (kHas2 && B::kAux);
+  static constexpr int kStages = A::kStages < B::kStages ? A::kStages : B::kStages;
+  static constexpr int kStageBytes = A::kStageBytes;
+  static constexpr int kAuxBytes = kAux ? 2 * 16384 : 0;
+  static constexpr int kWarps = kAux ? 11 : 10;
+  static constexpr bool kPair = A::kPair;
+  static constexpr int kCS = A::kCS;
+  static constexpr bool kStores = A::kStoreDims != 0 || (kHas2 && B::kStoreDims != 0);
+  static constexpr size_t kDynSmem =
+      (size_t)kStages * kStageBytes + kAuxBytes + kEpiStageBytes + 1024;
+  static_assert(A::kStageBytes == B::kStageBytes && A::kPair == B::kPair && A::kCS == B::kCS &&
+                    A::kAMn == B::kAMn && A::kBMn == B::kBMn && A::kBN == B::kBN &&
+                    A::kRagK == B::kRagK,
+                "fused modes must share the tile machinery");
+};
+
+// What every role needs about its CTA.
+struct Role {
+  uint8_t* smem;
+  SmemCtl* ctl;
+  uint32_t crank;
+  uint16_t cmask;
+  uint32_t tmem_base;
+  int lane;
+};
+
+// Tiles per expert -> exclusive prefix (warp 0).
 template <int MODE>
-__global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
+__device__ __forceinline__ void tile_prefix(const KParams& p, const int* off, int* tstart,
+                                            int lane) {
+  using M = Mode<MODE>;
+  int carry = 0;
+  for (int base = 0; base < p.E; base += 32) {
+    const int e = base + lane;
+    int n = 0;
+    if (e < p.E) {
+      const int cnt = off[e + 1] - off[e];
+      if (M::kRagK)
+        n = (((M::wg_mdim(p) + BM - 1) / BM + M::kCS - 1) / M::kCS) * M::ntiles(p);
+      else n = (((cnt + BM - 1) / BM + M::kCS - 1) / M::kCS) * M::ntiles(p);
+      if (cnt < 0) n = 0;
+    }
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (e < p.E) tstart[e] = carry + incl - n;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) tstart[p.E] = carry;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Producer of a second-mode tile: wait (bounded) until expert e's first-mode
+// tiles have all stored their output, then order those generic-proxy writes
+// before this thread's TMA (async-proxy) reads of them.
+__device__ __forceinline__ bool wait_expert(const KParams& p, int e, int target,
+                                            volatile int* abort) {
+  if (ld_acquire(p.dep + e) < target) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ld_acquire(p.dep + e) < target) {
+      __nanosleep(128);
+      if (*abort) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+// ==================================================================== producer
+// Loads one tile's K stages (A and B) into the stage ring.
+template <int MODE, int KSTAGES>
+__device__ __forceinline__ bool producer_tile(const Role& R, const KParams& p,
+                                              const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                              const Tile& t, int& stage, uint32_t& phase,
+                                              uint32_t& tail_phase) {
+  using M = Mode<MODE>;
+  SmemCtl& ctl = *R.ctl;
+  const int lane = R.lane;
+  const uint32_t crank = R.crank;
+  const uint16_t cmask = R.cmask;
+  for (int kt = 0; kt < t.nk; ++kt) {
+    if (!ptx::mbar_wait(&ctl.empty[stage], phase ^ 1, &ctl.abort, kWaitLimitNs)) {
+      if (lane == 0) flag_timeout(ctl, p.status, 1);
+      return false;
+    }
+    uint8_t* sA = R.smem + stage * M::kStageBytes;
+    uint8_t* sB = sA + kABytes;
+    const int k0 = kt * BK;
+    const bool tail = M::kRagK && (t.rows - k0 < BK);
+    uint64_t* bar = tail ? &ctl.tail : &ctl.full[stage];
+    if (lane == 0) {
+      if (M::kRagK) {
+        // A: this CTA's own M block. B: slice i of the shared tile is loaded
+        // by cluster rank i % kCS and multicast to every CTA of the cluster,
+        // so full[stage] collects all 32 KB of B in every CTA. On the tail
+        // stage A goes to the tail barrier and full[stage] gets its arrival
+        // only after the zeroing below.
+        if (tail) {
+          ptx::mbar_arrive_expect_tx(&ctl.tail, kABytes);
+          ptx::mbar_expect_tx(&ctl.full[stage], M::kBBytes);
+        } else {
+          ptx::mbar_arrive_expect_tx(&ctl.full[stage], M::kStageBytes);
+        }
+        const int r = t.row0 + k0;
+        ptx::tma_load_2d(sA, tmA, bar, t.m0, r);
+        ptx::tma_load_2d(sA + 8192, tmA, bar, t.m0 + 64, r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (M::kCS == 1)
+            ptx::tma_load_2d(sB + 8192 * i, tmB, &ctl.full[stage], t.n0 + 64 * i, r);
+          else if (i % M::kCS == (int)crank)
+            ptx::tma_load_2d_multicast(sB + 8192 * i, tmB, &ctl.full[stage], t.n0 + 64 * i, r,
+                                       cmask);
+        }
+      } else if (M::kPair) {
+        // both CTAs' loads complete on the even CTA's full[stage]
+        const uint32_t fb = ptx::mapa_shared(&ctl.full[stage], 0);
+        if (crank == 0) ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * M::kStageBytes);
+        ptx::tma_load_2d_pair(sA, tmA, fb, k0, t.row0 + t.m0);
+        if (MODE == GEMM_FC1_FWD) {  // even CTA: 128 gate rows, odd CTA: 128 up rows
+          ptx::tma_load_2d_pair(sB, tmB, fb, k0, t.e * 2 * p.F + (crank ? p.F : 0) + t.n0);
+        } else if (MODE == GEMM_FC2_FWD) {
+          ptx::tma_load_2d_pair(sB, tmB, fb, k0, t.e * p.H + t.n0 + 128 * crank);
+        } else {  // MN-major B: this CTA's half of the N columns
+          const int base = MODE == GEMM_FC2_DGRAD ? t.e * p.H : t.e * 2 * p.F;
+          constexpr int nb = M::kBN / 128;  // 64-wide boxes per CTA
+#pragma unroll
+          for (int i = 0; i < nb; ++i)
+            ptx::tma_load_2d_pair(sB + 8192 * i, tmB, fb, t.n0 + 64 * (crank * nb + i), base + k0);
+        }
+      } else {
+        ptx::mbar_arrive_expect_tx(bar, M::kStageBytes);
+        ptx::tma_load_2d(sA, tmA, bar, k0, t.row0 + t.m0);
+        // B boxes: box i is loaded by cluster rank i % kCS and multicast
+        auto load_b = [&](int i, void* dst, int c0, int c1) {
+          if (M::kCS == 1)
+            ptx::tma_load_2d(dst, tmB, bar, c0, c1);
+          else if (i % M::kCS == (int)crank)
+            ptx::tma_load_2d_multicast(dst, tmB, bar, c0, c1, cmask);
+        };
+        if (MODE == GEMM_FC1_FWD) {
+          const int base = t.e * 2 * p.F;
+          load_b(0, sB, k0, base + t.n0);                // 128 gate rows
+          load_b(1, sB + 16384, k0, base + p.F + t.n0);  // 128 up rows
+        } else if (MODE == GEMM_FC2_FWD) {
+          load_b(0, sB, k0, t.e * p.H + t.n0);
+          load_b(1, sB + 16384, k0, t.e * p.H + t.n0 + 128);
+        } else {
+          const int base = MODE == GEMM_FC2_DGRAD ? t.e * p.H : t.e * 2 * p.F;
+#pragma unroll
+          for (int i = 0; i < M::kBN / 64; ++i) load_b(i, sB + 8192 * i, t.n0 + 64 * i, base + k0);
+        }
+      }
+    }
+    if (tail) {
+      // last K stage of a wgrad tile: zero the A rows past the expert's end
+      if (!ptx::mbar_wait(&ctl.tail, tail_phase, &ctl.abort, kWaitLimitNs)) {
+        if (lane == 0) flag_timeout(ctl, p.status, 2);
+        return false;
+      }
+      tail_phase ^= 1;
+      const int valid = t.rows - k0;       // 1..63
+      const int nzero = (BK - valid) * 8;  // 16-byte chunks per atom
+      for (int i = lane; i < 2 * nzero; i += 32) {
+        const int atom = i / nzero, j = i % nzero;
+        uint4* dst = reinterpret_cast<uint4*>(sA + atom * 8192 + valid * 128) + j;
+        *dst = make_uint4(0, 0, 0, 0);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ctl.full[stage]);
+    }
+    if (++stage == KSTAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
+// ==================================================================== MMA issuer
+// Issues one tile's MMAs into accumulator acc (pair: for both CTAs).
+template <int MODE, int KSTAGES>
+__device__ __forceinline__ bool mma_tile(const Role& R, const KParams& p, const Tile& t,
+                                         int& stage, uint32_t& phase, int& acc,
+                                         uint32_t& acc_phase, int ti) {
+  using M = Mode<MODE>;
+  SmemCtl& ctl = *R.ctl;
+  constexpr uint32_t idesc =
+      ptx::idesc_bf16_f32(M::kPair ? 2 * BM : BM, M::kBN, M::kAMn, M::kBMn);
+  constexpr uint32_t a_lbo = M::kAMn ? 8192 : 16, b_lbo = M::kBMn ? 8192 : 16;
+  constexpr uint32_t a_adv = M::kAMn ? (2048 >> 4) : (32 >> 4);
+  constexpr uint32_t b_adv = M::kBMn ? (2048 >> 4) : (32 >> 4);
+  if (t.nk == 0) return true;
+  if (!ptx::mbar_wait(&ctl.tmem_empty[acc], acc_phase ^ 1, &ctl.abort, kWaitLimitNs)) {
+    flag_timeout(ctl, p.status, 3);
+    return false;
+  }
+  ptx::tc_fence_after();
+  trace(p, MODE, 2, ti);
+  const uint32_t d_tmem = R.tmem_base + acc * kAccCols;
+  for (int kt = 0; kt < t.nk; ++kt) {
+    if (!ptx::mbar_wait(&ctl.full[stage], phase, &ctl.abort, kWaitLimitNs)) {
+      flag_timeout(ctl, p.status, 4);
+      return false;
+    }
+    ptx::tc_fence_after();
+    const uint32_t a_addr = ptx::smem_u32(R.smem + stage * M::kStageBytes);
+    const uint32_t b_addr = a_addr + kABytes;
+    const uint64_t adesc = ptx::sdesc_sw128(a_addr, a_lbo, 1024);
+    const uint64_t bdesc = ptx::sdesc_sw128(b_addr, b_lbo, 1024);
+#pragma unroll
+    for (int kk = 0; kk < BK / 16; ++kk) {
+      if (M::kPair)
+        ptx::umma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * a_adv), bdesc + (uint64_t)(kk * b_adv),
+                            idesc, (kt | kk) != 0);
+      else
+        ptx::umma_bf16(d_tmem, adesc + (uint64_t)(kk * a_adv), bdesc + (uint64_t)(kk * b_adv),
+                       idesc, (kt | kk) != 0);
+    }
+    // the stage is free once every CTA whose shared memory the MMAs read
+    // (pair) or that received the multicast B slices has consumed it
+    if (M::kPair) ptx::umma_commit_pair(&ctl.empty[stage], 3);
+    else if (M::kCS > 1) ptx::umma_commit_multicast(&ctl.empty[stage], R.cmask);
+    else ptx::umma_commit(&ctl.empty[stage]);
+    if (++stage == KSTAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  trace(p, MODE, 3, ti);
+  if (M::kPair) ptx::umma_commit_pair(&ctl.tmem_full[acc], 3);
+  else ptx::umma_commit(&ctl.tmem_full[acc]);
+  if (++acc == 2) {
+    acc = 0;
+    acc_phase ^= 1;
+  }
+  return true;
+}
+
+// ==================================================================== aux loader
+// Loads a tile's saved pre-activation (FC2 dgrad), a 64-column quarter at a
+// time, each once the epilogue has released the previous quarter.
+template <int MODE, int KSTAGES>
+__device__ __forceinline__ bool aux_tile(const Role& R, const KParams& p, const CUtensorMap* tmC,
+                                         const Tile& t, uint32_t& ph) {
+  using M = Mode<MODE>;
+  SmemCtl& ctl = *R.ctl;
+  uint8_t* aux = R.smem + KSTAGES * M::kStageBytes;
+  const int row = t.row0 + t.m0;
+  for (int qt = 0; qt < M::kBN / 64; ++qt) {
+    if (!ptx::mbar_wait(&ctl.aux_empty, ph ^ 1, &ctl.abort, kWaitLimitNs)) {
+      flag_timeout(ctl, p.status, 7);
+      return false;
+    }
+    ph ^= 1;
+    const int c = t.n0 + 64 * qt;
+    ptx::mbar_arrive_expect_tx(&ctl.aux_full, 2 * 16384);
+    ptx::tma_load_2d(aux, tmC, &ctl.aux_full, c, row);                // gate
+    ptx::tma_load_2d(aux + 16384, tmC, &ctl.aux_full, p.F + c, row);  // up
+  }
+  return true;
+}
+
+// ==================================================================== epilogue
+// One epilogue warp's share of a tile: TMEM -> registers -> fused math ->
+// stores; then the warp releases the accumulator and, with SIGNAL (the first
+// mode of a fused launch), counts the tile's expert as one warp further done.
+template <int MODE, int KSTAGES, int AUXB, bool SIGNAL>
+__device__ __forceinline__ bool epilogue_tile(const Role& R, const KParams& p,
+                                              const CUtensorMap* tmD, const Tile& t, int& acc,
+                                              uint32_t& acc_phase, uint32_t& aux_phase, int ew,
+                                              int ti) {
+  using M = Mode<MODE>;
+  SmemCtl& ctl = *R.ctl;
+  const int lane = R.lane;
+  const int q = (ew + 2) & 3;  // TMEM lane quarter (hardware rule: warp id % 4)
+  const int hf = ew >> 2;
+  const int r = q * 32 + lane;
+  uint4* stage = reinterpret_cast<uint4*>(R.smem + KSTAGES * M::kStageBytes + AUXB) + ew * 128;
+  const bool tr = lane == 0 && (ew == 0 || ew == 4);
+  const int c0 = hf * (M::kBN / 64);  // first 32-column chunk of this warp's half
+  if (M::kRagK) {
+    const int Md = M::wg_mdim(p), Nd = M::wg_ndim(p);
+    bf16* outp = (MODE == GEMM_WGRAD_W1 ? p.out0 : p.out1) + (size_t)t.e * Md * Nd;
+    const int slab_rows = min(32, Md - (t.m0 + q * 32));
+    bf16* slab = outp + (size_t)(t.m0 + q * 32) * Nd;
+    if (t.nk == 0) {
+      // an expert with no rows: zero weight gradient (plain stores, after
+      // the last TMA store has finished reading the staging buffer)
+      float z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0.f;
+      if (lane == 0) ptx::bulk_wait_group_read0();
+      __syncwarp();
+      for (int cc = c0; cc < c0 + BN / 64; ++cc)
+        warp_store32(stage, z, slab + t.n0 + 32 * cc, Nd, lane, slab_rows, t.n0 + 32 * cc < Nd);
+      return true;
+    }
+    if (!ptx::mbar_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
+      if (lane == 0) flag_timeout(ctl, p.status, 5);
+      return false;
+    }
+    ptx::tc_fence_after();
+    if (tr) trace(p, MODE, ew == 0 ? 4 : 6, ti);
+    const uint32_t tbase = R.tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
+    store_chunks(stage, tbase, c0, slab + t.n0, Nd, t.n0, lane, slab_rows, tmD, M::kStoreDims,
+                 t.n0, t.m0 + q * 32, t.e);
+  } else {
+    if (!ptx::mbar_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
+      if (lane == 0) flag_timeout(ctl, p.status, 5);
+      return false;
+    }
+    ptx::tc_fence_after();
+    if (tr) trace(p, MODE, ew == 0 ? 4 : 6, ti);
+    const uint32_t tbase = R.tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
+    // this warp's 32-row slab of the tile, for the coalesced stores
+    const size_t slab_row0 = (size_t)t.row0 + t.m0 + q * 32;
+    const int slab_rows = min(32, t.rows - q * 32);
+    if (MODE == GEMM_FC1_FWD) {
+      // columns 0..127: gate f0.., columns 128..255: up f0..; this half: 2 chunks
+      for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
+        uint32_t g[32], u[32];
+        ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, g);
+        ptx::tmem_ld_32x32b_x32(tbase + 128 + 32 * cc, u);
+        ptx::tmem_ld_wait(g, u);
+        const int f = t.n0 + 32 * cc;
+        const bool cols_ok = f < p.F;
+        // round gate/up to bf16 in place, then h from the rounded values
+        float* ag = reinterpret_cast<float*>(g);
+        float* au = reinterpret_cast<float*>(u);
+        float hv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          ag[i] = round_bf16(ag[i]);
+          au[i] = round_bf16(au[i]);
+          hv[i] = ag[i] * fast_sigmoid(ag[i]) * au[i];
+        }
+        bf16* abase = p.out0 + slab_row0 * (size_t)(2 * p.F);
+        warp_store32(stage, ag, abase + f, 2 * p.F, lane, slab_rows, cols_ok);
+        warp_store32(stage, au, abase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
+        warp_store32(stage, hv, p.out1 + slab_row0 * (size_t)p.F + f, p.F, lane, slab_rows,
+                     cols_ok);
+      }
+    } else if (MODE == GEMM_FC2_DGRAD) {
+      // the pre-activation slab arrives one 64-column quarter at a time: a
+      // gate box and an up box of 128 rows x 64 columns, 128-byte swizzled
+      // (16-byte chunk j of row r sits at chunk j ^ (r & 7)). A quarter is
+      // 2 chunks of 32 columns; each warp takes one.
+      const uint8_t* aux = R.smem + KSTAGES * M::kStageBytes;
+      bf16* dbase = p.out0 + slab_row0 * (size_t)(2 * p.F);
+      for (int qt = 0; qt < M::kBN / 64; ++qt) {
+        if (!ptx::mbar_wait(&ctl.aux_full, aux_phase, &ctl.abort, kWaitLimitNs)) {
+          if (lane == 0) flag_timeout(ctl, p.status, 6);
+          return false;
+        }
+        aux_phase ^= 1;
+        const int cc = 2 * qt + hf;  // chunk within the tile
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
+        const int cb = hf * 4;
+        uint4 gc[4], uc[4];
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const int off = r * 128 + (((cb + k2) ^ (r & 7)) * 16);
+          gc[k2] = *reinterpret_cast<const uint4*>(aux + off);
+          uc[k2] = *reinterpret_cast<const uint4*>(aux + 16384 + off);
+        }
+        ptx::tmem_ld_wait(v);
+        const int f = t.n0 + 32 * cc;
+        const bool cols_ok = f < p.F;
+        float out[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {  // da_up = dh * silu(a_g)
+          const float ag = bf16_at(gc, i);
+          out[i] = __uint_as_float(v[i]) * ag * fast_sigmoid(ag);
+        }
+        ptx::mbar_arrive(&ctl.aux_empty);  // the quarter is in registers now
+        warp_store32(stage, out, dbase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {  // da_gate = dh * a_u * silu'(a_g)
+          const float ag = bf16_at(gc, i);
+          const float sg = fast_sigmoid(ag);
+          out[i] = __uint_as_float(v[i]) * bf16_at(uc, i) * sg * (1.f + ag * (1.f - sg));
+        }
+        warp_store32(stage, out, dbase + f, 2 * p.F, lane, slab_rows, cols_ok);
+      }
+    } else {
+      const int Nd = MODE == GEMM_FC2_FWD || MODE == GEMM_FC1_DGRAD ? p.H : p.F;
+      store_chunks(stage, tbase, c0, p.out0 + slab_row0 * (size_t)Nd + t.n0, Nd, t.n0, lane,
+                   slab_rows, tmD, M::kStoreDims, t.n0, (int)slab_row0, 0);
+    }
+  }
+  if (tr) trace(p, MODE, ew == 0 ? 5 : 7, ti);
+  if (SIGNAL) {
+    // this warp's stores of the tile are done: make them visible device-wide
+    // before the expert's counter moves
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(p.dep + t.e, 1);
+    }
+  }
+  // one arrival per epilogue warp once all its lanes' TMEM reads are done
+  // (in the odd CTA of a pair, on the local barrier its MMA warp forwards)
+  ptx::tc_fence_before();
+  __syncwarp();
+  if (lane == 0)
+    ptx::mbar_arrive(M::kPair && R.crank != 0 ? &ctl.epi_done[acc] : &ctl.tmem_empty[acc]);
+  if (++acc == 2) {
+    acc = 0;
+    acc_phase ^= 1;
+  }
+  return true;
+}
+
+template <int MODE, int MODE2>
+__global__ void __launch_bounds__(Fuse<MODE, MODE2>::kWarps * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
-                        const __grid_constant__ CUtensorMap tmD, const KParams p) {
-  using M = Mode<MODE>;
+                        const __grid_constant__ CUtensorMap tmD,
+                        const __grid_constant__ CUtensorMap tmA2,
+                        const __grid_constant__ CUtensorMap tmB2,
+                        const __grid_constant__ CUtensorMap tmC2,
+                        const __grid_constant__ CUtensorMap tmD2, const KParams p,
+                        const KParams p2) {
+  using F = Fuse<MODE, MODE2>;
+  constexpr int MODE_B = MODE2 >= 0 ? MODE2 : MODE;
+  constexpr int KS = F::kStages;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ SmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -322,19 +766,19 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
   const int E = p.E;
 
   // ---- per-CTA setup: barriers, TMEM, then (once the previous kernel on the
-  // stream has completed) offsets and the tile prefix
+  // stream has completed) offsets and the tile prefixes
   if (threadIdx.x == 0) {
-    for (int s = 0; s < M::kStages; ++s) {
+    for (int s = 0; s < KS; ++s) {
       ptx::mbar_init(&ctl.full[s], 1);
       // multicast B: every CTA of the cluster releases the stage; pair: the
       // even CTA's MMA releases it in both CTAs
-      ptx::mbar_init(&ctl.empty[s], M::kPair ? 1 : M::kCS);
+      ptx::mbar_init(&ctl.empty[s], F::kPair ? 1 : F::kCS);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl.tmem_full[b], 1);
       // one arrival per epilogue warp; pair: the even CTA's MMA also waits
       // for the odd CTA's epilogue, reported by one forwarded arrival
-      ptx::mbar_init(&ctl.tmem_empty[b], M::kPair ? 9 : 8);
+      ptx::mbar_init(&ctl.tmem_empty[b], F::kPair ? 9 : 8);
       ptx::mbar_init(&ctl.epi_done[b], 8);
     }
     ptx::mbar_init(&ctl.tail, 1);
@@ -344,7 +788,7 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
     ctl.abort = 0;
     ptx::fence_mbar_init();
   }
-  if (M::kPair) {
+  if (F::kPair) {
     // the pair's TMEM is allocated collectively; barriers must be live in both
     __syncthreads();
     ptx::cluster_sync();
@@ -359,236 +803,99 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    if (F::kHas2) {
+      ptx::tma_prefetch_desc(&tmA2);
+      ptx::tma_prefetch_desc(&tmB2);
+    }
   }
   pdl_wait();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) ctl.off[e] = p.off[e];
   __syncthreads();
   if (warp == 0) {
-    // tiles per expert -> exclusive prefix
-    int carry = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      int n = 0;
-      if (e < E) {
-        const int cnt = ctl.off[e + 1] - ctl.off[e];
-        if (M::kRagK)
-          n = (((M::wg_mdim(p) + BM - 1) / BM + M::kCS - 1) / M::kCS) * M::ntiles(p);
-        else n = (((cnt + BM - 1) / BM + M::kCS - 1) / M::kCS) * M::ntiles(p);
-        if (cnt < 0) n = 0;
-      }
-      int incl = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (e < E) ctl.tstart[e] = carry + incl - n;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) ctl.tstart[E] = carry;
+    tile_prefix<MODE>(p, ctl.off, ctl.tstart, lane);
+    if (F::kHas2) tile_prefix<MODE_B>(p2, ctl.off, ctl.tstart2, lane);
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   // peers multicast into this CTA's shared memory and barriers: all must be
   // initialised first
-  if (M::kCS > 1 && !M::kPair) ptx::cluster_sync();
-  const int total = ctl.tstart[E];
-  const uint32_t tmem_base = ctl.tmem_base;
-  const uint32_t crank = M::kCS > 1 ? ptx::cluster_ctarank() : 0;
-  const int first = M::kCS > 1 ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
-  const int stride = M::kCS > 1 ? (int)ptx::cluster_count_x() : (int)gridDim.x;
-  const uint16_t cmask = (uint16_t)((1u << M::kCS) - 1u);
+  if (F::kCS > 1 && !F::kPair) ptx::cluster_sync();
+  const int total1 = ctl.tstart[E];
+  const int total = total1 + (F::kHas2 ? ctl.tstart2[E] : 0);
+  Role R;
+  R.smem = smem;
+  R.ctl = &ctl;
+  R.tmem_base = ctl.tmem_base;
+  R.crank = F::kCS > 1 ? ptx::cluster_ctarank() : 0;
+  R.cmask = (uint16_t)((1u << F::kCS) - 1u);
+  R.lane = lane;
+  const int first = F::kCS > 1 ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
+  const int stride = F::kCS > 1 ? (int)ptx::cluster_count_x() : (int)gridDim.x;
+  // tile index -> (mode, tile); cursors walk the expert prefixes
+  int cur1 = 0, cur2 = 0;
+  auto tile1 = [&](int tile) { return tile_at<MODE>(p, ctl.tstart, ctl.off, tile, cur1, R.crank); };
+  auto tile2 = [&](int tile) {
+    return tile_at<MODE_B>(p2, ctl.tstart2, ctl.off, tile - total1, cur2, R.crank);
+  };
 
   if (warp == 0) {
     // ================================================================ producer
-    int stage = 0, cursor = 0;
+    int stage = 0;
     uint32_t phase = 0, tail_phase = 0;
-    bool ok = true;
     int ti = 0;
-    for (int tile = first; tile < total && ok; tile += stride, ++ti) {
-      const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
-      if (lane == 0) trace(p, MODE, 0, ti);
-      for (int kt = 0; kt < t.nk; ++kt) {
-        if (!ptx::mbar_wait(&ctl.empty[stage], phase ^ 1, &ctl.abort, kWaitLimitNs)) {
-          if (lane == 0) flag_timeout(ctl, p.status, 1);
-          ok = false;
-          break;
-        }
-        uint8_t* sA = smem + stage * M::kStageBytes;
-        uint8_t* sB = sA + kABytes;
-        const int k0 = kt * BK;
-        const bool tail = M::kRagK && (t.rows - k0 < BK);
-        uint64_t* bar = tail ? &ctl.tail : &ctl.full[stage];
+    for (int tile = first; tile < total; tile += stride, ++ti) {
+      bool ok;
+      if (!F::kHas2 || tile < total1) {
+        const Tile t = tile1(tile);
+        if (lane == 0) trace(p, MODE, 0, ti);
+        ok = producer_tile<MODE, KS>(R, p, &tmA, &tmB, t, stage, phase, tail_phase);
+      } else {
+        const Tile t = tile2(tile);
+        // the A operand of this tile is the first mode's output for expert t.e
         if (lane == 0) {
-          if (M::kRagK) {
-            // A: this CTA's own M block. B: slice i of the shared tile is loaded
-            // by cluster rank i % kCS and multicast to every CTA of the cluster,
-            // so full[stage] collects all 32 KB of B in every CTA. On the tail
-            // stage A goes to the tail barrier and full[stage] gets its arrival
-            // only after the zeroing below.
-            if (tail) {
-              ptx::mbar_arrive_expect_tx(&ctl.tail, kABytes);
-              ptx::mbar_expect_tx(&ctl.full[stage], M::kBBytes);
-            } else {
-              ptx::mbar_arrive_expect_tx(&ctl.full[stage], M::kStageBytes);
-            }
-            const int r = t.row0 + k0;
-            ptx::tma_load_2d(sA, &tmA, bar, t.m0, r);
-            ptx::tma_load_2d(sA + 8192, &tmA, bar, t.m0 + 64, r);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (M::kCS == 1)
-                ptx::tma_load_2d(sB + 8192 * i, &tmB, &ctl.full[stage], t.n0 + 64 * i, r);
-              else if (i % M::kCS == (int)crank)
-                ptx::tma_load_2d_multicast(sB + 8192 * i, &tmB, &ctl.full[stage], t.n0 + 64 * i,
-                                           r, cmask);
-            }
-          } else if (M::kPair) {
-            // both CTAs' loads complete on the even CTA's full[stage]
-            const uint32_t fb = ptx::mapa_shared(&ctl.full[stage], 0);
-            if (crank == 0) ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * M::kStageBytes);
-            ptx::tma_load_2d_pair(sA, &tmA, fb, k0, t.row0 + t.m0);
-            if (MODE == GEMM_FC1_FWD) {  // even CTA: 128 gate rows, odd CTA: 128 up rows
-              ptx::tma_load_2d_pair(sB, &tmB, fb, k0, t.e * 2 * p.F + (crank ? p.F : 0) + t.n0);
-            } else if (MODE == GEMM_FC2_FWD) {
-              ptx::tma_load_2d_pair(sB, &tmB, fb, k0, t.e * p.H + t.n0 + 128 * crank);
-            } else {  // MN-major B: this CTA's half of the N columns
-              const int base = MODE == GEMM_FC2_DGRAD ? t.e * p.H : t.e * 2 * p.F;
-              constexpr int nb = M::kBN / 128;  // 64-wide boxes per CTA
-#pragma unroll
-              for (int i = 0; i < nb; ++i)
-                ptx::tma_load_2d_pair(sB + 8192 * i, &tmB, fb, t.n0 + 64 * (crank * nb + i),
-                                      base + k0);
-            }
-          } else {
-            ptx::mbar_arrive_expect_tx(bar, M::kStageBytes);
-            ptx::tma_load_2d(sA, &tmA, bar, k0, t.row0 + t.m0);
-            // B boxes: box i is loaded by cluster rank i % kCS and multicast
-            auto load_b = [&](int i, void* dst, int c0, int c1) {
-              if (M::kCS == 1)
-                ptx::tma_load_2d(dst, &tmB, bar, c0, c1);
-              else if (i % M::kCS == (int)crank)
-                ptx::tma_load_2d_multicast(dst, &tmB, bar, c0, c1, cmask);
-            };
-            if (MODE == GEMM_FC1_FWD) {
-              const int base = t.e * 2 * p.F;
-              load_b(0, sB, k0, base + t.n0);                 // 128 gate rows
-              load_b(1, sB + 16384, k0, base + p.F + t.n0);   // 128 up rows
-            } else if (MODE == GEMM_FC2_FWD) {
-              load_b(0, sB, k0, t.e * p.H + t.n0);
-              load_b(1, sB + 16384, k0, t.e * p.H + t.n0 + 128);
-            } else {
-              const int base = MODE == GEMM_FC2_DGRAD ? t.e * p.H : t.e * 2 * p.F;
-#pragma unroll
-              for (int i = 0; i < M::kBN / 64; ++i) load_b(i, sB + 8192 * i, t.n0 + 64 * i, base + k0);
-            }
-          }
+          const int target = 8 * F::kCS * (ctl.tstart[t.e + 1] - ctl.tstart[t.e]);
+          ok = wait_expert(p, t.e, target, &ctl.abort);
+          if (!ok) flag_timeout(ctl, p.status, 10);
         }
-        if (tail) {
-          // last K stage of a wgrad tile: zero the A rows past the expert's end
-          if (!ptx::mbar_wait(&ctl.tail, tail_phase, &ctl.abort, kWaitLimitNs)) {
-            if (lane == 0) flag_timeout(ctl, p.status, 2);
-            ok = false;
-            break;
-          }
-          tail_phase ^= 1;
-          const int valid = t.rows - k0;  // 1..63
-          const int nzero = (BK - valid) * 8;  // 16-byte chunks per atom
-          for (int i = lane; i < 2 * nzero; i += 32) {
-            const int atom = i / nzero, j = i % nzero;
-            uint4* dst = reinterpret_cast<uint4*>(sA + atom * 8192 + valid * 128) + j;
-            *dst = make_uint4(0, 0, 0, 0);
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&ctl.full[stage]);
-        }
-        if (++stage == M::kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) ok = producer_tile<MODE_B, KS>(R, p2, &tmA2, &tmB2, t, stage, phase, tail_phase);
       }
       if (lane == 0) trace(p, MODE, 1, ti);
+      if (!ok) break;
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     // (pair mode: only the even CTA issues, for both CTAs)
-    if (lane == 0 && !(M::kPair && crank != 0)) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(M::kPair ? 2 * BM : BM, M::kBN, M::kAMn, M::kBMn);
-      const uint32_t a_lbo = M::kAMn ? 8192 : 16, b_lbo = M::kBMn ? 8192 : 16;
-      const uint32_t a_adv = M::kAMn ? (2048 >> 4) : (32 >> 4);
-      const uint32_t b_adv = M::kBMn ? (2048 >> 4) : (32 >> 4);
-      int stage = 0, cursor = 0, acc = 0;
+    if (lane == 0 && !(F::kPair && R.crank != 0)) {
+      int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
       int ti = -1;
-      for (int tile = first; tile < total && ok; tile += stride) {
-        const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
+      for (int tile = first; tile < total; tile += stride) {
         ++ti;
-        if (t.nk == 0) continue;
-        if (!ptx::mbar_wait(&ctl.tmem_empty[acc], acc_phase ^ 1, &ctl.abort, kWaitLimitNs)) {
-          flag_timeout(ctl, p.status, 3);
-          break;
-        }
-        ptx::tc_fence_after();
-        trace(p, MODE, 2, ti);
-        const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        for (int kt = 0; kt < t.nk; ++kt) {
-          if (!ptx::mbar_wait(&ctl.full[stage], phase, &ctl.abort, kWaitLimitNs)) {
-            flag_timeout(ctl, p.status, 4);
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t a_addr = ptx::smem_u32(smem + stage * M::kStageBytes);
-          const uint32_t b_addr = a_addr + kABytes;
-          const uint64_t adesc = ptx::sdesc_sw128(a_addr, a_lbo, 1024);
-          const uint64_t bdesc = ptx::sdesc_sw128(b_addr, b_lbo, 1024);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            if (M::kPair)
-              ptx::umma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * a_adv),
-                                  bdesc + (uint64_t)(kk * b_adv), idesc, (kt | kk) != 0);
-            else
-              ptx::umma_bf16(d_tmem, adesc + (uint64_t)(kk * a_adv), bdesc + (uint64_t)(kk * b_adv),
-                             idesc, (kt | kk) != 0);
-          }
-          // the stage is free once every CTA whose shared memory the MMAs read
-          // (pair) or that received the multicast B slices has consumed it
-          if (M::kPair) ptx::umma_commit_pair(&ctl.empty[stage], 3);
-          else if (M::kCS > 1) ptx::umma_commit_multicast(&ctl.empty[stage], cmask);
-          else ptx::umma_commit(&ctl.empty[stage]);
-          if (++stage == M::kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
+        bool ok;
+        if (!F::kHas2 || tile < total1)
+          ok = mma_tile<MODE, KS>(R, p, tile1(tile), stage, phase, acc, acc_phase, ti);
+        else
+          ok = mma_tile<MODE_B, KS>(R, p2, tile2(tile), stage, phase, acc, acc_phase, ti);
         if (!ok) break;
-        trace(p, MODE, 3, ti);
-        if (M::kPair) ptx::umma_commit_pair(&ctl.tmem_full[acc], 3);
-        else ptx::umma_commit(&ctl.tmem_full[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1;
-        }
       }
       // make sure no MMA is still running before TMEM is released
-      if (M::kPair) ptx::umma_commit_pair(&ctl.drain, 1);
+      if (F::kPair) ptx::umma_commit_pair(&ctl.drain, 1);
       else ptx::umma_commit(&ctl.drain);
       if (!ptx::mbar_wait(&ctl.drain, 0, &ctl.abort, kWaitLimitNs)) {
         // abort already flagged: wait once more with the abort flag ignored
         int dummy = 0;
         ptx::mbar_wait(&ctl.drain, 0, &dummy, kWaitLimitNs);
       }
-    } else if (lane == 0 && M::kPair) {
+    } else if (lane == 0 && F::kPair) {
       // odd CTA of a pair: forward "accumulator free" to the even CTA's MMA
       // issuer, one cluster arrival per tile once all 8 epilogue warps have
       // arrived locally (fewer cluster-scope arrivals than one per warp).
-      int cursor = 0, acc = 0;
+      int acc = 0;
       uint32_t acc_phase = 0;
       for (int tile = first; tile < total; tile += stride) {
-        const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
+        const Tile t = (!F::kHas2 || tile < total1) ? tile1(tile) : tile2(tile);
         if (t.nk == 0) continue;
         if (!ptx::mbar_wait(&ctl.epi_done[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
           flag_timeout(ctl, p.status, 9);
@@ -602,182 +909,45 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
       }
     }
     __syncwarp();
-  } else if (M::kAux && warp == 10) {
+  } else if (F::kAux && warp == 10) {
     // ================================================================ aux loader
-    // Loads each tile's saved pre-activation, a 64-column quarter at a time,
-    // each once the epilogue has released the previous quarter.
     if (lane == 0) {
-      ptx::tma_prefetch_desc(&tmC);
-      int cursor = 0;
+      ptx::tma_prefetch_desc(Mode<MODE>::kAux ? &tmC : &tmC2);
       uint32_t ph = 0;
       for (int tile = first; tile < total; tile += stride) {
-        const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
-        if (!ptx::mbar_wait(&ctl.aux_empty, ph ^ 1, &ctl.abort, kWaitLimitNs)) {
-          flag_timeout(ctl, p.status, 7);
-          break;
+        bool ok = true;
+        if (!F::kHas2 || tile < total1) {
+          const Tile t = tile1(tile);
+          if (Mode<MODE>::kAux) ok = aux_tile<MODE, KS>(R, p, &tmC, t, ph);
+        } else {
+          const Tile t = tile2(tile);
+          if (Mode<MODE_B>::kAux) ok = aux_tile<MODE_B, KS>(R, p2, &tmC2, t, ph);
         }
-        ph ^= 1;
-        uint8_t* aux = smem + M::kStages * M::kStageBytes;
-        const int row = t.row0 + t.m0;
-        for (int qt = 0; qt < M::kBN / 64; ++qt) {
-          if (qt > 0 && !ptx::mbar_wait(&ctl.aux_empty, ph ^ 1, &ctl.abort, kWaitLimitNs)) {
-            flag_timeout(ctl, p.status, 7);
-            break;
-          }
-          if (qt > 0) ph ^= 1;
-          const int c = t.n0 + 64 * qt;
-          ptx::mbar_arrive_expect_tx(&ctl.aux_full, M::kAuxBytes);
-          ptx::tma_load_2d(aux, &tmC, &ctl.aux_full, c, row);                  // gate
-          ptx::tma_load_2d(aux + 16384, &tmC, &ctl.aux_full, p.F + c, row);    // up
-        }
+        if (!ok) break;
       }
     }
     __syncwarp();
   } else {
     // ================================================================ epilogue
     // 8 warps: warp w reads TMEM lane quarter w % 4 (hardware rule) and owns
-    // half hf of the tile's columns.
+    // half of the tile's columns.
     const int ew = warp - 2;
-    const int q = warp & 3;
-    const int hf = ew >> 2;
-    const int r = q * 32 + lane;
-    uint4* stage = reinterpret_cast<uint4*>(smem + M::kStages * M::kStageBytes + M::kAuxBytes) + ew * 128;
-    int cursor = 0, acc = 0;
+    int acc = 0;
     uint32_t acc_phase = 0, aux_phase = 0;
     int ti = -1;
     for (int tile = first; tile < total; tile += stride) {
-      const Tile t = tile_at<MODE>(p, ctl, tile, cursor, crank);
       ++ti;
-      const bool tr = lane == 0 && (ew == 0 || ew == 4);
-      const int c0 = hf * (M::kBN / 64);  // first 32-column chunk of this warp's half
-      if (M::kRagK) {
-        const int Md = M::wg_mdim(p), Nd = M::wg_ndim(p);
-        bf16* outp = (MODE == GEMM_WGRAD_W1 ? p.out0 : p.out1) + (size_t)t.e * Md * Nd;
-        const int slab_rows = min(32, Md - (t.m0 + q * 32));
-        bf16* slab = outp + (size_t)(t.m0 + q * 32) * Nd;
-        if (t.nk == 0) {
-          // an expert with no rows: zero weight gradient (plain stores, after
-          // the last TMA store has finished reading the staging buffer)
-          float z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0.f;
-          if (lane == 0) ptx::bulk_wait_group_read0();
-          __syncwarp();
-          for (int cc = c0; cc < c0 + BN / 64; ++cc)
-            warp_store32(stage, z, slab + t.n0 + 32 * cc, Nd, lane, slab_rows, t.n0 + 32 * cc < Nd);
-          continue;
-        }
-        if (!ptx::mbar_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
-          if (lane == 0) flag_timeout(ctl, p.status, 5);
-          break;
-        }
-        ptx::tc_fence_after();
-        if (tr) trace(p, MODE, ew == 0 ? 4 : 6, ti);
-        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-        store_chunks(stage, tbase, c0, slab + t.n0, Nd, t.n0, lane, slab_rows, &tmD, M::kStoreDims,
-                     t.n0, t.m0 + q * 32, t.e);
-      } else {
-        if (!ptx::mbar_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
-          if (lane == 0) flag_timeout(ctl, p.status, 5);
-          break;
-        }
-        ptx::tc_fence_after();
-        if (tr) trace(p, MODE, ew == 0 ? 4 : 6, ti);
-        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-        // this warp's 32-row slab of the tile, for the coalesced stores
-        const size_t slab_row0 = (size_t)t.row0 + t.m0 + q * 32;
-        const int slab_rows = min(32, t.rows - q * 32);
-        if (MODE == GEMM_FC1_FWD) {
-          // columns 0..127: gate f0.., columns 128..255: up f0..; this half: 2 chunks
-          for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
-            uint32_t g[32], u[32];
-            ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, g);
-            ptx::tmem_ld_32x32b_x32(tbase + 128 + 32 * cc, u);
-            ptx::tmem_ld_wait(g, u);
-            const int f = t.n0 + 32 * cc;
-            const bool cols_ok = f < p.F;
-            // round gate/up to bf16 in place, then h from the rounded values
-            float* ag = reinterpret_cast<float*>(g);
-            float* au = reinterpret_cast<float*>(u);
-            float hv[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              ag[i] = round_bf16(ag[i]);
-              au[i] = round_bf16(au[i]);
-              hv[i] = ag[i] * fast_sigmoid(ag[i]) * au[i];
-            }
-            bf16* abase = p.out0 + slab_row0 * (size_t)(2 * p.F);
-            warp_store32(stage, ag, abase + f, 2 * p.F, lane, slab_rows, cols_ok);
-            warp_store32(stage, au, abase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
-            warp_store32(stage, hv, p.out1 + slab_row0 * (size_t)p.F + f, p.F, lane, slab_rows,
-                         cols_ok);
-          }
-        } else if (MODE == GEMM_FC2_DGRAD) {
-          // the pre-activation slab arrives one 64-column quarter at a time: a
-          // gate box and an up box of 128 rows x 64 columns, 128-byte swizzled
-          // (16-byte chunk j of row r sits at chunk j ^ (r & 7)). A quarter is
-          // 2 chunks of 32 columns; each warp takes one.
-          const uint8_t* aux = smem + M::kStages * M::kStageBytes;
-          bf16* dbase = p.out0 + slab_row0 * (size_t)(2 * p.F);
-          bool ok_aux = true;
-          for (int qt = 0; qt < M::kBN / 64 && ok_aux; ++qt) {
-            if (!ptx::mbar_wait(&ctl.aux_full, aux_phase, &ctl.abort, kWaitLimitNs)) {
-              if (lane == 0) flag_timeout(ctl, p.status, 6);
-              ok_aux = false;
-              break;
-            }
-            aux_phase ^= 1;
-            const int cc = 2 * qt + hf;  // chunk within the tile
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tbase + 32 * cc, v);
-            const int cb = hf * 4;
-            uint4 gc[4], uc[4];
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-              const int off = r * 128 + (((cb + k2) ^ (r & 7)) * 16);
-              gc[k2] = *reinterpret_cast<const uint4*>(aux + off);
-              uc[k2] = *reinterpret_cast<const uint4*>(aux + 16384 + off);
-            }
-            ptx::tmem_ld_wait(v);
-            const int f = t.n0 + 32 * cc;
-            const bool cols_ok = f < p.F;
-            float out[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {  // da_up = dh * silu(a_g)
-              const float ag = bf16_at(gc, i);
-              out[i] = __uint_as_float(v[i]) * ag * fast_sigmoid(ag);
-            }
-            ptx::mbar_arrive(&ctl.aux_empty);  // the quarter is in registers now
-            warp_store32(stage, out, dbase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {  // da_gate = dh * a_u * silu'(a_g)
-              const float ag = bf16_at(gc, i);
-              const float sg = fast_sigmoid(ag);
-              out[i] = __uint_as_float(v[i]) * bf16_at(uc, i) * sg * (1.f + ag * (1.f - sg));
-            }
-            warp_store32(stage, out, dbase + f, 2 * p.F, lane, slab_rows, cols_ok);
-          }
-          if (!ok_aux) break;
-        } else {
-          const int Nd = MODE == GEMM_FC2_FWD || MODE == GEMM_FC1_DGRAD ? p.H : p.F;
-          store_chunks(stage, tbase, c0, p.out0 + slab_row0 * (size_t)Nd + t.n0, Nd, t.n0, lane,
-                       slab_rows, &tmD, M::kStoreDims, t.n0, (int)slab_row0, 0);
-        }
-      }
-      if (tr) trace(p, MODE, ew == 0 ? 5 : 7, ti);
-      // one arrival per epilogue warp once all its lanes' TMEM reads are done
-      // (in the odd CTA of a pair, on the local barrier its MMA warp forwards)
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0)
-        ptx::mbar_arrive(M::kPair && crank != 0 ? &ctl.epi_done[acc] : &ctl.tmem_empty[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
-      }
+      bool ok;
+      if (!F::kHas2 || tile < total1)
+        ok = epilogue_tile<MODE, KS, F::kAuxBytes, F::kHas2>(R, p, &tmD, tile1(tile), acc,
+                                                               acc_phase, aux_phase, ew, ti);
+      else
+        ok = epilogue_tile<MODE_B, KS, F::kAuxBytes, false>(R, p2, &tmD2, tile2(tile), acc,
+                                                             acc_phase, aux_phase, ew, ti);
+      if (!ok) break;
     }
     // the staging buffers and the outputs must outlive the TMA stores
-    if (M::kStoreDims && lane == 0) ptx::bulk_wait_group0();
+    if (F::kStores && lane == 0) ptx::bulk_wait_group0();
     __syncwarp();
   }
 
@@ -785,10 +955,10 @@ __global__ void __launch_bounds__(Mode<MODE>::kWarps * 32, 1)
   __syncthreads();
   ptx::tc_fence_after();
   // peers may still arrive on this CTA's barriers until they are done
-  if (M::kCS > 1) ptx::cluster_sync();
+  if (F::kCS > 1) ptx::cluster_sync();
   if (warp == 1) {
-    if (M::kPair) ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
-    else ptx::tmem_dealloc(tmem_base, kTmemCols);
+    if (F::kPair) ptx::tmem_dealloc_pair(R.tmem_base, kTmemCols);
+    else ptx::tmem_dealloc(R.tmem_base, kTmemCols);
   }
 }
 
@@ -858,18 +1028,17 @@ bool make_store_map(CUtensorMap* m, void* base, long long experts, long long row
   return true;
 }
 
-template <int MODE>
-moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                         const CUtensorMap& dmap, const KParams& p, int grid,
-                         cudaStream_t st) {
-  constexpr int cs = Mode<MODE>::kCS;
+template <int MODE, int MODE2>
+moe_status_t launch_mode(const CUtensorMap (&m1)[4], const CUtensorMap (&m2)[4], const KParams& p,
+                         const KParams& p2, int grid, int kernel_id, cudaStream_t st) {
+  using F = Fuse<MODE, MODE2>;
+  constexpr int cs = F::kCS;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)Mode<MODE>::kDynSmem);
+    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, MODE2>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)F::kDynSmem);
     if (attr_err == cudaSuccess && cs > 1) {
       // how many clusters of cs CTAs (one per SM) can be resident at once
       cudaLaunchConfig_t cfg = {};
@@ -879,23 +1048,26 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUten
       at[0].val.clusterDim.y = 1;
       at[0].val.clusterDim.z = 1;
       cfg.gridDim = dim3(device_sm_count() / cs * cs);
-      cfg.blockDim = dim3(Mode<MODE>::kWarps * 32);
-      cfg.dynamicSmemBytes = Mode<MODE>::kDynSmem;
+      cfg.blockDim = dim3(F::kWarps * 32);
+      cfg.dynamicSmemBytes = F::kDynSmem;
       cfg.attrs = at;
       cfg.numAttrs = 1;
-      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_kernel<MODE>, &cfg);
+      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_kernel<MODE, MODE2>,
+                                                &cfg);
     }
   });
   if (attr_err != cudaSuccess) {
     set_error("kernel attribute setup failed: %s", cudaGetErrorString(attr_err));
     return MOE_ERR_CUDA;
   }
-  LaunchScope _ls(K_GEMM_FC1_FWD + MODE, st);
+  LaunchScope _ls(kernel_id, st);
   if (cs == 1) {
-    launch_k(grouped_gemm_kernel<MODE>, grid, Mode<MODE>::kWarps * 32, Mode<MODE>::kDynSmem, st, a,
-             b, c, dmap, p);
+    launch_k(grouped_gemm_kernel<MODE, MODE2>, grid, F::kWarps * 32, F::kDynSmem, st, m1[0],
+             m1[1], m1[2], m1[3], m2[0], m2[1], m2[2], m2[3], p, p2);
     return check_launch("grouped_gemm_kernel");
   }
+  // a fused launch relies on every CTA being resident at once (second-mode
+  // tiles wait on first-mode tiles of other CTAs): never more clusters than fit
   int clusters = (grid + cs - 1) / cs;
   if (max_clusters > 0 && clusters > max_clusters) clusters = max_clusters;
   if (clusters < 1) clusters = 1;
@@ -908,17 +1080,87 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUten
   at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[1].val.programmaticStreamSerializationAllowed = MOE_PDL;
   cfg.gridDim = dim3(clusters * cs);
-  cfg.blockDim = dim3(Mode<MODE>::kWarps * 32);
-  cfg.dynamicSmemBytes = Mode<MODE>::kDynSmem;
+  cfg.blockDim = dim3(F::kWarps * 32);
+  cfg.dynamicSmemBytes = F::kDynSmem;
   cfg.stream = st;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, b, c, dmap, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, MODE2>, m1[0], m1[1], m1[2],
+                                     m1[3], m2[0], m2[1], m2[2], m2[3], p, p2);
   if (e != cudaSuccess) {
     set_error("grouped_gemm_kernel cluster launch: %s", cudaGetErrorString(e));
     return MOE_ERR_CUDA;
   }
   return check_launch("grouped_gemm_kernel");
+}
+
+// Tensor maps (A, B, aux, store), kernel parameters and an upper bound on the
+// tiles of one mode.
+bool mode_setup(const moe_layer_desc_t& d, const GemmArgs& g, CUtensorMap (&m)[4], KParams& p,
+                long long& ntile_bound) {
+  const long long N = (long long)d.T * d.k;
+  const int E = d.E, H = d.H, F = d.F;
+  bool ok = true;
+  switch (g.mode) {
+    case GEMM_FC1_FWD:
+      ok = make_map(&m[0], g.A, N, H, 128) && make_map(&m[1], g.B, (long long)E * 2 * F, H, 128);
+      ntile_bound = (N / BM + 2 * E) * ((F + 127) / 128);
+      break;
+    case GEMM_FC2_FWD:
+      ok = make_map(&m[0], g.A, N, F, 128) && make_map(&m[1], g.B, (long long)E * H, F, 128);
+      ntile_bound = (N / BM + 2 * E) * ((H + BN - 1) / BN);
+      break;
+    case GEMM_FC2_DGRAD:
+      ok = make_map(&m[0], g.A, N, H, 128) && make_map(&m[1], g.B, (long long)E * H, F, 64) &&
+           make_map(&m[2], g.aux, N, 2 * F, 128);
+      ntile_bound = (N / BM + 2 * E) * ((F + 127) / 128);
+      break;
+    case GEMM_FC1_DGRAD:
+      ok = make_map(&m[0], g.A, N, 2 * F, 128) && make_map(&m[1], g.B, (long long)E * 2 * F, H, 64);
+      ntile_bound = (N / BM + 2 * E) * ((H + BN - 1) / BN);
+      break;
+    case GEMM_WGRAD_W1:
+      ok = make_map(&m[0], g.A, N, 2 * F, 64) && make_map(&m[1], g.B, N, H, 64);
+      ntile_bound = (long long)E * ceil_div(ceil_div(2 * F, BM), Mode<GEMM_WGRAD_W1>::kCS) *
+                    Mode<GEMM_WGRAD_W1>::kCS * ((H + BN - 1) / BN);
+      break;
+    case GEMM_WGRAD_W2:
+      ok = make_map(&m[0], g.A, N, H, 64) && make_map(&m[1], g.B, N, F, 64);
+      ntile_bound = (long long)E * ceil_div(ceil_div(H, BM), Mode<GEMM_WGRAD_W2>::kCS) *
+                    Mode<GEMM_WGRAD_W2>::kCS * ((F + BN - 1) / BN);
+      break;
+    default:
+      set_error("unknown grouped GEMM mode %d", g.mode);
+      return false;
+  }
+  if (!ok) return false;
+  if (g.mode != GEMM_FC2_DGRAD) m[2] = m[0];  // only FC2 dgrad reads a third tensor
+  switch (g.mode) {  // the outputs written by TMA stores
+    case GEMM_FC2_FWD:
+    case GEMM_FC1_DGRAD: ok = make_store_map(&m[3], g.out0, 1, N, H, 2); break;
+    case GEMM_WGRAD_W1: ok = make_store_map(&m[3], g.out0, E, 2 * F, H, 3); break;
+    case GEMM_WGRAD_W2: ok = make_store_map(&m[3], g.out1, E, H, F, 3); break;
+    default: m[3] = m[0];
+  }
+  if (!ok) return false;
+  p.E = E;
+  p.H = H;
+  p.F = F;
+  p.N = N;
+  p.off = g.off;
+  p.out0 = g.out0;
+  p.out1 = g.out1;
+  p.aux = g.aux;
+  p.status = g.status;
+  p.dep = g.dep;
+  return true;
+}
+
+int grid_for(const GemmArgs& g, long long ntile_bound) {
+  int grid = device_sm_count();
+  if (g.max_ctas > 0 && g.max_ctas < grid) grid = g.max_ctas;
+  if (ntile_bound < grid) grid = (int)(ntile_bound > 0 ? ntile_bound : 1);
+  return grid;
 }
 
 }  // namespace
@@ -937,72 +1179,52 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
     }
     return MOE_OK;
   }
-  CUtensorMap ma, mb, mc, md;
-  bool ok = true;
-  long long ntile_bound = 0;  // upper bound on tiles, for the grid size
-  switch (g.mode) {
-    case GEMM_FC1_FWD:
-      ok = make_map(&ma, g.A, N, H, 128) && make_map(&mb, g.B, (long long)E * 2 * F, H, 128);
-      ntile_bound = (N / BM + 2 * E) * ((F + 127) / 128);
-      break;
-    case GEMM_FC2_FWD:
-      ok = make_map(&ma, g.A, N, F, 128) && make_map(&mb, g.B, (long long)E * H, F, 128);
-      ntile_bound = (N / BM + 2 * E) * ((H + BN - 1) / BN);
-      break;
-    case GEMM_FC2_DGRAD:
-      ok = make_map(&ma, g.A, N, H, 128) && make_map(&mb, g.B, (long long)E * H, F, 64) &&
-           make_map(&mc, g.aux, N, 2 * F, 128);
-      ntile_bound = (N / BM + 2 * E) * ((F + 127) / 128);
-      break;
-    case GEMM_FC1_DGRAD:
-      ok = make_map(&ma, g.A, N, 2 * F, 128) && make_map(&mb, g.B, (long long)E * 2 * F, H, 64);
-      ntile_bound = (N / BM + 2 * E) * ((H + BN - 1) / BN);
-      break;
-    case GEMM_WGRAD_W1:
-      ok = make_map(&ma, g.A, N, 2 * F, 64) && make_map(&mb, g.B, N, H, 64);
-      ntile_bound = (long long)E * ceil_div(ceil_div(2 * F, BM), Mode<GEMM_WGRAD_W1>::kCS) *
-                    Mode<GEMM_WGRAD_W1>::kCS * ((H + BN - 1) / BN);
-      break;
-    case GEMM_WGRAD_W2:
-      ok = make_map(&ma, g.A, N, H, 64) && make_map(&mb, g.B, N, F, 64);
-      ntile_bound = (long long)E * ceil_div(ceil_div(H, BM), Mode<GEMM_WGRAD_W2>::kCS) *
-                    Mode<GEMM_WGRAD_W2>::kCS * ((F + BN - 1) / BN);
-      break;
-    default:
-      set_error("unknown grouped GEMM mode %d", g.mode);
-      return MOE_ERR_INVALID_ARG;
-  }
-  if (!ok) return MOE_ERR_CUDA;
-  if (g.mode != GEMM_FC2_DGRAD) mc = ma;  // only FC2 dgrad reads a third tensor
-  switch (g.mode) {  // the outputs written by TMA stores
-    case GEMM_FC2_FWD:
-    case GEMM_FC1_DGRAD: ok = make_store_map(&md, g.out0, 1, N, H, 2); break;
-    case GEMM_WGRAD_W1: ok = make_store_map(&md, g.out0, E, 2 * F, H, 3); break;
-    case GEMM_WGRAD_W2: ok = make_store_map(&md, g.out1, E, H, F, 3); break;
-    default: md = ma;
-  }
-  if (!ok) return MOE_ERR_CUDA;
+  CUtensorMap m[4];
   KParams p;
-  p.E = E;
-  p.H = H;
-  p.F = F;
-  p.N = N;
-  p.off = g.off;
-  p.out0 = g.out0;
-  p.out1 = g.out1;
-  p.aux = g.aux;
-  p.status = g.status;
-  int grid = device_sm_count();
-  if (g.max_ctas > 0 && g.max_ctas < grid) grid = g.max_ctas;
-  if (ntile_bound < grid) grid = (int)(ntile_bound > 0 ? ntile_bound : 1);
+  long long ntile_bound = 0;  // upper bound on tiles, for the grid size
+  if (!mode_setup(d, g, m, p, ntile_bound))
+    return g.mode > GEMM_WGRAD_W2 ? MOE_ERR_INVALID_ARG : MOE_ERR_CUDA;
+  const int grid = grid_for(g, ntile_bound);
+  const int id = K_GEMM_FC1_FWD + g.mode;
   switch (g.mode) {
-    case GEMM_FC1_FWD: return launch_mode<GEMM_FC1_FWD>(ma, mb, mc, md, p, grid, st);
-    case GEMM_FC2_FWD: return launch_mode<GEMM_FC2_FWD>(ma, mb, mc, md, p, grid, st);
-    case GEMM_FC2_DGRAD: return launch_mode<GEMM_FC2_DGRAD>(ma, mb, mc, md, p, grid, st);
-    case GEMM_FC1_DGRAD: return launch_mode<GEMM_FC1_DGRAD>(ma, mb, mc, md, p, grid, st);
-    case GEMM_WGRAD_W1: return launch_mode<GEMM_WGRAD_W1>(ma, mb, mc, md, p, grid, st);
-    default: return launch_mode<GEMM_WGRAD_W2>(ma, mb, mc, md, p, grid, st);
+    case GEMM_FC1_FWD: return launch_mode<GEMM_FC1_FWD, -1>(m, m, p, p, grid, id, st);
+    case GEMM_FC2_FWD: return launch_mode<GEMM_FC2_FWD, -1>(m, m, p, p, grid, id, st);
+    case GEMM_FC2_DGRAD: return launch_mode<GEMM_FC2_DGRAD, -1>(m, m, p, p, grid, id, st);
+    case GEMM_FC1_DGRAD: return launch_mode<GEMM_FC1_DGRAD, -1>(m, m, p, p, grid, id, st);
+    case GEMM_WGRAD_W1: return launch_mode<GEMM_WGRAD_W1, -1>(m, m, p, p, grid, id, st);
+    default: return launch_mode<GEMM_WGRAD_W2, -1>(m, m, p, p, grid, id, st);
   }
+}
+
+moe_status_t launch_grouped_gemm_chain(const moe_layer_desc_t& d, const GemmArgs& g1,
+                                       const GemmArgs& g2, cudaStream_t st) {
+  const long long N = (long long)d.T * d.k;
+  if (N == 0) return MOE_OK;
+  const bool fwd = g1.mode == GEMM_FC1_FWD && g2.mode == GEMM_FC2_FWD;
+  const bool dgrad = g1.mode == GEMM_FC2_DGRAD && g2.mode == GEMM_FC1_DGRAD;
+  if (!fwd && !dgrad) {
+    set_error("unsupported grouped GEMM chain %d -> %d", g1.mode, g2.mode);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!g1.dep) {
+    set_error("a grouped GEMM chain needs its per-expert counters");
+    return MOE_ERR_INVALID_ARG;
+  }
+  CUtensorMap m1[4], m2[4];
+  KParams p1, p2;
+  long long b1 = 0, b2 = 0;
+  if (!mode_setup(d, g1, m1, p1, b1) || !mode_setup(d, g2, m2, p2, b2)) return MOE_ERR_CUDA;
+  p2.dep = p1.dep;
+  // the counters start at zero for every launch
+  cudaError_t e = cudaMemsetAsync(g1.dep, 0, (size_t)d.E * sizeof(int), st);
+  if (e != cudaSuccess) {
+    set_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  const int grid = grid_for(g1, b1 + b2);
+  if (fwd)
+    return launch_mode<GEMM_FC1_FWD, GEMM_FC2_FWD>(m1, m2, p1, p2, grid, K_GEMM_FFN_FWD, st);
+  return launch_mode<GEMM_FC2_DGRAD, GEMM_FC1_DGRAD>(m1, m2, p1, p2, grid, K_GEMM_FFN_DGRAD, st);
 }
 
 }  // namespace moe

@@ -26,7 +26,7 @@ constexpr int kLayoutTokensPerBlock = 256;
 constexpr int kRouteBwdRowsPerChunk = 64;
 
 struct WsLayout {
-  size_t status, logits, hist, dz, dwr_part, total;
+  size_t status, logits, hist, dz, dwr_part, dep, total;
 };
 WsLayout ws_layout(const moe_layer_desc_t& d);
 
@@ -37,7 +37,7 @@ enum KernelId {
   K_ROUTE_LOGITS = 0, K_ROUTE_TOPK, K_LAYOUT_COUNT, K_LAYOUT_ASSIGN, K_PERMUTE, K_COMBINE,
   K_COMBINE_BWD, K_PERMUTE_BWD, K_ROUTE_BWD_DX, K_ROUTE_BWD_DWR_PARTIAL, K_ROUTE_BWD_DWR_REDUCE,
   K_GEMM_FC1_FWD, K_GEMM_FC2_FWD, K_GEMM_FC2_DGRAD, K_GEMM_FC1_DGRAD, K_GEMM_WGRAD_W1,
-  K_GEMM_WGRAD_W2, K_DISPATCH_BWD, K_NUM
+  K_GEMM_WGRAD_W2, K_DISPATCH_BWD, K_GEMM_FFN_FWD, K_GEMM_FFN_DGRAD, K_NUM
 };
 
 // Wraps one kernel launch: counts it and, while profiling is on, brackets it
@@ -137,7 +137,13 @@ struct GemmArgs {
   const bf16* aux;
   int* status;
   int max_ctas;       // 0 = all SMs
+  int* dep;           // [E] per-expert counters for a chain (workspace), else NULL
 };
 moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, cudaStream_t st);
+// Two dependent GEMMs in one persistent launch: FC1 fwd then FC2 fwd, or FC2
+// dgrad then FC1 dgrad. A tile of the second reads the first's output of its
+// expert and waits for it through the per-expert counters g1.dep (zeroed here).
+moe_status_t launch_grouped_gemm_chain(const moe_layer_desc_t& d, const GemmArgs& g1,
+                                       const GemmArgs& g2, cudaStream_t st);
 
 }  // namespace moe
