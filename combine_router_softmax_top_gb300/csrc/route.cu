@@ -308,17 +308,19 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
   pdl_wait();
   constexpr int KB = KMAX < 8 ? KMAX : 8;  // rows in flight per batch
   extern __shared__ __align__(16) uint8_t s_wr[];  // [E][kDxPitchB]
-  const int c = blockIdx.y * 8 + (threadIdx.x & 7);  // 16-byte chunk of the row
+  // slices vary fastest across the grid: blocks resident together read
+  // different column windows of the rows
+  const int c = blockIdx.x * 8 + (threadIdx.x & 7);  // 16-byte chunk of the row
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) {
     const int e = i >> 3, q = i & 7;
     *reinterpret_cast<uint4*>(s_wr + e * kDxPitchB + q * 16) =
-        __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)e * H) + blockIdx.y * 8 + q);
+        __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)e * H) + blockIdx.x * 8 + q);
   }
   __syncthreads();
   const long long N = (long long)T * k;
-  const bool writer = blockIdx.y == 0 && (threadIdx.x & 7) == 0;
+  const bool writer = blockIdx.x == 0 && (threadIdx.x & 7) == 0;
   for (int tl = threadIdx.x >> 3; tl < kDxTok; tl += 32) {
-    const int t = blockIdx.x * kDxTok + tl;
+    const int t = blockIdx.y * kDxTok + tl;
     if (t >= T) break;
     const size_t tk = (size_t)t * k;
     float dzj[KMAX];
@@ -598,7 +600,7 @@ template <bool FUSED>
 void launch_dx(const moe_layer_desc_t& d, const float* dgates, const float* gates,
                const int32_t* idx, const bf16* w_r, const float* dx32, const bf16* dx_perm,
                const int32_t* slot, bf16* dx, float* dz, int* status, cudaStream_t st) {
-  const dim3 g(ceil_div(d.T, kDxTok), d.H / 64);
+  const dim3 g(d.H / 64, ceil_div(d.T, kDxTok));
   const size_t smem = (size_t)d.E * kDxPitchB;
   if (d.k <= 4)
     launch_k(route_bwd_dx_kernel<4, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
