@@ -262,7 +262,10 @@ typedef struct moe_mb_bufs {
 moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b, void* stream);
 
 /* Backward in the chain order combine -> experts (dgrad) -> dispatch -> router,
- * then the expert wgrad when run_wgrad != 0. The dispatch backward is fused
+ * and the expert wgrad when run_wgrad != 0. The wgrad runs on a library-owned
+ * side stream (one per device, created by the first call with that device
+ * current) beside the dispatch and router backward, forked after the dgrad and
+ * joined into `stream` before the call returns. The dispatch backward is fused
  * into the router's dx pass here: the row sums of dx_perm stay in registers,
  * so b->dx32 is not written (dx has the same bits as the two-call path
  * moe_permute_bwd + moe_route_bwd). */
