@@ -34,11 +34,11 @@ def make_pair(name=None, **kw):
     return d, (i0, i1), (b0, b1)
 
 
-def run(d, bufs, overlap, defer, steps=2):
+def run(d, bufs, overlap, defer, steps=2, gemm_sms=0):
     sc = torch.cuda.Stream(priority=-1)
     sg = torch.cuda.Stream()
     torch.cuda.synchronize()
-    s = moe.Scheduler(d, sc, sg, gemm_sms=0)
+    s = moe.Scheduler(d, sc, sg, gemm_sms=gemm_sms)
     for _ in range(steps):
         s.step(bufs[0], bufs[1], overlap=overlap, defer_wgrad=defer)
     tm = s.timings()
@@ -95,3 +95,21 @@ def test_two_microbatch_workload_overlap_matches_serial():
     for m in range(2):
         for key in ref[m]:
             assert np.array_equal(got[m][key], ref[m][key]), (m, key)
+
+
+@pytest.mark.parametrize("gemm_sms", [8, 30, 120])
+def test_capped_gemm_grid_is_bit_identical(gemm_sms):
+    """With the GEMM grid capped, each CTA of a chained expert GEMM (FC1 -> FC2,
+    FC2 dgrad -> FC1 dgrad) works through many rounds of tiles and the second
+    GEMM's tiles wait on other CTAs' first-GEMM tiles: same bits as uncapped."""
+    d, inps, bufs = make_pair(**SMALL)
+    run(d, bufs, overlap=False, defer=False)
+    ref = [collect(b, i) for b, i in zip(bufs, inps)]
+    for b in bufs:
+        for n in ("y", "dx", "dw1", "dw2", "dw_r", "a", "h", "o", "da", "d_o", "dx_perm"):
+            getattr(b, n).zero_()
+    run(d, bufs, overlap=True, defer=True, gemm_sms=gemm_sms)
+    got = [collect(b, i) for b, i in zip(bufs, inps)]
+    for m in range(2):
+        for key in ref[m]:
+            assert np.array_equal(got[m][key], ref[m][key]), (gemm_sms, m, key)
