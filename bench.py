@@ -94,6 +94,46 @@ def algorithmic(d) -> dict:
     return out
 
 
+def kernel_stats(agg: dict, algo: dict, pk: dict, wr_gbs: float) -> dict:
+    """Per-kernel figures from {kernel: [launches, total ms]} and the
+    algorithmic (read, write, flops) of each launch."""
+    kernels = {}
+    for name, (n, tot) in agg.items():
+        avg_ms = tot / n
+        rd, wr, fl = algo.get(name, (0.0, 0.0, 0.0))
+        by = rd + wr
+        # HBM floor with writes counted at the write-only rate: a kernel that
+        # mostly writes (the weight gradients) cannot reach the copy bandwidth
+        t_floor = max(by / (pk["hbm_gbs"] * 1e9), wr / (wr_gbs * 1e9))
+        gbs = by / (avg_ms * 1e-3) / 1e9 if avg_ms > 0 else 0.0
+        tfl = fl / (avg_ms * 1e-3) / 1e12 if avg_ms > 0 else 0.0
+        t_hbm = by / (pk["hbm_gbs"] * 1e9)
+        t_tc = fl / (pk["bf16_tflops_sustained"] * 1e12) if name.startswith("gemm") else 0.0
+        t_alu = fl / (FP32_TFLOPS * 1e12) if name in ALU_BOUND else 0.0
+        bound = "tensor" if t_tc > t_hbm else "hbm"
+        if t_alu > max(t_tc, t_hbm):
+            bound = "alu"
+        t_bound = {"tensor": t_tc, "hbm": t_hbm, "alu": t_alu}[bound]
+        frac = t_bound / (avg_ms * 1e-3) if avg_ms > 0 else 0.0
+        kernels[name] = {"launches": n, "avg_us": round(avg_ms * 1e3, 2),
+                         "share": None, "GB_s": round(gbs, 1), "TFLOP_s": round(tfl, 1),
+                         "bound": bound, "roofline_frac": round(frac, 3),
+                         "hbm_floor_us": round(t_floor * 1e6, 1),
+                         "hbm_floor_frac": round(t_floor / (avg_ms * 1e-3), 3) if avg_ms > 0 else None,
+                         "algo_bytes": int(by), "algo_write_bytes": int(wr), "algo_flops": fl}
+    return kernels
+
+
+def accum_algorithmic(d) -> dict:
+    """Bytes and flops of the weight-gradient GEMMs that add into fp32 main
+    gradients: the operands, plus each main gradient read and written once."""
+    T, H, E, k, F = d["T"], d["H"], d["E"], d["k"], d["F"]
+    N = T * k
+    w1, w2 = E * 2 * F * H * 4, E * H * F * 4
+    return {"gemm_wgrad_w1": (N * 2 * F * 2 + N * H * 2 + w1, w1, 2.0 * N * 2 * F * H),
+            "gemm_wgrad_w2": (N * H * 2 + N * F * 2 + w2, w2, 2.0 * N * H * F)}
+
+
 def hbm_write_gbs(dev) -> float:
     """Write-only HBM bandwidth, measured live: best of 5 zero-fills of 1 GiB."""
     buf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
@@ -319,30 +359,7 @@ def run_ours(args, rank, world, local):
         a[0] += 1
         a[1] += t
     wr_gbs = hbm_write_gbs(dev)
-    kernels = {}
-    for name, (n, tot) in agg.items():
-        avg_ms = tot / n
-        rd, wr, fl = algo.get(name, (0.0, 0.0, 0.0))
-        by = rd + wr
-        # HBM floor with writes counted at the write-only rate: a kernel that
-        # mostly writes (the weight gradients) cannot reach the copy bandwidth
-        t_floor = max(by / (pk["hbm_gbs"] * 1e9), wr / (wr_gbs * 1e9))
-        gbs = by / (avg_ms * 1e-3) / 1e9 if avg_ms > 0 else 0.0
-        tfl = fl / (avg_ms * 1e-3) / 1e12 if avg_ms > 0 else 0.0
-        t_hbm = by / (pk["hbm_gbs"] * 1e9)
-        t_tc = fl / (pk["bf16_tflops_sustained"] * 1e12) if name.startswith("gemm") else 0.0
-        t_alu = fl / (FP32_TFLOPS * 1e12) if name in ALU_BOUND else 0.0
-        bound = "tensor" if t_tc > t_hbm else "hbm"
-        if t_alu > max(t_tc, t_hbm):
-            bound = "alu"
-        t_bound = {"tensor": t_tc, "hbm": t_hbm, "alu": t_alu}[bound]
-        frac = t_bound / (avg_ms * 1e-3) if avg_ms > 0 else 0.0
-        kernels[name] = {"launches": n, "avg_us": round(avg_ms * 1e3, 2),
-                         "share": None, "GB_s": round(gbs, 1), "TFLOP_s": round(tfl, 1),
-                         "bound": bound, "roofline_frac": round(frac, 3),
-                         "hbm_floor_us": round(t_floor * 1e6, 1),
-                         "hbm_floor_frac": round(t_floor / (avg_ms * 1e-3), 3) if avg_ms > 0 else None,
-                         "algo_bytes": int(by), "algo_write_bytes": int(wr), "algo_flops": fl}
+    kernels = kernel_stats(agg, algo, pk, wr_gbs)
     total = sum(v[1] for v in agg.values())
     for name in kernels:
         kernels[name]["share"] = round(agg[name][1] / total, 4) if total else None
@@ -370,6 +387,36 @@ def run_ours(args, rank, world, local):
                 if n in agg]
     pc_ms = sum(agg[n][1] for n in pc_names) / args.steps
     pc_bytes = sum(algo[n][0] + algo[n][1] for n in pc_names)
+
+    # ---- the weight gradients added into fp32 main gradients (gradient
+    # accumulation fusion), timed on their own on the step's saved tensors: not
+    # part of the step above, which stores bf16 weight gradients
+    accum = None
+    if not args.no_accum:
+        m1 = torch.zeros(inp.E, 2 * inp.F, inp.H, dtype=torch.float32, device=dev)
+        m2 = torch.zeros(inp.E, inp.H, inp.F, dtype=torch.float32, device=dev)
+
+        def accum_call():
+            moe.moe_expert_ffn_bwd_wgrad_accum(d, b.x_perm, b.h, b.d_o, b.da, b.off, m1, m2,
+                                               b.ws, st)
+        for _ in range(args.warmup):
+            accum_call()
+        torch.cuda.synchronize(dev)
+        moe.moe_profile_start(2 * args.steps + 8)
+        for _ in range(args.steps):
+            accum_call()
+        torch.cuda.synchronize(dev)
+        aprof = moe.moe_profile_stop(2 * args.steps + 8)
+        status = moe.moe_device_status(d, b.ws, st)
+        if status != moe.MOE_OK:
+            raise RuntimeError(f"device status {status}: {moe.lib().moe_last_error()}")
+        aagg = {}
+        for name, t in aprof:
+            a = aagg.setdefault(name, [0, 0.0])
+            a[0] += 1
+            a[1] += t
+        accum = kernel_stats(aagg, accum_algorithmic(shape), pk, wr_gbs)
+        del m1, m2
 
     # ---- end to end through the host-buffer C-ABI call
     hx = inp.x.clone().pin_memory()
@@ -404,6 +451,10 @@ def run_ours(args, rank, world, local):
         "grouped_gemm_TFLOP_s": round(gemm_fl / (gemm_ms * 1e-3) / 1e12, 1) if gemm_ms else None,
         "kernels": kernels,
     }
+    if accum is not None:
+        out["wgrad_accum_fp32"] = {"note": "weight gradients added into fp32 main gradients, "
+                                           "timed separately; not in value",
+                                   "kernels": accum}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, dt = oracle_tokens_per_s(args.workload, args.cpu_sample_tokens)
         out["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cpu_cores(),
@@ -510,6 +561,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_30b_a3b_balanced")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-accum", action="store_true",
+                    help="skip the separate timing of the fp32-accumulating weight gradients")
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
     ap.add_argument("--ref-sample-tokens", type=int, default=64)
     ap.add_argument("--schedule", action="store_true",

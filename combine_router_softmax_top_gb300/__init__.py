@@ -22,6 +22,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "moe.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(5)
 ROUTE_SOFTMAX_TOPK, ROUTE_FORCED_BALANCED = 0, 1
+FLAG_WGRAD_ACCUM_FP32 = 1  # MOE_FLAG_WGRAD_ACCUM_FP32: add wgrad into fp32 main gradients
 PHASES = ("dispatch", "ffn_fwd", "combine", "combine_bwd", "dgrad", "dispatch_bwd", "wgrad")
 
 _STATUS = {1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout"}
@@ -37,8 +38,8 @@ class LayerDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "E", "k", "F", "R", "mode", "flags")]
 
     @classmethod
-    def of(cls, T, H, E, k, F, R=1, mode=ROUTE_SOFTMAX_TOPK):
-        return cls(T, H, E, k, F, R, mode, 0)
+    def of(cls, T, H, E, k, F, R=1, mode=ROUTE_SOFTMAX_TOPK, flags=0):
+        return cls(T, H, E, k, F, R, mode, flags)
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -49,8 +50,12 @@ _MB_FIELDS = ["x", "dy", "w_r", "bias", "w1", "w2", "logits", "idx", "gates", "c
               "dgates", "da", "dx_perm", "dx32", "dx", "dw_r", "dw1", "dw2", "ws"]
 
 
+_MB_FIELDS_TAIL = ["main_dw1", "main_dw2"]
+
+
 class MbBufs(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in _MB_FIELDS] + [("ws_bytes", ctypes.c_size_t)]
+    _fields_ = ([(n, ctypes.c_void_p) for n in _MB_FIELDS] + [("ws_bytes", ctypes.c_size_t)]
+                + [(n, ctypes.c_void_p) for n in _MB_FIELDS_TAIL])
 
 
 class PhaseTime(ctypes.Structure):
@@ -85,6 +90,8 @@ _SIGS = {
     "moe_combine_bwd": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
     "moe_expert_ffn_bwd_dgrad": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_expert_ffn_bwd_wgrad": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
+    "moe_expert_ffn_bwd_wgrad_accum": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP],
+                                       _I32),
     "moe_permute_bwd": ([_DP, _VP, _VP, _VP, _VP], _I32),
     "moe_route_bwd": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_layer_forward": ([_DP, ctypes.POINTER(MbBufs), _VP], _I32),
@@ -225,6 +232,14 @@ def moe_expert_ffn_bwd_wgrad(desc, x_perm, h, d_o, da, off, dw1, dw2, ws, stream
            "moe_expert_ffn_bwd_wgrad")
 
 
+def moe_expert_ffn_bwd_wgrad_accum(desc, x_perm, h, d_o, da, off, main_dw1, main_dw2, ws,
+                                   stream=None):
+    _check(lib().moe_expert_ffn_bwd_wgrad_accum(_d(desc), _p(x_perm), _p(h), _p(d_o), _p(da),
+                                                _p(off), _p(main_dw1), _p(main_dw2), _p(ws),
+                                                ws.numel() * ws.element_size(), _s(stream)),
+           "moe_expert_ffn_bwd_wgrad_accum")
+
+
 def moe_permute_bwd(desc, dx_perm, slot, dx32, stream=None):
     _check(lib().moe_permute_bwd(_d(desc), _p(dx_perm), _p(slot), _p(dx32), _s(stream)),
            "moe_permute_bwd")
@@ -280,7 +295,13 @@ class LayerBuffers:
         self.da, self.dx_perm = z(rows, 2 * F, dt=bf), z(rows, H, dt=bf)
         self.dx32, self.dx = z(T, H, dt=f32), z(T, H, dt=bf)
         self.dw_r = z(E, H, dt=f32)
-        self.dw1, self.dw2 = z(E, 2 * F, H, dt=bf), z(E, H, F, dt=bf)
+        if desc.flags & FLAG_WGRAD_ACCUM_FP32:
+            # the weight gradients are added into fp32 main gradients
+            self.dw1 = self.dw2 = None
+            self.main_dw1, self.main_dw2 = z(E, 2 * F, H, dt=f32), z(E, H, F, dt=f32)
+        else:
+            self.dw1, self.dw2 = z(E, 2 * F, H, dt=bf), z(E, H, F, dt=bf)
+            self.main_dw1 = self.main_dw2 = None
         nbytes = moe_workspace_size(desc)
         self.ws = z((nbytes + 15) // 16 * 16, dt=torch.uint8)
         self._struct = None
@@ -299,7 +320,7 @@ class LayerBuffers:
     def struct(self) -> MbBufs:
         if self._struct is None:
             s = MbBufs()
-            for n in _MB_FIELDS:
+            for n in _MB_FIELDS + _MB_FIELDS_TAIL:
                 t = getattr(self, n)
                 setattr(s, n, None if t is None else t.data_ptr())
             s.ws_bytes = self.ws.numel()

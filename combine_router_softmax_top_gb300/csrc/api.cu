@@ -114,7 +114,10 @@ moe_status_t validate(const moe_layer_desc_t* d) {
   if (d->mode != MOE_ROUTE_SOFTMAX_TOPK && d->mode != MOE_ROUTE_FORCED_BALANCED) {
     set_error("unknown routing mode %d", d->mode); return MOE_ERR_INVALID_ARG;
   }
-  if (d->flags != 0) { set_error("flags must be 0"); return MOE_ERR_INVALID_ARG; }
+  if ((d->flags & ~MOE_FLAG_WGRAD_ACCUM_FP32) != 0) {
+    set_error("unknown flags 0x%x", (unsigned)d->flags);
+    return MOE_ERR_INVALID_ARG;
+  }
   if (d->H % 64 || d->F % 64) {
     set_error("H=%d and F=%d must be multiples of 64", d->H, d->F); return MOE_ERR_UNSUPPORTED;
   }
@@ -217,15 +220,18 @@ moe_status_t op_dgrad(const moe_layer_desc_t& d, const bf16* d_o, const bf16* a,
   return launch_grouped_gemm_chain(d, g, g2, st);
 }
 
+// Weight gradients: stored as bf16 into dw1/dw2, or, when main_dw1/main_dw2
+// are given, added in fp32 into those main gradients (dw1/dw2 unused).
 moe_status_t op_wgrad(const moe_layer_desc_t& d, const bf16* x_perm, const bf16* h,
                       const bf16* d_o, const bf16* da, const int32_t* off, bf16* dw1, bf16* dw2,
-                      void* ws, int max_ctas, cudaStream_t st) {
+                      float* main_dw1, float* main_dw2, void* ws, int max_ctas, cudaStream_t st) {
   GemmArgs g = {};
   g.mode = GEMM_WGRAD_W1;
   g.A = da;
   g.B = x_perm;
   g.off = off;
-  g.out0 = dw1;
+  g.out0 = main_dw1 ? nullptr : dw1;
+  g.acc = main_dw1;
   g.status = status_of(ws);
   g.max_ctas = max_ctas;
   MOE_CHECK(launch_grouped_gemm(d, g, st));
@@ -233,7 +239,8 @@ moe_status_t op_wgrad(const moe_layer_desc_t& d, const bf16* x_perm, const bf16*
   g.A = d_o;
   g.B = h;
   g.out0 = nullptr;
-  g.out1 = dw2;
+  g.out1 = main_dw2 ? nullptr : dw2;
+  g.acc = main_dw2;
   return launch_grouped_gemm(d, g, st);
 }
 
@@ -297,10 +304,11 @@ moe_status_t op_dispatch_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* 
 
 moe_status_t op_wgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
                          cudaStream_t st) {
+  const bool acc = (d.flags & MOE_FLAG_WGRAD_ACCUM_FP32) != 0;
   return op_wgrad(d, reinterpret_cast<const bf16*>(b->x_perm), reinterpret_cast<const bf16*>(b->h),
                   reinterpret_cast<const bf16*>(b->d_o), reinterpret_cast<const bf16*>(b->da),
-                  b->off, reinterpret_cast<bf16*>(b->dw1), reinterpret_cast<bf16*>(b->dw2), b->ws,
-                  max_ctas, st);
+                  b->off, reinterpret_cast<bf16*>(b->dw1), reinterpret_cast<bf16*>(b->dw2),
+                  acc ? b->main_dw1 : nullptr, acc ? b->main_dw2 : nullptr, b->ws, max_ctas, st);
 }
 
 moe_status_t check_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, bool bwd) {
@@ -311,7 +319,12 @@ moe_status_t check_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, bool bw
   MOE_PTR(b->x_perm); MOE_PTR(b->a); MOE_PTR(b->h); MOE_PTR(b->o); MOE_PTR(b->y);
   if (bwd) {
     MOE_PTR(b->dy); MOE_PTR(b->d_o); MOE_PTR(b->dgates); MOE_PTR(b->da); MOE_PTR(b->dx_perm);
-    MOE_PTR(b->dx32); MOE_PTR(b->dx); MOE_PTR(b->dw_r); MOE_PTR(b->dw1); MOE_PTR(b->dw2);
+    MOE_PTR(b->dx32); MOE_PTR(b->dx); MOE_PTR(b->dw_r);
+    if (d.flags & MOE_FLAG_WGRAD_ACCUM_FP32) {
+      MOE_PTR(b->main_dw1); MOE_PTR(b->main_dw2);
+    } else {
+      MOE_PTR(b->dw1); MOE_PTR(b->dw2);
+    }
   }
   return check_ws(d, b->ws, b->ws_bytes);
 }
@@ -432,8 +445,21 @@ moe_status_t moe_expert_ffn_bwd_wgrad(const moe_layer_desc_t* d, const moe_bf16*
   MOE_CHECK(validate(d));
   MOE_PTR(x_perm); MOE_PTR(h); MOE_PTR(d_o); MOE_PTR(da); MOE_PTR(off); MOE_PTR(dw1); MOE_PTR(dw2);
   MOE_CHECK(check_ws(*d, ws, ws_bytes));
-  return op_wgrad(*d, BF(x_perm), BF(h), BF(d_o), BF(da), off, BFW(dw1), BFW(dw2), ws, 0,
-                  S(stream));
+  return op_wgrad(*d, BF(x_perm), BF(h), BF(d_o), BF(da), off, BFW(dw1), BFW(dw2), nullptr,
+                  nullptr, ws, 0, S(stream));
+}
+
+moe_status_t moe_expert_ffn_bwd_wgrad_accum(const moe_layer_desc_t* d, const moe_bf16* x_perm,
+                                            const moe_bf16* h, const moe_bf16* d_o,
+                                            const moe_bf16* da, const int32_t* off,
+                                            float* main_dw1, float* main_dw2, void* ws,
+                                            size_t ws_bytes, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(x_perm); MOE_PTR(h); MOE_PTR(d_o); MOE_PTR(da); MOE_PTR(off); MOE_PTR(main_dw1);
+  MOE_PTR(main_dw2);
+  MOE_CHECK(check_ws(*d, ws, ws_bytes));
+  return op_wgrad(*d, BF(x_perm), BF(h), BF(d_o), BF(da), off, nullptr, nullptr, main_dw1,
+                  main_dw2, ws, 0, S(stream));
 }
 
 moe_status_t moe_permute_bwd(const moe_layer_desc_t* d, const moe_bf16* dx_perm,

@@ -68,6 +68,7 @@ struct KParams {
   const bf16* aux;
   int* status;
   int* dep;  // fused launches: per-expert count of first-mode epilogue warps done
+  int accum;  // wgrad: add the fp32 result into the store map's fp32 buffer
 };
 
 template <int MODE>
@@ -290,6 +291,48 @@ __device__ __forceinline__ void store_chunks(uint4* stage, uint32_t tbase, int c
       }
       warp_store32(stage, reinterpret_cast<float*>(cur), slab + 32 * cc, ld, lane, slab_rows,
                    cols_ok);
+    }
+    if (i + 1 < BN / 64) ptx::tmem_ld_wait(nxt);
+  }
+}
+
+// Adds this warp's half of an fp32 accumulator tile (BN/64 chunks of 32
+// columns from chunk c0) into an fp32 3D [expert, rows, cols] buffer. Each
+// chunk leaves as two 32-row x 16-column boxes through the staging buffer
+// (64-byte rows, the same swizzle as the bf16 boxes), added element-wise in L2
+// by TMA reductions; the map clips boxes at the matrix edge. Every element is
+// added exactly once per launch, so the result is fl(old + tile) whatever the
+// order in which tiles finish.
+__device__ __forceinline__ void reduce_chunks_f32(uint4* stage, uint32_t tbase, int c0, int lane,
+                                                  int ncols, const CUtensorMap* tm, int x0, int y0,
+                                                  int z0) {
+  uint32_t va[32], vb[32];
+  ptx::tmem_ld_32x32b_x32(tbase + 32 * c0, va);
+  ptx::tmem_ld_wait(va);
+#pragma unroll
+  for (int i = 0; i < BN / 64; ++i) {
+    const int cc = c0 + i;
+    uint32_t(&cur)[32] = (i & 1) ? vb : va;
+    uint32_t(&nxt)[32] = (i & 1) ? va : vb;
+    if (i + 1 < BN / 64) ptx::tmem_ld_32x32b_x32(tbase + 32 * (cc + 1), nxt);
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const int x = x0 + 32 * cc + 16 * hb;
+      if (x < ncols) {
+        if (lane == 0) ptx::bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          stage[lane * 4 + (q ^ ((lane >> 1) & 3))] =
+              make_uint4(cur[16 * hb + 4 * q], cur[16 * hb + 4 * q + 1],
+                         cur[16 * hb + 4 * q + 2], cur[16 * hb + 4 * q + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_reduce_add_3d(tm, stage, x, y0, z0);
+          ptx::bulk_commit_group();
+        }
+      }
     }
     if (i + 1 < BN / 64) ptx::tmem_ld_wait(nxt);
   }
@@ -616,7 +659,9 @@ __device__ __forceinline__ bool epilogue_tile(const Role& R, const KParams& p,
     bf16* slab = outp + (size_t)(t.m0 + q * 32) * Nd;
     if (t.nk == 0) {
       // an expert with no rows: zero weight gradient (plain stores, after
-      // the last TMA store has finished reading the staging buffer)
+      // the last TMA store has finished reading the staging buffer); when
+      // accumulating, nothing is added
+      if (p.accum) return true;
       float z[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) z[i] = 0.f;
@@ -633,8 +678,12 @@ __device__ __forceinline__ bool epilogue_tile(const Role& R, const KParams& p,
     ptx::tc_fence_after();
     if (tr) trace(p, MODE, ew == 0 ? 4 : 6, ti);
     const uint32_t tbase = R.tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-    store_chunks(stage, tbase, c0, slab + t.n0, Nd, t.n0, lane, slab_rows, tmD, M::kStoreDims,
-                 t.n0, t.m0 + q * 32, t.e);
+    if (p.accum) {
+      if (slab_rows > 0) reduce_chunks_f32(stage, tbase, c0, lane, Nd, tmD, t.n0, t.m0 + q * 32, t.e);
+    } else {
+      store_chunks(stage, tbase, c0, slab + t.n0, Nd, t.n0, lane, slab_rows, tmD, M::kStoreDims,
+                   t.n0, t.m0 + q * 32, t.e);
+    }
   } else {
     if (!ptx::mbar_wait(&ctl.tmem_full[acc], acc_phase, &ctl.abort, kWaitLimitNs)) {
       if (lane == 0) flag_timeout(ctl, p.status, 5);
@@ -1003,21 +1052,24 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
   return true;
 }
 
-// Store map of a bf16 output: 2D [rows, cols] or 3D [experts, rows, cols],
-// row-major, box 32 columns x 32 rows (x 1 expert), 64-byte swizzle (the
-// staging buffer's layout: 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)).
+// Store map of an output: 2D [rows, cols] or 3D [experts, rows, cols],
+// row-major, boxes of 32 rows (x 1 expert) and 64 bytes: 32 bf16 columns, or
+// 16 fp32 columns for the accumulated weight gradients (f32). 64-byte swizzle,
+// the staging buffer's layout: 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3).
 bool make_store_map(CUtensorMap* m, void* base, long long experts, long long rows, long long cols,
-                    int dims) {
+                    int dims, bool f32 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
     return false;
   }
+  const int es_bytes = f32 ? 4 : 2;
   cuuint64_t dim[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)experts};
-  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(rows * cols * 2)};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * es_bytes, (cuuint64_t)(rows * cols * es_bytes)};
+  cuuint32_t box[3] = {(cuuint32_t)(64 / es_bytes), 32, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dims, base, dim, strides, box, es,
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   dims, base, dim, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -1138,8 +1190,14 @@ bool mode_setup(const moe_layer_desc_t& d, const GemmArgs& g, CUtensorMap (&m)[4
   switch (g.mode) {  // the outputs written by TMA stores
     case GEMM_FC2_FWD:
     case GEMM_FC1_DGRAD: ok = make_store_map(&m[3], g.out0, 1, N, H, 2); break;
-    case GEMM_WGRAD_W1: ok = make_store_map(&m[3], g.out0, E, 2 * F, H, 3); break;
-    case GEMM_WGRAD_W2: ok = make_store_map(&m[3], g.out1, E, H, F, 3); break;
+    case GEMM_WGRAD_W1:
+      ok = g.acc ? make_store_map(&m[3], g.acc, E, 2 * F, H, 3, true)
+                 : make_store_map(&m[3], g.out0, E, 2 * F, H, 3);
+      break;
+    case GEMM_WGRAD_W2:
+      ok = g.acc ? make_store_map(&m[3], g.acc, E, H, F, 3, true)
+                 : make_store_map(&m[3], g.out1, E, H, F, 3);
+      break;
     default: m[3] = m[0];
   }
   if (!ok) return false;
@@ -1153,6 +1211,7 @@ bool mode_setup(const moe_layer_desc_t& d, const GemmArgs& g, CUtensorMap (&m)[4
   p.aux = g.aux;
   p.status = g.status;
   p.dep = g.dep;
+  p.accum = g.acc != nullptr;
   return true;
 }
 
@@ -1169,6 +1228,7 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
   const long long N = (long long)d.T * d.k;
   const int E = d.E, H = d.H, F = d.F;
   if (N == 0) {
+    if (g.acc) return MOE_OK;  // accumulating nothing
     if (g.mode == GEMM_WGRAD_W1) {
       cudaError_t e = cudaMemsetAsync(g.out0, 0, (size_t)E * 2 * F * H * 2, st);
       if (e != cudaSuccess) { set_error("cudaMemsetAsync: %s", cudaGetErrorString(e)); return MOE_ERR_CUDA; }

@@ -138,6 +138,7 @@ struct GemmArgs {
   int* status;
   int max_ctas;       // 0 = all SMs
   int* dep;           // [E] per-expert counters for a chain (workspace), else NULL
+  float* acc;         // wgrad: fp32 gradient to add the result into (out0/out1 unused), else NULL
 };
 moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, cudaStream_t st);
 // Two dependent GEMMs in one persistent launch: FC1 fwd then FC2 fwd, or FC2

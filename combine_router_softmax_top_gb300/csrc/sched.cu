@@ -164,8 +164,12 @@ moe_status_t moe_sched_step(moe_sched_t* s, const moe_mb_bufs_t* mb, int32_t ove
   const moe_layer_desc_t& d = s->d;
   SCHK(check_mb(d, &mb[0], true));
   SCHK(check_mb(d, &mb[1], true));
-  if (mb[0].ws == mb[1].ws || mb[0].dw1 == mb[1].dw1 || mb[0].dw2 == mb[1].dw2 ||
-      mb[0].dw_r == mb[1].dw_r) {
+  const bool acc = (d.flags & MOE_FLAG_WGRAD_ACCUM_FP32) != 0;
+  const void* g1[2] = {acc ? (const void*)mb[0].main_dw1 : mb[0].dw1,
+                       acc ? (const void*)mb[1].main_dw1 : mb[1].dw1};
+  const void* g2[2] = {acc ? (const void*)mb[0].main_dw2 : mb[0].dw2,
+                       acc ? (const void*)mb[1].main_dw2 : mb[1].dw2};
+  if (mb[0].ws == mb[1].ws || g1[0] == g1[1] || g2[0] == g2[1] || mb[0].dw_r == mb[1].dw_r) {
     set_error("the two micro-batches need their own workspace and weight-gradient buffers");
     return MOE_ERR_INVALID_ARG;
   }

@@ -65,7 +65,20 @@ typedef enum {
   MOE_ROUTE_FORCED_BALANCED = 1 /* token t -> experts (k*t + j) mod E, j = 0..k-1 */
 } moe_route_mode_t;
 
-/* One MoE layer's shape. flags must be 0. */
+/* Layer flags (moe_layer_desc_t.flags, 0 or a bitwise or of these).
+ *
+ * MOE_FLAG_WGRAD_ACCUM_FP32: the layer calls (moe_layer_backward,
+ * moe_layer_step_host, moe_sched_step) add the expert weight gradients into the
+ * fp32 main gradients b->main_dw1 / b->main_dw2 instead of overwriting the bf16
+ * b->dw1 / b->dw2 (which may then be NULL). This is gradient accumulation
+ * fusion: the MoE expert-parallel overlap skill card, section "compatibility
+ * and constraints" and its troubleshooting table (delay_wgrad_compute with
+ * gradient_accumulation_fusion), and the "1. MoE EP Overlap" note's backward
+ * call with accumulate_grad=True (gradients add into .grad instead of
+ * overwriting it). See moe_expert_ffn_bwd_wgrad_accum for the arithmetic. */
+#define MOE_FLAG_WGRAD_ACCUM_FP32 1
+
+/* One MoE layer's shape. flags: 0 or MOE_FLAG_* bits. */
 typedef struct moe_layer_desc {
   int32_t T, H, E, k, F, R;
   int32_t mode;  /* moe_route_mode_t */
@@ -225,6 +238,22 @@ moe_status_t moe_expert_ffn_bwd_wgrad(const moe_layer_desc_t* d, const moe_bf16*
                                       const int32_t* off, moe_bf16* dw1, moe_bf16* dw2, void* ws,
                                       size_t ws_bytes, void* stream);
 
+/* Expert FFN weight gradient accumulated into fp32 main gradients (gradient
+ * accumulation fusion, see MOE_FLAG_WGRAD_ACCUM_FP32):
+ *   main_dw1[e] = fl32(main_dw1[e] + (da_e^T @ x_perm_e))   [2F,H]
+ *   main_dw2[e] = fl32(main_dw2[e] + (d_o_e^T @ h_e))       [H,F]
+ * The product is reduced in fp32 over the expert's rows (one tensor-core
+ * accumulator per output tile) and added with one fp32 addition per element,
+ * so repeated calls accumulate micro-batch after micro-batch in call order.
+ * An expert with no rows adds nothing. main_dw1 [E,2F,H] and main_dw2 [E,H,F]
+ * are fp32, read and written in place; the other arguments are as for
+ * moe_expert_ffn_bwd_wgrad. The call does not look at d->flags. */
+moe_status_t moe_expert_ffn_bwd_wgrad_accum(const moe_layer_desc_t* d, const moe_bf16* x_perm,
+                                            const moe_bf16* h, const moe_bf16* d_o,
+                                            const moe_bf16* da, const int32_t* off,
+                                            float* main_dw1, float* main_dw2, void* ws,
+                                            size_t ws_bytes, void* stream);
+
 /* Permute backward (dispatch backward): dx32[t,:] = sum_j dx_perm[slot[t,j], :]
  * in fp32, j ascending. dx_perm [N,H] bf16, slot [T,k] -> dx32 [T,H] fp32. */
 moe_status_t moe_permute_bwd(const moe_layer_desc_t* d, const moe_bf16* dx_perm,
@@ -256,6 +285,8 @@ typedef struct moe_mb_bufs {
   moe_bf16* d_o; float* dgates; moe_bf16* da; moe_bf16* dx_perm;        /* backward*/
   float* dx32; moe_bf16* dx; float* dw_r; moe_bf16* dw1; moe_bf16* dw2;
   void* ws; size_t ws_bytes;
+  float* main_dw1; float* main_dw2; /* fp32 [E,2F,H], [E,H,F]: used (+=) only
+                                       with MOE_FLAG_WGRAD_ACCUM_FP32 */
 } moe_mb_bufs_t;
 
 /* Forward: route, dispatch layout, permute, expert FFN, combine. */
@@ -314,8 +345,10 @@ moe_status_t moe_sched_create(const moe_layer_desc_t* d, void* stream_comm, void
                               int32_t gemm_sms, moe_sched_t** out);
 
 /* One step = forward and backward of both micro-batches mb[0], mb[1] (each with
- * its own buffers and workspace; weights may be shared, weight gradients must
- * not be). overlap = 0: every phase on stream_comm in the order F0 F1 B0 B1.
+ * its own buffers and workspace; weights may be shared, weight gradients, and
+ * the fp32 main gradients under MOE_FLAG_WGRAD_ACCUM_FP32, must not be, so
+ * that the order of the fp32 additions does not depend on the schedule).
+ * overlap = 0: every phase on stream_comm in the order F0 F1 B0 B1.
  * overlap = 1: phases spread over the two streams so one micro-batch's
  * dispatch/combine runs beside the other's GEMMs, ordered by events on data
  * dependencies only. defer_wgrad = 1: micro-batch 1's wgrad is not run in this

@@ -41,6 +41,9 @@ notes):
      expert path's plus the router's: dx = bf16(sum_j dx_perm + dz @ w_r).
   R8 stored tensors are bf16 (round to nearest even) at: a, h, o, y, d_o, da,
      dx_perm, dx, dW1, dW2. Gates, dgates, dz and dW_r are kept in high precision.
+  R9 gradient accumulation fusion (optional): the expert weight gradients, rounded
+     once to fp32, are added into fp32 main gradients with one fp32 addition per
+     element, call after call; an expert with no rows adds nothing.
 Everything else is computed in float64; ``rnd=identity`` turns the bf16 rounding
 off for the finite-difference pins.
 """
@@ -52,7 +55,7 @@ __all__ = [
     "bf16_rne", "identity", "router_logits_fp32", "router_logits_exact", "route_topk",
     "route_forced", "softmax_full", "dispatch_layout", "permute", "expert_ffn_fwd",
     "combine", "combine_bwd", "expert_ffn_bwd_dgrad", "expert_ffn_bwd_wgrad",
-    "permute_bwd", "route_bwd", "layer_forward", "layer_backward",
+    "expert_ffn_bwd_wgrad_accum", "permute_bwd", "route_bwd", "layer_forward", "layer_backward",
 ]
 
 
@@ -278,6 +281,36 @@ def expert_ffn_bwd_wgrad(x_perm, h, d_o, da, off, E: int, rnd=bf16_rne):
         dw1[e] = rnd(da[r].T @ x_perm[r])
         dw2[e] = rnd(d_o[r].T @ h[r])
     return dw1, dw2
+
+
+def expert_ffn_bwd_wgrad_accum(main_dw1, main_dw2, x_perm, h, d_o, da, off, E: int):
+    """Weight gradients added into fp32 main gradients (gradient accumulation fusion).
+
+    The skill card lists gradient_accumulation_fusion beside delay_wgrad_compute
+    (section "compatibility and constraints", and the troubleshooting table),
+    and the "1. MoE EP Overlap" note runs the backward with accumulate_grad=True,
+    which adds into the existing gradient instead of overwriting it. Reading:
+    the expert's weight gradient, computed exactly (float64) and rounded once to
+    fp32, is added to the fp32 main gradient with one fp32 addition:
+      main_dw1[e] <- fp32(main_dw1[e] + fp32(da_e^T @ x_e))
+      main_dw2[e] <- fp32(main_dw2[e] + fp32(d_o_e^T @ h_e))
+    An expert with no rows adds nothing. Returns new float32 arrays.
+    """
+    m1 = np.array(main_dw1, dtype=np.float32, copy=True)
+    m2 = np.array(main_dw2, dtype=np.float32, copy=True)
+    x_perm = np.asarray(x_perm, np.float64)
+    h = np.asarray(h, np.float64)
+    d_o = np.asarray(d_o, np.float64)
+    da = np.asarray(da, np.float64)
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        g1 = (da[lo:hi].T @ x_perm[lo:hi]).astype(np.float32)
+        g2 = (d_o[lo:hi].T @ h[lo:hi]).astype(np.float32)
+        m1[e] = m1[e] + g1  # float32 + float32: one fp32 rounding
+        m2[e] = m2[e] + g2
+    return m1, m2
 
 
 def permute_bwd(dx_perm, slot) -> np.ndarray:

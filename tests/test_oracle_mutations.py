@@ -101,3 +101,24 @@ def test_descending_logit_sum_is_caught(monkeypatch):
         return orig(np.asarray(x)[:, ::-1], np.asarray(w_r)[:, ::-1], bias)
     monkeypatch.setattr(O, "router_logits_fp32", logits)
     _fails(P.test_logit_summation_order_is_ascending_h)
+
+
+def test_wgrad_accumulation_that_overwrites_is_caught(monkeypatch):
+    """Accumulation that forgets the existing main gradient."""
+    orig = O.expert_ffn_bwd_wgrad_accum
+
+    def accum(main_dw1, main_dw2, *args):
+        return orig(np.zeros_like(main_dw1), np.zeros_like(main_dw2), *args)
+    monkeypatch.setattr(O, "expert_ffn_bwd_wgrad_accum", accum)
+    _fails(P.test_wgrad_accumulation_against_finite_differences)
+    _fails(P.test_wgrad_accumulation_adds_call_after_call)
+
+
+def test_wgrad_accumulation_with_a_sign_flip_is_caught(monkeypatch):
+    """Accumulation that subtracts the gradient."""
+    orig = O.expert_ffn_bwd_wgrad_accum
+
+    def accum(main_dw1, main_dw2, x_perm, h, d_o, da, off, E):
+        return orig(main_dw1, main_dw2, x_perm, h, -np.asarray(d_o), -np.asarray(da), off, E)
+    monkeypatch.setattr(O, "expert_ffn_bwd_wgrad_accum", accum)
+    _fails(P.test_wgrad_accumulation_against_finite_differences)

@@ -316,3 +316,75 @@ def test_logit_summation_order_is_ascending_h():
     assert O.router_logits_fp32(x, w)[0, 0] == np.float32(1.0)
     x_rev = x[:, ::-1].copy()
     assert O.router_logits_fp32(x_rev, w)[0, 0] == np.float32(1.0 + 2.0 ** -23)
+
+
+# ----------------------------------------------------------------------------- wgrad accumulation
+def _fd_grad(inp, dy, name, pos, eps=1e-6):
+    base = getattr(inp, name).to(torch.float64).clone()
+    vals = []
+    for sgn in (1.0, -1.0):
+        pert = base.clone()
+        pert[pos] += sgn * eps
+        setattr(inp, name, pert)
+        vals.append(_loss(inp, dy)[0])
+    setattr(inp, name, base)
+    return (vals[0] - vals[1]) / (2 * eps)
+
+
+def _accum_case(seed=31):
+    inp = small_inputs(T=10, H=8, E=5, k=2, F=4, seed=seed, w_std=0.5)
+    inp.w_r = inp.w_r * 4
+    fwd = O.layer_forward(inp, rnd=O.identity, exact_logits=True)
+    bwd = O.layer_backward(inp, fwd, rnd=O.identity)
+    rng = np.random.default_rng(seed)
+    m1 = rng.standard_normal(tuple(inp.w1.shape)).astype(np.float32)
+    m2 = rng.standard_normal(tuple(inp.w2.shape)).astype(np.float32)
+    args = (fwd["x_perm"], fwd["h"], bwd["d_o"], bwd["da"], fwd["off"], inp.E)
+    return inp, fwd, m1, m2, args
+
+
+def test_wgrad_accumulation_against_finite_differences():
+    """What the accumulation adds to a random fp32 main gradient is the loss's
+    gradient, by float64 central differences of the whole layer."""
+    inp, fwd, m1, m2, args = _accum_case()
+    a1, a2 = O.expert_ffn_bwd_wgrad_accum(m1, m2, *args)
+    dy = O._np(inp.dy)
+    g = np.random.default_rng(2)
+    for name, acc, main in (("w1", a1, m1), ("w2", a2, m2)):
+        for _ in range(10):
+            pos = tuple(int(g.integers(0, s)) for s in main.shape)
+            fd = _fd_grad(inp, dy, name, pos)
+            got = float(acc[pos]) - float(main[pos])
+            # two fp32 roundings of values of size |main| + |fd|
+            tol = 1e-6 * max(1.0, abs(fd)) + 2.4e-7 * (abs(float(main[pos])) + abs(fd))
+            assert abs(got - fd) <= tol, (name, pos, got, fd)
+
+
+def test_wgrad_accumulation_adds_call_after_call():
+    """Two calls add the gradient twice, each with one fp32 addition; a zero
+    main gradient takes the fp32-rounded gradient exactly."""
+    inp, fwd, m1, m2, args = _accum_case(seed=32)
+    z1, z2 = O.expert_ffn_bwd_wgrad_accum(np.zeros_like(m1), np.zeros_like(m2), *args)
+    b1, b2 = O.expert_ffn_bwd_wgrad_accum(m1, m2, *args)
+    c1, c2 = O.expert_ffn_bwd_wgrad_accum(b1, b2, *args)
+    for z, m, b, c in ((z1, m1, b1, c1), (z2, m2, b2, c2)):
+        assert z.dtype == np.float32 and c.dtype == np.float32
+        np.testing.assert_array_equal(b, (m + z).astype(np.float32))
+        np.testing.assert_array_equal(c, (b + z).astype(np.float32))
+        assert np.abs(z).max() > 0
+
+
+def test_wgrad_accumulation_leaves_empty_experts_alone():
+    inp = small_inputs(T=3, H=8, E=8, k=2, F=4, seed=33)
+    fwd = O.layer_forward(inp)
+    bwd = O.layer_backward(inp, fwd)
+    cnt = np.diff(fwd["off"])
+    assert (cnt == 0).any() and (cnt > 0).any()
+    rng = np.random.default_rng(3)
+    m1 = rng.standard_normal(tuple(inp.w1.shape)).astype(np.float32)
+    m2 = rng.standard_normal(tuple(inp.w2.shape)).astype(np.float32)
+    a1, a2 = O.expert_ffn_bwd_wgrad_accum(m1, m2, fwd["x_perm"], fwd["h"], bwd["d_o"],
+                                          bwd["da"], fwd["off"], inp.E)
+    for e in range(inp.E):
+        same = np.array_equal(a1[e], m1[e]) and np.array_equal(a2[e], m2[e])
+        assert same == (cnt[e] == 0), e
