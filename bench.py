@@ -388,6 +388,29 @@ def run_ours(args, rank, world, local):
     pc_ms = sum(agg[n][1] for n in pc_names) / args.steps
     pc_bytes = sum(algo[n][0] + algo[n][1] for n in pc_names)
 
+    # ---- the same step replayed from one captured CUDA graph
+    graph = None
+    if not args.no_graph:
+        gr = moe.Graph(d, b, moe.GRAPH_LAYER_STEP, st)
+        for _ in range(args.warmup):
+            gr.replay(st)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(st)
+        for _ in range(args.steps):
+            gr.replay(st)
+        g1.record(st)
+        torch.cuda.synchronize(dev)
+        gms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world)
+        status = moe.moe_device_status(d, b.ws, st)
+        if status != moe.MOE_OK:
+            raise RuntimeError(f"device status {status}: {moe.lib().moe_last_error()}")
+        graph = {"ms_per_step": round(gms, 4), "value": round(world * inp.T / (gms / 1e3), 1),
+                 "unit": "tokens/s", "kernels_per_step": gr.kernels,
+                 "note": "moe_graph_capture(MOE_GRAPH_LAYER_STEP) replayed; same work as value"}
+        gr.close()
+
     # ---- the weight gradients added into fp32 main gradients (gradient
     # accumulation fusion), timed on their own on the step's saved tensors: not
     # part of the step above, which stores bf16 weight gradients
@@ -451,6 +474,8 @@ def run_ours(args, rank, world, local):
         "grouped_gemm_TFLOP_s": round(gemm_fl / (gemm_ms * 1e-3) / 1e12, 1) if gemm_ms else None,
         "kernels": kernels,
     }
+    if graph is not None:
+        out["graph_step"] = graph
     if accum is not None:
         out["wgrad_accum_fp32"] = {"note": "weight gradients added into fp32 main gradients, "
                                            "timed separately; not in value",
@@ -561,6 +586,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_30b_a3b_balanced")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the timing of the step replayed from a CUDA graph")
     ap.add_argument("--no-accum", action="store_true",
                     help="skip the separate timing of the fp32-accumulating weight gradients")
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)

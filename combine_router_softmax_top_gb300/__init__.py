@@ -22,6 +22,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "moe.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(5)
 ROUTE_SOFTMAX_TOPK, ROUTE_FORCED_BALANCED = 0, 1
+GRAPH_ROUTER_PREPROCESS, GRAPH_LAYER_FORWARD, GRAPH_LAYER_STEP = 0, 1, 2
 FLAG_WGRAD_ACCUM_FP32 = 1  # MOE_FLAG_WGRAD_ACCUM_FP32: add wgrad into fp32 main gradients
 PHASES = ("dispatch", "ffn_fwd", "combine", "combine_bwd", "dgrad", "dispatch_bwd", "wgrad")
 
@@ -97,6 +98,10 @@ _SIGS = {
     "moe_layer_forward": ([_DP, ctypes.POINTER(MbBufs), _VP], _I32),
     "moe_layer_backward": ([_DP, ctypes.POINTER(MbBufs), _I32, _VP], _I32),
     "moe_layer_step_host": ([_DP, ctypes.POINTER(MbBufs), _VP, _VP, _VP, _VP, _VP], _I32),
+    "moe_graph_capture": ([_DP, ctypes.POINTER(MbBufs), _I32, _VP, ctypes.POINTER(_VP)], _I32),
+    "moe_graph_launch": ([_VP, _VP], _I32),
+    "moe_graph_kernel_count": ([_VP], _I32),
+    "moe_graph_destroy": ([_VP], None),
     "moe_sched_create": ([_DP, _VP, _VP, _I32, ctypes.POINTER(_VP)], _I32),
     "moe_sched_step": ([_VP, ctypes.POINTER(MbBufs), _I32, _I32], _I32),
     "moe_sched_flush": ([_VP], _I32),
@@ -326,6 +331,34 @@ class LayerBuffers:
             s.ws_bytes = self.ws.numel()
             self._struct = s
         return self._struct
+
+
+# ----------------------------------------------------------------------------- graphs
+class Graph:
+    """A captured CUDA graph of one scope of the layer on fixed buffers
+    (moe_graph_capture); replay() enqueues it. The buffers must outlive it."""
+
+    def __init__(self, desc: LayerDesc, bufs: "LayerBuffers", scope: int, stream):
+        self._h = ctypes.c_void_p()
+        self.desc, self.bufs = desc, bufs
+        self._struct = bufs.struct()
+        _check(lib().moe_graph_capture(_d(desc), ctypes.byref(self._struct), scope, _s(stream),
+                                       ctypes.byref(self._h)), "moe_graph_capture")
+        self.kernels = lib().moe_graph_kernel_count(self._h)
+
+    def replay(self, stream=None):
+        _check(lib().moe_graph_launch(self._h, _s(stream)), "moe_graph_launch")
+
+    def close(self):
+        if self._h:
+            lib().moe_graph_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # ----------------------------------------------------------------------------- scheduler

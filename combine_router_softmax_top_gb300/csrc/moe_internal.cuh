@@ -55,6 +55,11 @@ class LaunchScope {
   int rec_;
 };
 
+// True while moe_profile_start() has per-launch timing on.
+bool profiling_active();
+// Adds n (may be negative) to the count moe_kernel_launches() returns.
+void count_launches(long long n);
+
 // ---------------------------------------------------------------- errors
 void set_error(const char* fmt, ...);
 moe_status_t check_launch(const char* what);

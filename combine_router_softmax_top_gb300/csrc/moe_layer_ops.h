@@ -7,6 +7,10 @@
 namespace moe {
 
 moe_status_t validate(const moe_layer_desc_t* d);
+// The current device's library-owned helper streams (copy stream, backward
+// side stream), created on first use; NULL (with an error message) on failure.
+struct CopyLane;
+CopyLane* copy_lane();
 moe_status_t check_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, bool bwd);
 
 // route + dispatch layout + permute

@@ -45,6 +45,15 @@ LaunchScope::LaunchScope(int kernel, cudaStream_t st) : kernel_(kernel), st_(st)
   g_recs.push_back(r);
 }
 
+bool profiling_active() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_on;
+}
+
+void count_launches(long long n) {
+  g_launches.fetch_add(static_cast<unsigned long long>(n), std::memory_order_relaxed);
+}
+
 LaunchScope::~LaunchScope() {
   if (rec_ < 0) return;
   std::lock_guard<std::mutex> lk(g_mu);

@@ -108,7 +108,8 @@ moe_status_t moe_device_status(const moe_layer_desc_t* d, void* ws, void* stream
 
 /* ------------------------------------------------------------------ diagnostics */
 
-/* Number of kernels this library has launched in the process so far. */
+/* Number of kernels this library has launched in the process so far (a graph
+ * replay counts its kernel nodes; a capture counts nothing). */
 uint64_t moe_kernel_launches(void);
 
 /* Name of kernel id `kernel` as reported by moe_profile_stop ("" if unknown). */
@@ -314,6 +315,44 @@ moe_status_t moe_layer_backward(const moe_layer_desc_t* d, const moe_mb_bufs_t* 
 moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
                                  const moe_bf16* host_x, const moe_bf16* host_dy,
                                  moe_bf16* host_y, moe_bf16* host_dx, void* stream);
+
+/* ------------------------------------------------------------------ CUDA graphs */
+
+/* Capture scopes. The skill card's production benchmark (section "HybridEP
+ * production benchmark") runs the router and the dispatch preprocessing under
+ * CUDA graphs (Transformer Engine scopes moe_router + moe_preprocess);
+ * MOE_GRAPH_ROUTER_PREPROCESS is that scope. The wider scopes put a whole
+ * forward, or forward + backward, into one graph launch. */
+typedef enum {
+  MOE_GRAPH_ROUTER_PREPROCESS = 0, /* route + dispatch layout + permute          */
+  MOE_GRAPH_LAYER_FORWARD = 1,     /* moe_layer_forward                          */
+  MOE_GRAPH_LAYER_STEP = 2         /* moe_layer_forward + moe_layer_backward
+                                      (with wgrad, as d->flags selects)          */
+} moe_graph_scope_t;
+
+typedef struct moe_graph moe_graph_t;
+
+/* Captures the calls of `scope` on buffers b into a CUDA graph and instantiates
+ * it. Nothing runs during the capture. `stream` must be a caller-created stream
+ * (not a default stream), not already capturing, and per-launch profiling
+ * (moe_profile_start) must be off. The graph keeps every device pointer of b,
+ * the layer shape and d->flags as they were at capture: a replay reads and
+ * writes the same buffers, so new inputs are copied into them before a replay.
+ * The backward's side-stream fork/join becomes graph edges. Allocates the
+ * graph (host and driver memory), which moe_graph_destroy frees. *out is NULL
+ * on error. */
+moe_status_t moe_graph_capture(const moe_layer_desc_t* d, const moe_mb_bufs_t* b, int32_t scope,
+                               void* stream, moe_graph_t** out);
+
+/* Enqueues one replay of the graph on `stream` (any stream of the device it
+ * was captured on). Replays on one stream run in order. */
+moe_status_t moe_graph_launch(moe_graph_t* g, void* stream);
+
+/* Kernel nodes in the graph (moe_kernel_launches() grows by this per replay). */
+int32_t moe_graph_kernel_count(const moe_graph_t* g);
+
+/* Frees the graph; the caller makes sure no replay is still running. */
+void moe_graph_destroy(moe_graph_t* g);
 
 /* ------------------------------------------------------------------ two-stream scheduler */
 
