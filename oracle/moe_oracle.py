@@ -41,9 +41,9 @@ notes):
      expert path's plus the router's: dx = bf16(sum_j dx_perm + dz @ w_r).
   R8 stored tensors are bf16 (round to nearest even) at: a, h, o, y, d_o, da,
      dx_perm, dx, dW1, dW2. Gates, dgates, dz and dW_r are kept in high precision.
-  R9 gradient accumulation fusion (optional): the expert weight gradients, rounded
-     once to fp32, are added into fp32 main gradients with one fp32 addition per
-     element, call after call; an expert with no rows adds nothing.
+  R13 gradient accumulation fusion (optional): the expert weight gradients, rounded
+      once to fp32, are added into fp32 main gradients with one fp32 addition per
+      element, call after call; an expert with no rows adds nothing.
 Everything else is computed in float64; ``rnd=identity`` turns the bf16 rounding
 off for the finite-difference pins.
 """
