@@ -67,6 +67,11 @@ def algorithmic(d) -> dict:
         "route_logits": (T * H * b2 + E * H * b2,
                          T * E * b4 + (2 * N * b4 if fused_topk else 0), 2.0 * T * H * E),
         "route_topk": (T * E * b4, 2 * N * b4, 0.0),
+        # route + layout + permute in one launch: x and w_r read once; logits,
+        # idx, gates, slot, row_src and x_perm written once
+        "dispatch_fused": (T * H * b2 + E * H * b2,
+                           T * E * b4 + 4 * N * b4 + N * H * b2 + (2 * E + 2) * b4,
+                           2.0 * T * H * E),
         "layout_count": (N * b4, 0, 0.0),
         "layout_assign": (N * b4, 2 * N * b4, 0.0),
         "permute": (T * H * b2 + N * b4, N * H * b2, 0.0),

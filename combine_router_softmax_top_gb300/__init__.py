@@ -86,6 +86,7 @@ _SIGS = {
     "moe_dispatch_layout": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_dispatch_layout_static": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
     "moe_permute": ([_DP, _VP, _VP, _VP, _VP], _I32),
+    "moe_dispatch_fused": ([_DP] + [_VP] * 14 + [_SZ, _VP], _I32),
     "moe_expert_ffn_fwd": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_combine": ([_DP, _VP, _VP, _VP, _VP, _VP], _I32),
     "moe_combine_bwd": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
@@ -206,6 +207,15 @@ def moe_dispatch_layout_static(desc, idx, cnt, off, slot, row_src, cnt_re, rank_
 
 def moe_permute(desc, x, row_src, x_perm, stream=None):
     _check(lib().moe_permute(_d(desc), _p(x), _p(row_src), _p(x_perm), _s(stream)), "moe_permute")
+
+
+def moe_dispatch_fused(desc, x, w_r, bias, logits, idx, gates, cnt, off, slot, row_src, cnt_re,
+                       rank_off, x_perm, ws, stream=None):
+    _check(lib().moe_dispatch_fused(_d(desc), _p(x), _p(w_r), _p(bias), _p(logits), _p(idx),
+                                    _p(gates), _p(cnt), _p(off), _p(slot), _p(row_src),
+                                    _p(cnt_re), _p(rank_off), _p(x_perm), _p(ws),
+                                    ws.numel() * ws.element_size(), _s(stream)),
+           "moe_dispatch_fused")
 
 
 def moe_expert_ffn_fwd(desc, x_perm, off, w1, w2, a, h, o, ws, stream=None):

@@ -98,6 +98,10 @@ WsLayout ws_layout(const moe_layer_desc_t& d) {
   o = align256(o + (size_t)chunks * d.H * sizeof(float));
   w.dep = o;
   o = align256(o + (size_t)d.E * sizeof(int));
+  w.fhist = o;  // fused dispatch: per-tile expert counts (tiles of >= 4 tokens) + totals
+  o = align256(o + ((size_t)(d.T + 3) / 4 + 1) * d.E * sizeof(int));
+  w.bar = o;
+  o = align256(o + sizeof(int));
   w.total = o;
   return w;
 }
@@ -255,13 +259,30 @@ moe_status_t op_route_bwd(const moe_layer_desc_t& d, const float* dgates, const 
                           status_of(ws), st);
 }
 
+// Route + dispatch layout + permute: one cooperative launch when the block
+// routes every expert of its tokens (E <= 128), else the three launches.
+moe_status_t op_dispatch_all(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
+                             const float* bias, float* logits, int32_t* idx, float* gates,
+                             int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
+                             int32_t* cnt_re, int32_t* rank_off, bf16* x_perm, void* ws,
+                             cudaStream_t st) {
+  if (d.T > 0 && d.E <= 128) {
+    const WsLayout w = ws_layout(d);
+    float* z = logits ? logits : ws_at<float>(ws, w.logits);
+    return launch_dispatch_fused(d, x, w_r, bias, z, idx, gates, cnt, off, slot, row_src, cnt_re,
+                                 rank_off, x_perm, ws_at<int>(ws, w.fhist), ws_at<int>(ws, w.bar),
+                                 status_of(ws), st);
+  }
+  MOE_CHECK(op_route(d, x, w_r, bias, logits, idx, gates, ws, st));
+  MOE_CHECK(op_layout(d, idx, cnt, off, slot, row_src, cnt_re, rank_off, ws, st));
+  return launch_permute(d, x, row_src, x_perm, st);
+}
+
 moe_status_t op_dispatch(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st) {
-  const bf16* x = reinterpret_cast<const bf16*>(b->x);
-  MOE_CHECK(op_route(d, x, reinterpret_cast<const bf16*>(b->w_r), b->bias, b->logits, b->idx,
-                     b->gates, b->ws, st));
-  MOE_CHECK(op_layout(d, b->idx, b->cnt, b->off, b->slot, b->row_src, b->cnt_re, b->rank_off,
-                      b->ws, st));
-  return launch_permute(d, x, b->row_src, reinterpret_cast<bf16*>(b->x_perm), st);
+  return op_dispatch_all(d, reinterpret_cast<const bf16*>(b->x),
+                         reinterpret_cast<const bf16*>(b->w_r), b->bias, b->logits, b->idx,
+                         b->gates, b->cnt, b->off, b->slot, b->row_src, b->cnt_re, b->rank_off,
+                         reinterpret_cast<bf16*>(b->x_perm), b->ws, st);
 }
 
 moe_status_t op_ffn_fwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
@@ -383,6 +404,20 @@ moe_status_t moe_route(const moe_layer_desc_t* d, const moe_bf16* x, const moe_b
   MOE_PTR(x); MOE_PTR(w_r); MOE_PTR_OPT(bias); MOE_PTR_OPT(logits); MOE_PTR(idx); MOE_PTR(gates);
   MOE_CHECK(check_ws(*d, ws, ws_bytes));
   return op_route(*d, BF(x), BF(w_r), bias, logits, idx, gates, ws, S(stream));
+}
+
+moe_status_t moe_dispatch_fused(const moe_layer_desc_t* d, const moe_bf16* x, const moe_bf16* w_r,
+                                const float* bias, float* logits, int32_t* idx, float* gates,
+                                int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
+                                int32_t* cnt_re, int32_t* rank_off, moe_bf16* x_perm, void* ws,
+                                size_t ws_bytes, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_PTR(x); MOE_PTR(w_r); MOE_PTR_OPT(bias); MOE_PTR_OPT(logits); MOE_PTR(idx); MOE_PTR(gates);
+  MOE_PTR(cnt); MOE_PTR(off); MOE_PTR(slot); MOE_PTR(row_src); MOE_PTR(cnt_re);
+  MOE_PTR(rank_off); MOE_PTR(x_perm);
+  MOE_CHECK(check_ws(*d, ws, ws_bytes));
+  return op_dispatch_all(*d, BF(x), BF(w_r), bias, logits, idx, gates, cnt, off, slot, row_src,
+                         cnt_re, rank_off, BFW(x_perm), ws, S(stream));
 }
 
 moe_status_t moe_dispatch_layout(const moe_layer_desc_t* d, const int32_t* idx, int32_t* cnt,

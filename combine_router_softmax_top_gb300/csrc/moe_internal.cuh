@@ -26,7 +26,7 @@ constexpr int kLayoutTokensPerBlock = 256;
 constexpr int kRouteBwdRowsPerChunk = 64;
 
 struct WsLayout {
-  size_t status, logits, hist, dz, dwr_part, dep, total;
+  size_t status, logits, hist, dz, dwr_part, dep, fhist, bar, total;
 };
 WsLayout ws_layout(const moe_layer_desc_t& d);
 
@@ -37,7 +37,7 @@ enum KernelId {
   K_ROUTE_LOGITS = 0, K_ROUTE_TOPK, K_LAYOUT_COUNT, K_LAYOUT_ASSIGN, K_PERMUTE, K_COMBINE,
   K_COMBINE_BWD, K_PERMUTE_BWD, K_ROUTE_BWD_DX, K_ROUTE_BWD_DWR_PARTIAL, K_ROUTE_BWD_DWR_REDUCE,
   K_GEMM_FC1_FWD, K_GEMM_FC2_FWD, K_GEMM_FC2_DGRAD, K_GEMM_FC1_DGRAD, K_GEMM_WGRAD_W1,
-  K_GEMM_WGRAD_W2, K_DISPATCH_BWD, K_GEMM_FFN_FWD, K_GEMM_FFN_DGRAD, K_NUM
+  K_GEMM_WGRAD_W2, K_DISPATCH_BWD, K_GEMM_FFN_FWD, K_GEMM_FFN_DGRAD, K_DISPATCH_FUSED, K_NUM
 };
 
 // Wraps one kernel launch: counts it and, while profiling is on, brackets it
@@ -102,6 +102,14 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
                           const float* bias, float* logits, int32_t* idx, float* gates,
                           int* status, cudaStream_t st);
+// Route + dispatch layout + permute in one cooperative launch (E <= 128, T > 0;
+// MOE_ERR_UNSUPPORTED otherwise). fhist: ws area of (ceil(T/4) + 1) * E ints;
+// bar: one int, zeroed by the launcher.
+moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
+                                   const float* bias, float* z, int32_t* idx, float* gates,
+                                   int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
+                                   int32_t* cnt_re, int32_t* rank_off, bf16* x_perm, int* fhist,
+                                   int* bar, int* status, cudaStream_t st);
 moe_status_t launch_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_t* cnt,
                            int32_t* off, int32_t* slot, int32_t* row_src, int32_t* cnt_re,
                            int32_t* rank_off, int* hist, int* status, cudaStream_t st);

@@ -7,6 +7,8 @@
 // moe_router + moe_preprocess). Its arithmetic is the layer definition in moe.h.
 #include <float.h>
 
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -36,7 +38,7 @@ __device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
 template <int EPL>
 __device__ __forceinline__ void topk_row(const float* zt, int t, int32_t* __restrict__ idx,
                                          float* __restrict__ gates, int E, int k, int forced,
-                                         int lane) {
+                                         int lane, int* s_hist = nullptr) {
   float v[EPL];
   float m = -FLT_MAX;
 #pragma unroll
@@ -97,6 +99,7 @@ __device__ __forceinline__ void topk_row(const float* zt, int t, int32_t* __rest
   if (lane < k) {
     idx[(size_t)t * k + lane] = my_e;
     gates[(size_t)t * k + lane] = my_p / ps;
+    if (s_hist && (unsigned)my_e < (unsigned)E) atomicAdd(s_hist + my_e, 1);
   }
 }
 
@@ -154,12 +157,21 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Shared memory of one tile: the operand ring (and, with FUSE, the parked logits).
+template <int TPL>
+constexpr size_t route_tile_smem() {
+  return (size_t)kRouteStages * (4 * TPL + kRouteEb) * kRoutePitchB;
+}
+
+// One tile: tokens t0.. (4*TPL of them) x experts e0..e0+127, by the whole block.
 template <int TPL, bool FUSE>
-__global__ void __launch_bounds__(kRouteNw * 32, 1) route_logits_kernel(
-    const bf16* __restrict__ x, const bf16* __restrict__ w_r, const float* __restrict__ bias,
-    float* __restrict__ z, int32_t* __restrict__ idx, float* __restrict__ gates, int T, int H,
-    int E, int k, int forced) {
-  pdl_wait();
+__device__ __forceinline__ void route_tile(uint8_t* route_smem, int t0, int e0,
+                                           const bf16* __restrict__ x,
+                                           const bf16* __restrict__ w_r,
+                                           const float* __restrict__ bias, float* __restrict__ z,
+                                           int32_t* __restrict__ idx, float* __restrict__ gates,
+                                           int T, int H, int E, int k, int forced,
+                                           int* s_hist = nullptr) {
   constexpr int NW = kRouteNw, NT = NW * 32;
   constexpr int TB = 4 * TPL;
   constexpr int EW = kRouteEb / NW;  // experts per warp
@@ -168,11 +180,9 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) route_logits_kernel(
   constexpr int STAGE_B = ROWS * kRoutePitchB;
   constexpr int PIECES = ROWS * (kRouteHc / 8);  // 16-byte pieces per chunk
   static_assert(EPL >= 1, "route tile");
-  extern __shared__ __align__(16) uint8_t route_smem[];
+  static_assert(STAGE_B * kRouteStages == route_tile_smem<TPL>(), "route tile smem");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tg = lane >> 3, eg = lane & 7;
-  const int t0 = blockIdx.x * TB;
-  const int e0 = blockIdx.y * kRouteEb;
   const int nchunks = H / kRouteHc;
 
   // rows 0..TB-1 of a stage: x (tokens, clamped to T-1); rows TB..: w_r
@@ -265,8 +275,21 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) route_logits_kernel(
   if (FUSE) {
     __syncthreads();
     for (int tl = warp; tl < TB; tl += NW)
-      if (t0 + tl < T) topk_row<kRouteEb / 32>(zs + tl * kRouteEb, t0 + tl, idx, gates, E, k, forced, lane);
+      if (t0 + tl < T)
+        topk_row<kRouteEb / 32>(zs + tl * kRouteEb, t0 + tl, idx, gates, E, k, forced, lane,
+                                s_hist);
   }
+}
+
+template <int TPL, bool FUSE>
+__global__ void __launch_bounds__(kRouteNw * 32, 1) route_logits_kernel(
+    const bf16* __restrict__ x, const bf16* __restrict__ w_r, const float* __restrict__ bias,
+    float* __restrict__ z, int32_t* __restrict__ idx, float* __restrict__ gates, int T, int H,
+    int E, int k, int forced) {
+  pdl_wait();
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  route_tile<TPL, FUSE>(route_smem, blockIdx.x * 4 * TPL, blockIdx.y * kRouteEb, x, w_r, bias, z,
+                        idx, gates, T, H, E, k, forced);
 }
 
 // One warp per token, logits from global memory (E > 128).
@@ -280,6 +303,224 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   topk_row<EPL>(z + (size_t)t * E, t, idx, gates, E, k, forced, lane);
+}
+
+// ------------------------------------------------------------------ fused dispatch
+// Routing, dispatch layout and permute of every token in one cooperative
+// persistent launch (E <= 128), the fused dispatch the skill card mentions
+// (moe_permute_fusion, "HybridEP production benchmark" and the dispatcher
+// table). Tiles of 4*TPL tokens (<= 32, so one warp holds a tile's tokens) go
+// to blocks round-robin in token order; fhist[tile][e] counts tile entries
+// per expert.
+//   1. each block routes its tiles (route_tile) and writes their histograms;
+//   -- grid barrier --
+//   2. block b turns column e = b, b+G, .. of fhist into exclusive prefixes
+//      over tiles, in place, and writes the column total to tot[e];
+//   -- grid barrier --
+//   3. every block scans tot into the expert offsets (block 0 writes cnt, off,
+//      cnt_re, rank_off); slot of entry (t, j) with e = idx[t][j] is
+//      off[e] + fhist[tile][e] + (tokens of the tile before t that chose e),
+//      which is the layout's stable token order; the block then copies each
+//      of its tokens' x rows to their k slots of x_perm.
+// The results are those of route + layout + permute run separately. The
+// launch is cooperative, so every block is resident and the barrier waits
+// end; each is still bounded, and on expiry the block records the site and
+// returns.
+constexpr uint64_t kDispatchWaitNs = 2000000000ull;
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// All blocks of the grid arrive; true once every block has (false on timeout).
+__device__ __forceinline__ bool grid_barrier(int* bar, int target, int* status, int site,
+                                             int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    __threadfence();
+    atomicAdd(bar, 1);
+    const uint64_t t0 = global_ns();
+    while (ld_acquire_gpu(bar) < target) {
+      if (global_ns() - t0 > kDispatchWaitNs) {
+        atomicExch(status + ST_TIMEOUT, site);
+        ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+// Shared memory of the fused dispatch beyond the route tile's.
+constexpr size_t kFusedExtraInts = 3 * kRouteEb + 32 * 32 + 4;
+
+template <int TPL>
+__global__ void __launch_bounds__(kRouteNw * 32, 1) dispatch_fused_kernel(
+    const bf16* __restrict__ x, const bf16* __restrict__ w_r, const float* __restrict__ bias,
+    float* __restrict__ z, int32_t* __restrict__ idx, float* __restrict__ gates,
+    int32_t* __restrict__ cnt, int32_t* __restrict__ off, int32_t* __restrict__ slot,
+    int32_t* __restrict__ row_src, int32_t* __restrict__ cnt_re, int32_t* __restrict__ rank_off,
+    bf16* __restrict__ x_perm, int* __restrict__ fhist, int* __restrict__ bar,
+    int* __restrict__ status, int T, int H, int E, int k, int R, int forced) {
+  pdl_wait();
+  constexpr int TB = 4 * TPL;
+  static_assert(TB <= 32, "one warp holds a tile's tokens");
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  int* s_hist = reinterpret_cast<int*>(route_smem + route_tile_smem<TPL>());  // [128]
+  uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_hist + kRouteEb);        // [128]
+  int* s_base = reinterpret_cast<int*>(s_mask + kRouteEb);                  // [128]
+  int* s_ent = s_base + kRouteEb;                                           // [TB * k <= 1024]
+  int* s_flag = s_ent + 32 * 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = (T + TB - 1) / TB;
+  int* tot = fhist + (size_t)ntiles * E;
+
+  // 1. route, counting each tile's entries per expert as the top-k picks them
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+    // (route_tile synchronises the block before its top-k step)
+    route_tile<TPL, true>(route_smem, tile * TB, 0, x, w_r, bias, z, idx, gates, T, H, E, k,
+                          forced, s_hist);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) fhist[(size_t)tile * E + e] = s_hist[e];
+    __syncthreads();
+  }
+  if (!grid_barrier(bar, gridDim.x, status, 20, s_flag)) return;
+
+  // 2. exclusive prefix over tiles, one expert column per block and round;
+  // 8 x 32 tiles are loaded before they are scanned
+  if (warp == 0) {
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+      int carry = 0;
+      for (int b0 = 0; b0 < ntiles; b0 += 256) {
+        int c[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int b = b0 + 32 * u + lane;
+          c[u] = b < ntiles ? __ldcg(fhist + (size_t)b * E + e) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int b = b0 + 32 * u + lane;
+          int incl = c[u];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+          }
+          if (b < ntiles) fhist[(size_t)b * E + e] = carry + incl - c[u];
+          carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      if (lane == 0) tot[e] = carry;
+    }
+  }
+  if (!grid_barrier(bar, 2 * (int)gridDim.x, status, 21, s_flag)) return;
+
+  // 3. expert offsets, then slots and rows tile by tile
+  if (warp == 0) {
+    int c[kRouteEb / 32];
+#pragma unroll
+    for (int u = 0; u < kRouteEb / 32; ++u) {
+      const int e = 32 * u + lane;
+      c[u] = e < E ? __ldcg(tot + e) : 0;
+    }
+    int carry = 0;
+#pragma unroll
+    for (int u = 0; u < kRouteEb / 32; ++u) {
+      const int e = 32 * u + lane;
+      int incl = c[u];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) {
+        const int ex = carry + incl - c[u];
+        s_base[e] = ex;
+        if (blockIdx.x == 0) {
+          off[e] = ex;
+          cnt[e] = c[u];
+          cnt_re[e] = c[u];  // [R][E/R] row-major is the expert order itself
+        }
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (blockIdx.x == 0 && lane == 0) off[E] = carry;
+    if (lane == 0) *s_flag = carry;  // N
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    const int El = E / R;
+    for (int r = threadIdx.x; r <= R; r += blockDim.x)
+      rank_off[r] = r < R ? s_base[r * El] : *s_flag;
+  }
+  const int cpr = H / 8;  // 16-byte chunks per row
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int t0 = tile * TB, nt = min(TB, T - t0), nent = nt * k;
+    // the tile's routing and its entries' offsets within each expert
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      s_mask[e] = 0u;
+      s_hist[e] = __ldcg(fhist + (size_t)tile * E + e);
+    }
+    for (int i = threadIdx.x; i < nent; i += blockDim.x) s_ent[i] = idx[(size_t)t0 * k + i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < nent; i += blockDim.x) {
+      const int e = s_ent[i];
+      if ((unsigned)e < (unsigned)E) atomicOr(&s_mask[e], 1u << (i / k));
+    }
+    __syncthreads();
+    // entry i = (token t0 + i / k, choice i % k): its slot, in place of its expert
+    for (int i = threadIdx.x; i < nent; i += blockDim.x) {
+      const int e = s_ent[i];
+      int sl = -1;
+      if ((unsigned)e < (unsigned)E) {
+        sl = s_base[e] + s_hist[e] + __popc(s_mask[e] & ((1u << (i / k)) - 1u));
+        row_src[sl] = t0 * k + i;
+      } else {
+        atomicAdd(status + ST_BAD_INDEX, 1);
+      }
+      slot[(size_t)t0 * k + i] = sl;
+      s_ent[i] = sl;
+    }
+    __syncthreads();
+    // warp w copies tokens w, w + 8, ..: 4 KB of the row at a time, loaded
+    // once and stored to each of the token's k slots
+    for (int tl = warp; tl < nt; tl += kRouteNw) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t0 + tl) * H);
+      for (int c0 = 0; c0 < cpr; c0 += 256) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c = c0 + 32 * u + lane;
+          v[u] = c < cpr ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        }
+        for (int j = 0; j < k; ++j) {
+          const int sl = s_ent[tl * k + j];
+          if (sl < 0) continue;
+          uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)sl * H);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int c = c0 + 32 * u + lane;
+            if (c < cpr) __stcs(dst + c, v[u]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
 }
 
 // ------------------------------------------------------------------ backward
@@ -596,6 +837,42 @@ moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* 
   return check_launch("route_topk_kernel");
 }
 
+template <int TPL>
+cudaError_t launch_fused_t(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
+                           const float* bias, float* z, int32_t* idx, float* gates, int32_t* cnt,
+                           int32_t* off, int32_t* slot, int32_t* row_src, int32_t* cnt_re,
+                           int32_t* rank_off, bf16* x_perm, int* fhist, int* bar, int* status,
+                           cudaStream_t st) {
+  const int forced = d.mode == MOE_ROUTE_FORCED_BALANCED;
+  const size_t smem = route_tile_smem<TPL>() + kFusedExtraInts * sizeof(int);
+  static cudaError_t attr = cudaFuncSetAttribute(
+      dispatch_fused_kernel<TPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (attr != cudaSuccess) return attr;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, dispatch_fused_kernel<TPL>, kRouteNw * 32, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // every block must be resident: at most one wave
+  const int ntiles = ceil_div(d.T, 4 * TPL);
+  const int grid = std::min(ntiles, per_sm * device_sm_count());
+  e = cudaMemsetAsync(bar, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRouteNw * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dispatch_fused_kernel<TPL>, x, w_r, bias, z, idx, gates, cnt,
+                            off, slot, row_src, cnt_re, rank_off, x_perm, fhist, bar, status,
+                            d.T, d.H, d.E, d.k, d.R, forced);
+}
+
 template <bool FUSED>
 void launch_dx(const moe_layer_desc_t& d, const float* dgates, const float* gates,
                const int32_t* idx, const bf16* w_r, const float* dx32, const bf16* dx_perm,
@@ -614,6 +891,41 @@ void launch_dx(const moe_layer_desc_t& d, const float* dgates, const float* gate
   else
     launch_k(route_bwd_dx_kernel<32, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
              dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
+}
+
+moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
+                                   const float* bias, float* z, int32_t* idx, float* gates,
+                                   int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
+                                   int32_t* cnt_re, int32_t* rank_off, bf16* x_perm, int* fhist,
+                                   int* bar, int* status, cudaStream_t st) {
+  if (d.T == 0 || d.E > kRouteEb) return MOE_ERR_UNSUPPORTED;
+  // tokens per lane as for the router alone: about one wave of one block per SM
+  const int per_sm = ceil_div(d.T, 4 * device_sm_count());
+  const int tpl = per_sm < 1 ? 1 : per_sm > 7 ? 7 : per_sm;
+  cudaError_t e;
+  {
+    LaunchScope _ls(K_DISPATCH_FUSED, st);
+#define MOE_FUSED_CASE(n)                                                                     \
+  case n:                                                                                     \
+    e = launch_fused_t<n>(d, x, w_r, bias, z, idx, gates, cnt, off, slot, row_src, cnt_re,  \
+                          rank_off, x_perm, fhist, bar, status, st);                         \
+    break;
+    switch (tpl) {
+      MOE_FUSED_CASE(1)
+      MOE_FUSED_CASE(2)
+      MOE_FUSED_CASE(3)
+      MOE_FUSED_CASE(4)
+      MOE_FUSED_CASE(5)
+      MOE_FUSED_CASE(6)
+      default: MOE_FUSED_CASE(7)
+    }
+#undef MOE_FUSED_CASE
+  }
+  if (e != cudaSuccess) {
+    set_error("dispatch_fused_kernel launch: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return check_launch("dispatch_fused_kernel");
 }
 
 moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,

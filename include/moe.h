@@ -188,6 +188,26 @@ moe_status_t moe_dispatch_layout_static(const moe_layer_desc_t* d, const int32_t
 moe_status_t moe_permute(const moe_layer_desc_t* d, const moe_bf16* x, const int32_t* row_src,
                          moe_bf16* x_perm, void* stream);
 
+/* Route + dispatch layout + permute in one call, with the results of moe_route,
+ * moe_dispatch_layout and moe_permute run in that order (the same bits). With
+ * E <= 128 it is one cooperative persistent launch (the fused dispatch of the
+ * skill card: moe_permute_fusion, "HybridEP production benchmark"):
+ *   - blocks route their token tiles and count each tile's entries per expert;
+ *   - after a grid-wide barrier, each expert's counts are scanned over tiles;
+ *   - after a second barrier, every block derives the expert offsets, numbers
+ *     its own entries in token order, and copies its tokens' rows into x_perm.
+ * The barrier waits are bounded (2 s). On expiry the device status reads
+ * MOE_ERR_TIMEOUT. Every block is resident by the launch's construction. With
+ * E > 128 or T = 0 the three calls run as separate launches.
+ * x [T,H], w_r [E,H] bf16; bias [E] fp32 or NULL; logits [T,E] fp32 or NULL
+ * -> idx, gates [T,k]; cnt [E]; off [E+1]; slot [T,k]; row_src [N];
+ * cnt_re [R,E/R]; rank_off [R+1]; x_perm [N,H] bf16. */
+moe_status_t moe_dispatch_fused(const moe_layer_desc_t* d, const moe_bf16* x, const moe_bf16* w_r,
+                                const float* bias, float* logits, int32_t* idx, float* gates,
+                                int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
+                                int32_t* cnt_re, int32_t* rank_off, moe_bf16* x_perm, void* ws,
+                                size_t ws_bytes, void* stream);
+
 /* Expert FFN forward (the "mlp" phase), per expert e on its rows off[e]..off[e+1]-1:
  *   a = bf16(x_perm_e @ w1[e]^T)               [rows, 2F], fp32 accumulate
  *   h = bf16(silu(a[:, :F]) * a[:, F:])        [rows, F] (from the bf16 a)
@@ -290,7 +310,8 @@ typedef struct moe_mb_bufs {
                                        with MOE_FLAG_WGRAD_ACCUM_FP32 */
 } moe_mb_bufs_t;
 
-/* Forward: route, dispatch layout, permute, expert FFN, combine. */
+/* Forward: route, dispatch layout, permute (as moe_dispatch_fused: one launch
+ * when E <= 128), expert FFN, combine. */
 moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b, void* stream);
 
 /* Backward in the chain order combine -> experts (dgrad) -> dispatch -> router,
