@@ -48,6 +48,11 @@ CASES = {
     "max_experts": lambda: moe_synth.make_inputs(T=200, H=128, E=256, k=8, F=64, seed=26),
     # k above 16: the 32-slot variants of the combine and router backward
     "large_k": lambda: moe_synth.make_inputs(T=150, H=192, E=32, k=20, F=64, seed=27),
+    # the largest hidden size the header allows: 256 K stages in FC1 and the
+    # router, 256 column slices in the dispatch backward, 32 KB rows
+    "max_hidden": lambda: moe_synth.make_inputs(T=48, H=16384, E=4, k=2, F=128, seed=28),
+    # the largest expert inner size: 128 FC1 column blocks, 256 K stages in FC2
+    "max_inner": lambda: moe_synth.make_inputs(T=48, H=128, E=4, k=2, F=16384, seed=29),
 }
 
 
