@@ -29,6 +29,9 @@ def test_header_declares_the_whole_path():
                  "moe_expert_ffn_bwd_wgrad", "moe_permute_bwd", "moe_route_bwd",
                  "moe_sched_create", "moe_sched_step", "moe_sched_timings", "moe_sched_destroy"):
         assert want in names
+    for want in ("moe_dispatch_fused", "moe_expert_ffn_bwd_wgrad_accum", "moe_graph_capture",
+                 "moe_graph_launch", "moe_graph_kernel_count", "moe_graph_destroy"):
+        assert want in names
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -55,6 +58,8 @@ def test_library_is_in_tree_and_sm103a(L):
     (dict(T=16, H=128, E=300, k=2, F=256), moe.MOE_ERR_UNSUPPORTED),    # E > 256
     (dict(T=16, H=128, E=64, k=33, F=256), moe.MOE_ERR_UNSUPPORTED),    # k > 32
     (dict(T=16, H=128, E=8, k=2, F=256, mode=7), moe.MOE_ERR_INVALID_ARG),
+    (dict(T=16, H=128, E=8, k=2, F=256, flags=moe.FLAG_WGRAD_ACCUM_FP32), moe.MOE_OK),
+    (dict(T=16, H=128, E=8, k=2, F=256, flags=2), moe.MOE_ERR_INVALID_ARG),  # unknown flag
 ])
 def test_descriptor_validation(L, kw, status):
     d = moe.LayerDesc.of(**kw)
@@ -91,3 +96,57 @@ def test_scheduler_needs_two_streams(L):
     st = L.moe_sched_create(ctypes.byref(d), ctypes.c_void_p(1), ctypes.c_void_p(1), 0,
                             ctypes.byref(h))
     assert st == moe.MOE_ERR_INVALID_ARG
+
+
+def _fake_bufs(d, accum=False):
+    """A buffer struct of aligned, never-dereferenced addresses (host checks only)."""
+    b = moe.MbBufs()
+    for n in moe._MB_FIELDS + moe._MB_FIELDS_TAIL:
+        setattr(b, n, 4096)
+    if not accum:
+        b.main_dw1 = b.main_dw2 = None
+    b.ws_bytes = moe.moe_workspace_size(d)
+    return b
+
+
+def test_new_entry_points_check_arguments_before_any_launch(L):
+    d = moe.LayerDesc.of(T=16, H=128, E=8, k=2, F=256)
+    p = ctypes.c_void_p(4096)
+    ws = moe.moe_workspace_size(d)
+    # fused dispatch: a NULL input
+    st = L.moe_dispatch_fused(ctypes.byref(d), None, p, None, None, p, p, p, p, p, p, p, p, p, p,
+                              ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"NULL" in L.moe_last_error()
+    # accumulating wgrad: a NULL main gradient, then a misaligned one
+    st = L.moe_expert_ffn_bwd_wgrad_accum(ctypes.byref(d), p, p, p, p, p, None, p, p, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"NULL" in L.moe_last_error()
+    st = L.moe_expert_ffn_bwd_wgrad_accum(ctypes.byref(d), p, p, p, p, p, ctypes.c_void_p(4100),
+                                          p, p, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"aligned" in L.moe_last_error()
+
+
+def test_accumulating_layer_needs_main_gradients_not_bf16_ones(L):
+    d = moe.LayerDesc.of(T=16, H=128, E=8, k=2, F=256, flags=moe.FLAG_WGRAD_ACCUM_FP32)
+    b = _fake_bufs(d, accum=True)
+    b.dw1 = b.dw2 = None  # unused when accumulating: NULL is allowed
+    b.main_dw1 = None     # but the main gradients are required
+    st = L.moe_layer_backward(ctypes.byref(d), ctypes.byref(b), 1, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"NULL" in L.moe_last_error()
+
+
+def test_graph_capture_checks_arguments_before_any_cuda_call(L):
+    d = moe.LayerDesc.of(T=16, H=128, E=8, k=2, F=256)
+    b = _fake_bufs(d)
+    h = ctypes.c_void_p()
+    st = L.moe_graph_capture(ctypes.byref(d), ctypes.byref(b), moe.GRAPH_LAYER_STEP,
+                             ctypes.c_void_p(64), None)
+    assert st == moe.MOE_ERR_INVALID_ARG  # no place for the result
+    st = L.moe_graph_capture(ctypes.byref(d), ctypes.byref(b), 9, ctypes.c_void_p(64),
+                             ctypes.byref(h))
+    assert st == moe.MOE_ERR_INVALID_ARG and b"scope" in L.moe_last_error() and not h.value
+    st = L.moe_graph_capture(ctypes.byref(d), ctypes.byref(b), moe.GRAPH_LAYER_STEP, None,
+                             ctypes.byref(h))
+    assert st == moe.MOE_ERR_INVALID_ARG and b"default stream" in L.moe_last_error()
+    assert L.moe_graph_launch(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_graph_kernel_count(None) == 0
+    L.moe_graph_destroy(None)  # a no-op
