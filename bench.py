@@ -135,8 +135,8 @@ def accum_algorithmic(d) -> dict:
     T, H, E, k, F = d["T"], d["H"], d["E"], d["k"], d["F"]
     N = T * k
     w1, w2 = E * 2 * F * H * 4, E * H * F * 4
-    return {"gemm_wgrad_w1": (N * 2 * F * 2 + N * H * 2 + w1, w1, 2.0 * N * 2 * F * H),
-            "gemm_wgrad_w2": (N * H * 2 + N * F * 2 + w2, w2, 2.0 * N * H * F)}
+    return {"gemm_wgrad_w1_accum": (N * 2 * F * 2 + N * H * 2 + w1, w1, 2.0 * N * 2 * F * H),
+            "gemm_wgrad_w2_accum": (N * H * 2 + N * F * 2 + w2, w2, 2.0 * N * H * F)}
 
 
 def hbm_write_gbs(dev) -> float:

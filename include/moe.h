@@ -122,7 +122,10 @@ typedef struct moe_kernel_time {
 } moe_kernel_time_t;
 
 /* Starts recording per-launch durations of the next `capacity` launches (on any
- * stream). Creates CUDA events on first use; allocates no device memory. */
+ * stream). Creates CUDA events on first use; allocates no device memory.
+ * While recording, moe_layer_backward runs the weight gradients in order on
+ * its `stream` after the dispatch backward, instead of beside it on the side
+ * stream, so that each launch is timed alone. */
 moe_status_t moe_profile_start(int32_t capacity);
 
 /* Stops recording, waits for the recorded events and returns up to cap entries
