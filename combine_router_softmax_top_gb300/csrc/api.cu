@@ -360,7 +360,7 @@ using namespace moe;
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 1; }
+int32_t moe_abi_version(void) { return 2; }  // 2: moe_mb_bufs_t gained main_dw1, main_dw2
 
 const char* moe_last_error(void) { return g_err; }
 

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_library_is_in_tree_and_sm103a(L):
     assert os.path.dirname(moe.LIB_PATH) == os.path.dirname(os.path.abspath(moe.__file__))
-    assert L.moe_abi_version() == 1
+    assert L.moe_abi_version() == 2
     assert "compute_103a,code=sm_103a" in " ".join(build.ARCH)
 
 
