@@ -856,14 +856,19 @@ cudaError_t launch_fused_t(const moe_layer_desc_t& d, const bf16* x, const bf16*
                            cudaStream_t st) {
   const int forced = d.mode == MOE_ROUTE_FORCED_BALANCED;
   const size_t smem = route_tile_smem<TPL, HC>() + kFusedExtraInts * sizeof(int);
-  static cudaError_t attr = cudaFuncSetAttribute(
-      dispatch_fused_kernel<TPL, HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // resident blocks per SM, looked up once (with the shared-memory attribute)
+  static int per_sm = 0;
+  static cudaError_t attr = [smem] {
+    cudaError_t a = cudaFuncSetAttribute(dispatch_fused_kernel<TPL, HC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (a == cudaSuccess)
+      a = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fused_kernel<TPL, HC>,
+                                                        kRouteNw * 32, smem);
+    return a;
+  }();
   if (attr != cudaSuccess) return attr;
-  int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, dispatch_fused_kernel<TPL, HC>, kRouteNw * 32, smem);
-  if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  cudaError_t e;
   // every block must be resident: at most one wave
   const int ntiles = ceil_div(d.T, 4 * TPL);
   const int grid = std::min(ntiles, per_sm * device_sm_count());
