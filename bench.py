@@ -504,7 +504,8 @@ def run_reference(args, rank, world):
     from oracle import moe_oracle as O
     Ts = args.ref_sample_tokens
     inp = moe_synth.workload(args.workload, T=Ts)
-    shape = inp.shape_dict()
+    # the workload's own shape: each timed step is a bounded sample of its tokens
+    full_shape = dict(inp.shape_dict(), T=moe_synth.WORKLOADS[args.workload]["T"])
 
     def step():
         fwd = O.layer_forward(inp)
@@ -521,8 +522,9 @@ def run_reference(args, rank, world):
           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
           "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-          "config": {"workload": args.workload, **shape, "T_full": moe_synth.WORKLOADS[args.workload]["T"],
-                     "parallelism": "single process"},
+          "config": {"workload": args.workload, **full_shape, "steps_per_call": "fwd+dgrad+wgrad",
+                     "parallelism": "single process on the host cores",
+                     "sample_tokens_per_step": Ts},
           "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": cpu_cores(),
                            "kind": "oracle",
                            "sample": f"first {Ts} tokens of the workload per step"},
