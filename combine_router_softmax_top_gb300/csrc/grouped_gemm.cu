@@ -8,11 +8,17 @@
 // One persistent kernel per call, one CTA per SM, warp-specialised:
 //   warp 0      TMA producer (ring of A|B stages: 4 x 48 KB, or 6 x 32 KB per CTA in pairs)
 //   warp 1      TMEM allocator + single-thread MMA issuer
-//   warps 2..9  epilogue: TMEM -> registers -> fused math -> coalesced global stores
+//   warps 2..9  epilogue: TMEM -> registers -> fused math -> global, by TMA
+//               tensor stores (or fp32 TMA reductions when a weight gradient
+//               is accumulated) or coalesced warp stores
 //               (two warps per TMEM lane quarter, each owning half the columns)
+//   warp 10     FC2 dgrad only: loads the saved pre-activation for the epilogue
 // Tiles are 128 x 256 (one tcgen05.mma M=128, N=256, K=16 per step, 4 steps
-// per 64-wide K stage). The 512 TMEM columns hold two accumulators, so the
-// epilogue of one tile overlaps the MMAs of the next.
+// per 64-wide K stage); forward and dgrad tiles run on CTA pairs (M = 256).
+// The 512 TMEM columns hold two accumulators, so the epilogue of one tile
+// overlaps the MMAs of the next. A launch may chain two modes (FC1 -> FC2
+// forward, FC2 dgrad -> FC1 dgrad): the second mode's tiles of an expert start
+// once the first mode's tiles of that expert are stored.
 //
 // Ragged groups. Expert e owns rows off[e]..off[e+1]-1 of the permuted
 // activations. Forward and dgrad tiles are (expert, 128-row block, N block):
