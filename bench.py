@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -165,14 +166,28 @@ KERNEL_SOURCES = {  # the files each kernel family is built from
 }
 
 
-def source_digest(kernel: str) -> str:
-    """Hash of the sources of one kernel: ncu traffic figures count only while it matches."""
+def code_only(text: str) -> str:
+    """C/C++ source with comments and blank lines removed, trailing space trimmed
+    (string literals are left as they are; none of the sources puts comment
+    markers inside one)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
+def source_digest(kernel: str, read=None) -> str:
+    """Hash of the code (comments stripped) of one kernel's sources: ncu traffic
+    figures count only while it matches. read(name) -> text overrides the files."""
     files = KERNEL_SOURCES.get(kernel.split("_")[0], ())
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_router_softmax_top_gb300", "csrc")
     for f in files:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        if read is None:
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(f.encode() + code_only(text).encode())
     return h.hexdigest()[:16]
 
 
