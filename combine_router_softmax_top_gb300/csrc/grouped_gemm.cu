@@ -347,13 +347,16 @@ __device__ __forceinline__ void reduce_chunks_f32(uint4* stage, uint32_t tbase, 
   }
 }
 
-// Logistic sigmoid from the identity s(x) = (1 + tanh(x/2)) / 2, with the
-// hardware tanh approximation (one MUFU op; relative error ~2^-11, below the
-// bf16 rounding the epilogue applies to its results).
-__device__ __forceinline__ float fast_sigmoid(float x) {
-  float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
-  return fmaf(0.5f, t, 0.5f);
+// Logistic sigmoid s(x) = 1 / (1 + e^-x), from the fast exponential and the
+// fast division intrinsics. Its relative error stays near 1e-6 over the whole
+// range, including large negative x where s is tiny: there e^-x is large and
+// both intrinsics keep their relative accuracy (for x below about -88, e^-x is
+// inf and s rounds to 0, the correct value to fp32 precision). A form through
+// (1 + tanh(x/2)) / 2 with the hardware tanh loses s for negative x: tanh's
+// ~2^-11 relative error near t = -1 is an absolute error of ~2.4e-4 in s,
+// which is 1.3% of s at x = -4 and exceeds s itself below x = -9.
+__device__ __forceinline__ float sigmoid_f(float x) {
+  return __fdividef(1.f, 1.f + __expf(-x));
 }
 
 __device__ __forceinline__ float round_bf16(float x) {
@@ -722,7 +725,7 @@ __device__ __forceinline__ bool epilogue_tile(const Role& R, const KParams& p,
         for (int i = 0; i < 32; ++i) {
           ag[i] = round_bf16(ag[i]);
           au[i] = round_bf16(au[i]);
-          hv[i] = ag[i] * fast_sigmoid(ag[i]) * au[i];
+          hv[i] = ag[i] * sigmoid_f(ag[i]) * au[i];
         }
         bf16* abase = p.out0 + slab_row0 * (size_t)(2 * p.F);
         warp_store32(stage, ag, abase + f, 2 * p.F, lane, slab_rows, cols_ok);
@@ -761,14 +764,14 @@ __device__ __forceinline__ bool epilogue_tile(const Role& R, const KParams& p,
 #pragma unroll
         for (int i = 0; i < 32; ++i) {  // da_up = dh * silu(a_g)
           const float ag = bf16_at(gc, i);
-          out[i] = __uint_as_float(v[i]) * ag * fast_sigmoid(ag);
+          out[i] = __uint_as_float(v[i]) * ag * sigmoid_f(ag);
         }
         ptx::mbar_arrive(&ctl.aux_empty);  // the quarter is in registers now
         warp_store32(stage, out, dbase + p.F + f, 2 * p.F, lane, slab_rows, cols_ok);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {  // da_gate = dh * a_u * silu'(a_g)
           const float ag = bf16_at(gc, i);
-          const float sg = fast_sigmoid(ag);
+          const float sg = sigmoid_f(ag);
           out[i] = __uint_as_float(v[i]) * bf16_at(uc, i) * sg * (1.f + ag * (1.f - sg));
         }
         warp_store32(stage, out, dbase + f, 2 * p.F, lane, slab_rows, cols_ok);

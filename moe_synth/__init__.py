@@ -116,14 +116,26 @@ def make_inputs(T: int, H: int, E: int, k: int, F: int, R: int = 1,
                 mode: int = ROUTE_SOFTMAX_TOPK, bias: Optional[str] = None,
                 seed: int = SEED_BASE, microbatch: int = 0,
                 x_std: float = 1.0, w_std: float = 0.02, dy_std: float = 1.0,
-                name: str = "") -> LayerInputs:
-    """Draw one micro-batch's inputs; micro-batch m>0 redraws x and dy only."""
+                w1_gate_std: Optional[float] = None, name: str = "") -> LayerInputs:
+    """Draw one micro-batch's inputs; micro-batch m>0 redraws x and dy only.
+
+    w1_gate_std, when given, is the std of w1's gate rows (rows 0..F-1 of each
+    expert) instead of w_std: it widens the gate pre-activations (std about
+    w1_gate_std * sqrt(H) for x ~ N(0,1)) to exercise SwiGLU far into both
+    tails of the sigmoid. The same normal draws are used, only scaled."""
     xs = _S_X + 16 * microbatch
     ds = _S_DY + 16 * microbatch
     x = _normal_bf16(seed, xs, (T, H), x_std)
     dy = _normal_bf16(seed, ds, (T, H), dy_std)
     w_r = _normal_bf16(seed, _S_WR, (E, H), w_std)
-    w1 = _normal_bf16(seed, _S_W1, (E, 2 * F, H), w_std)
+    if w1_gate_std is None:
+        w1 = _normal_bf16(seed, _S_W1, (E, 2 * F, H), w_std)
+    else:
+        g = _rng(seed, _S_W1).standard_normal(E * 2 * F * H, dtype=np.float32)
+        g = g.reshape(E, 2 * F, H)
+        g[:, :F] *= np.float32(w1_gate_std)
+        g[:, F:] *= np.float32(w_std)
+        w1 = torch.from_numpy(g).to(torch.bfloat16)
     w2 = _normal_bf16(seed, _S_W2, (E, H, F), w_std)
     b = zipf_bias(E, seed, bias) if bias else None
     return LayerInputs(T=T, H=H, E=E, k=k, F=F, R=R, mode=mode, x=x, w_r=w_r, w1=w1,

@@ -53,7 +53,8 @@ import numpy as np
 
 __all__ = [
     "bf16_rne", "identity", "router_logits_fp32", "router_logits_exact", "route_topk",
-    "route_forced", "softmax_full", "dispatch_layout", "permute", "expert_ffn_fwd",
+    "route_forced", "softmax_full", "dispatch_layout", "permute", "swiglu", "swiglu_bwd",
+    "expert_fc1_fwd", "expert_fc2_fwd", "expert_ffn_fwd", "expert_fc2_dgrad", "expert_fc1_dgrad",
     "combine", "combine_bwd", "expert_ffn_bwd_dgrad", "expert_ffn_bwd_wgrad",
     "expert_ffn_bwd_wgrad_accum", "permute_bwd", "route_bwd", "layer_forward", "layer_backward",
 ]
@@ -88,6 +89,28 @@ def _silu(u):
 
 def _sigmoid(u):
     return 1.0 / (1.0 + np.exp(-u))
+
+
+def swiglu(a, rnd=bf16_rne) -> np.ndarray:
+    """h = rnd(silu(a_gate) * a_up) for rows a = [a_gate | a_up] of width 2F (R6)."""
+    a = np.asarray(a, np.float64)
+    F = a.shape[1] // 2
+    return rnd(_silu(a[:, :F]) * a[:, F:])
+
+
+def swiglu_bwd(dh, a, rnd=bf16_rne) -> np.ndarray:
+    """Gradient of swiglu at a for the upstream dh [rows, F]:
+    da_gate = rnd(dh * a_up * silu'(a_gate)), silu'(u) = s(u) * (1 + u * (1 - s(u)));
+    da_up = rnd(dh * silu(a_gate)), with s the logistic sigmoid."""
+    dh = np.asarray(dh, np.float64)
+    a = np.asarray(a, np.float64)
+    F = a.shape[1] // 2
+    ag, au = a[:, :F], a[:, F:]
+    s = _sigmoid(ag)
+    da = np.empty_like(a)
+    da[:, :F] = rnd(dh * au * s * (1.0 + ag * (1.0 - s)))
+    da[:, F:] = rnd(dh * ag * s)
+    return da
 
 
 # ----------------------------------------------------------------------------- route
@@ -186,25 +209,39 @@ def permute(x, row_src, k: int) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------- experts
+def _per_expert(off, rows_out, fn):
+    """Runs fn(e, r) for every expert e with rows r = off[e]..off[e+1]-1."""
+    for e in range(len(off) - 1):
+        r = slice(int(off[e]), int(off[e + 1]))
+        if r.stop > r.start:
+            rows_out[r] = fn(e, r)
+    return rows_out
+
+
+def expert_fc1_fwd(x_perm, off, w1, rnd=bf16_rne):
+    """a = rnd(x_e @ W1_e^T) per expert (the first GEMM of the mlp phase, R6)."""
+    x_perm = np.asarray(x_perm, np.float64)
+    a = np.zeros((x_perm.shape[0], w1.shape[1]))
+    return _per_expert(off, a, lambda e, r: rnd(x_perm[r] @ np.asarray(w1[e], np.float64).T))
+
+
+def expert_fc2_fwd(h, off, w2, rnd=bf16_rne):
+    """o = rnd(h_e @ W2_e^T) per expert (the second GEMM of the mlp phase)."""
+    h = np.asarray(h, np.float64)
+    o = np.zeros((h.shape[0], w2.shape[1]))
+    return _per_expert(off, o, lambda e, r: rnd(h[r] @ np.asarray(w2[e], np.float64).T))
+
+
 def expert_ffn_fwd(x_perm, off, w1, w2, rnd=bf16_rne):
     """Per-expert SwiGLU FFN on the expert-contiguous rows (mlp phase, R6).
 
     a = rnd(x_e @ W1_e^T); h = rnd(silu(a_gate) * a_up); o = rnd(h @ W2_e^T).
+    Rows outside every expert's range (none in a dropless layout) stay 0.
     """
-    x_perm = np.asarray(x_perm, np.float64)
-    E, twoF, H = w1.shape
-    F = twoF // 2
-    N = x_perm.shape[0]
-    a = np.zeros((N, twoF))
-    h = np.zeros((N, F))
-    o = np.zeros((N, H))
-    for e in range(E):
-        r = slice(int(off[e]), int(off[e + 1]))
-        if r.stop == r.start:
-            continue
-        a[r] = rnd(x_perm[r] @ np.asarray(w1[e], np.float64).T)
-        h[r] = rnd(_silu(a[r, :F]) * a[r, F:])
-        o[r] = rnd(h[r] @ np.asarray(w2[e], np.float64).T)
+    a = expert_fc1_fwd(x_perm, off, w1, rnd)
+    h = np.zeros((a.shape[0], a.shape[1] // 2))
+    _per_expert(off, h, lambda e, r: swiglu(a[r], rnd))
+    o = expert_fc2_fwd(h, off, w2, rnd)
     return a, h, o
 
 
@@ -235,30 +272,31 @@ def combine_bwd(dy, o, slot, gates, rnd=bf16_rne):
     return d_o, dgates
 
 
+def expert_fc2_dgrad(d_o, a, off, w2, rnd=bf16_rne):
+    """da = swiglu_bwd(d_o_e @ W2_e, a_e) per expert: the gradient through the
+    second GEMM and the SwiGLU (dh is not rounded; da is)."""
+    d_o = np.asarray(d_o, np.float64)
+    a = np.asarray(a, np.float64)
+    da = np.zeros_like(a)
+    return _per_expert(off, da, lambda e, r: swiglu_bwd(d_o[r] @ np.asarray(w2[e], np.float64),
+                                                        a[r], rnd))
+
+
+def expert_fc1_dgrad(da, off, w1, rnd=bf16_rne):
+    """dx_perm = rnd(da_e @ W1_e) per expert: the gradient through the first GEMM."""
+    da = np.asarray(da, np.float64)
+    dx = np.zeros((da.shape[0], w1.shape[2]))
+    return _per_expert(off, dx, lambda e, r: rnd(da[r] @ np.asarray(w1[e], np.float64)))
+
+
 def expert_ffn_bwd_dgrad(d_o, a, off, w1, w2, rnd=bf16_rne):
     """Activation gradient of the experts (the part computed before wgrad).
 
     dh = d_o_e @ W2_e; da_up = dh * silu(a_g); da_gate = dh * a_u * silu'(a_g),
     silu'(u) = s(u) * (1 + u * (1 - s(u))); dx_perm = rnd(rnd(da) @ W1_e).
     """
-    d_o = np.asarray(d_o, np.float64)
-    a = np.asarray(a, np.float64)
-    E, twoF, H = w1.shape
-    F = twoF // 2
-    N = d_o.shape[0]
-    da = np.zeros((N, twoF))
-    dx_perm = np.zeros((N, H))
-    for e in range(E):
-        r = slice(int(off[e]), int(off[e + 1]))
-        if r.stop == r.start:
-            continue
-        dh = d_o[r] @ np.asarray(w2[e], np.float64)
-        ag, au = a[r, :F], a[r, F:]
-        s = _sigmoid(ag)
-        da[r, :F] = rnd(dh * au * s * (1.0 + ag * (1.0 - s)))
-        da[r, F:] = rnd(dh * ag * s)
-        dx_perm[r] = rnd(da[r] @ np.asarray(w1[e], np.float64))
-    return da, dx_perm
+    da = expert_fc2_dgrad(d_o, a, off, w2, rnd)
+    return da, expert_fc1_dgrad(da, off, w1, rnd)
 
 
 def expert_ffn_bwd_wgrad(x_perm, h, d_o, da, off, E: int, rnd=bf16_rne):

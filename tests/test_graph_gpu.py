@@ -1,14 +1,17 @@
-"""CUDA-graph capture of the layer (moe_graph_capture): a replay gives the same
-bits as the eager calls on the same inputs, reads its buffers afresh on every
-replay, keeps the side-stream fork/join and the accumulation flag, and rejects
-what cannot be captured."""
+"""CUDA-graph capture of the layer (moe_graph_capture): a replay matches the
+oracle on every output of its scope, gives the same bits as the eager calls on
+the same inputs, reads its buffers afresh on every replay, keeps the
+side-stream fork/join and the accumulation flag, and rejects what cannot be
+captured."""
+import numpy as np
 import pytest
 import torch
 
 import combine_router_softmax_top_gb300 as moe
 import moe_synth
+from oracle import moe_oracle as O
 
-from _parity import desc_of
+from _parity import FLOAT_KEYS, INT_KEYS, assert_close, collect, compare_layer, desc_of, oracle_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +55,60 @@ def same_bits(b1, b2, names):
 
 
 CASE = dict(T=600, H=256, E=16, k=4, F=256, R=2, seed=51)
+
+# outputs of each scope in the oracle's names (logits is compared bit for bit)
+SCOPE_KEYS = {
+    moe.GRAPH_ROUTER_PREPROCESS: set(INT_KEYS) | {"logits", "gates", "x_perm"},
+}
+SCOPE_KEYS[moe.GRAPH_LAYER_FORWARD] = SCOPE_KEYS[moe.GRAPH_ROUTER_PREPROCESS] | {"a", "h", "o",
+                                                                                 "y"}
+SCOPE_KEYS[moe.GRAPH_LAYER_STEP] = SCOPE_KEYS[moe.GRAPH_LAYER_FORWARD] | {
+    "d_o", "dgates", "da", "dx_perm", "dx", "dw_r", "dw1", "dw2"}
+
+
+@pytest.mark.parametrize("scope,flags", [(moe.GRAPH_ROUTER_PREPROCESS, 0),
+                                         (moe.GRAPH_LAYER_FORWARD, 0),
+                                         (moe.GRAPH_LAYER_STEP, 0),
+                                         (moe.GRAPH_LAYER_STEP, moe.FLAG_WGRAD_ACCUM_FP32)])
+def test_replay_matches_oracle(scope, flags):
+    """Each replay of a captured scope, on new inputs copied into the captured
+    buffers, against the oracle of those inputs: integers and logits exact,
+    floats within 2e-2. Under MOE_FLAG_WGRAD_ACCUM_FP32 the main gradients
+    start at zero and take one accumulation per replay."""
+    st = torch.cuda.Stream()
+    inps = [moe_synth.make_inputs(**CASE, microbatch=m) for m in range(2)]
+    d = desc_of(inps[0])
+    d.flags = flags
+    b = moe.LayerBuffers(d)
+    b.load_inputs(inps[0])
+    torch.cuda.synchronize()
+    g = moe.Graph(d, b, scope, st)
+    keys = SCOPE_KEYS[scope]
+    if flags:
+        keys = keys - {"dw1", "dw2"}
+    skip = (set(INT_KEYS) | set(FLOAT_KEYS) | {"logits"}) - keys
+    for inp in inps:
+        b.x.copy_(inp.x)
+        b.dy.copy_(inp.dy)
+        if flags:
+            b.main_dw1.zero_()
+            b.main_dw2.zero_()
+        torch.cuda.synchronize()
+        g.replay(st)
+        st.synchronize()
+        assert moe.moe_device_status(d, b.ws) == moe.MOE_OK
+        got = collect(b, inp)
+        ora = oracle_layer(inp)
+        errs = compare_layer(got, ora, skip=skip)
+        print(scope, flags, {k: f"{v:.2e}" for k, v in errs.items()})
+        if flags:
+            z1 = np.zeros(tuple(inp.w1.shape), np.float32)
+            z2 = np.zeros(tuple(inp.w2.shape), np.float32)
+            m1, m2 = O.expert_ffn_bwd_wgrad_accum(z1, z2, ora["x_perm"], ora["h"], ora["d_o"],
+                                                  ora["da"], ora["off"], inp.E)
+            assert_close("main_dw1", got["main_dw1"], m1)
+            assert_close("main_dw2", got["main_dw2"], m2)
+    g.close()
 
 
 @pytest.mark.parametrize("scope", [moe.GRAPH_ROUTER_PREPROCESS, moe.GRAPH_LAYER_FORWARD,

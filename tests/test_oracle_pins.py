@@ -235,6 +235,33 @@ def test_identical_experts_reduce_to_dense_ffn():
     np.testing.assert_allclose(fwd["y"], want, rtol=1e-12, atol=1e-12)
 
 
+def test_swiglu_and_its_gradient_against_torch_over_both_tails():
+    """SwiGLU and its gradient against torch's silu and autograd in float64, on
+    pre-activations far into both tails of the sigmoid (|a_gate| up to 40),
+    element by element: the large-|gate| regime the GPU epilogue must also
+    handle without losing the sigmoid's relative accuracy."""
+    g = np.random.default_rng(17)
+    rows, F = 64, 48
+    ag = np.concatenate([np.linspace(-40.0, 40.0, rows * F // 2),
+                         g.standard_normal(rows * F // 2) * 8.0]).reshape(rows, F)
+    au = g.standard_normal((rows, F)) * 3.0
+    a = np.concatenate([ag, au], axis=1)
+    dh = g.standard_normal((rows, F))
+    at = torch.tensor(a, dtype=torch.float64, requires_grad=True)
+    ht = torch.nn.functional.silu(at[:, :F]) * at[:, F:]
+    ht.backward(torch.tensor(dh))
+    want_h, want_da = ht.detach().numpy(), at.grad.numpy()
+    np.testing.assert_allclose(O.swiglu(a, O.identity), want_h, rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(O.swiglu_bwd(dh, a, O.identity), want_da, rtol=1e-11,
+                               atol=1e-300)
+    # with the bf16 rounding of R8: one rounding of those values
+    assert np.array_equal(O.swiglu(a), O.bf16_rne(O.swiglu(a, O.identity)))
+    # deep negative gates: silu(u) ~ u e^u, nonzero and of the right sign
+    h = O.swiglu(a, O.identity)
+    deep = ag < -20
+    assert np.all(np.sign(h[deep]) == -np.sign(au[deep]))
+
+
 # ----------------------------------------------------------------------------- gradients
 def _loss(inp, dy):
     fwd = O.layer_forward(inp, rnd=O.identity, exact_logits=True)

@@ -9,8 +9,8 @@ import combine_router_softmax_top_gb300 as moe
 import moe_synth
 from oracle import moe_oracle as O
 
-from _parity import (assert_close, assert_equal, compare_layer, desc_of, np64, npi,
-                     oracle_layer, run_layer)
+from _parity import (assert_close, assert_equal, check_stages, compare_layer, desc_of, np64,
+                     npi, oracle_layer, run_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,8 +61,12 @@ def test_layer_parity(case):
     inp = CASES[case]()
     g = run_layer(inp)
     o = oracle_layer(inp)
-    errs = compare_layer(g, o)
+    ew = {}
+    errs = compare_layer(g, o, elementwise=ew)
+    stages = check_stages(g, inp)
     print(case, {k: f"{v:.2e}" for k, v in errs.items()})
+    print(case, "element-wise", {k: f"{v:.2e}" for k, v in ew.items()})
+    print(case, "stages", {k: {m: f"{x:.2e}" for m, x in v.items()} for k, v in stages.items()})
 
 
 def test_zero_tokens():
