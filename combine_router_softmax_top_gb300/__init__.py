@@ -79,12 +79,14 @@ _SIGS = {
     "moe_workspace_size": ([_DP], _SZ),
     "moe_device_status": ([_DP, _VP, _VP], _I32),
     "moe_kernel_launches": ([], ctypes.c_uint64),
+    "moe_set_barrier_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_uint64),
     "moe_kernel_name": ([_I32], ctypes.c_char_p),
     "moe_profile_start": ([_I32], _I32),
     "moe_profile_stop": ([ctypes.POINTER(KernelTime), _I32, ctypes.POINTER(_I32)], _I32),
     "moe_route": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_dispatch_layout": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
     "moe_dispatch_layout_static": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], _I32),
+    "moe_dispatch_layout_static_status": ([_VP], _I32),
     "moe_permute": ([_DP, _VP, _VP, _VP, _VP], _I32),
     "moe_dispatch_fused": ([_DP] + [_VP] * 14 + [_SZ, _VP], _I32),
     "moe_expert_ffn_fwd": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
@@ -96,6 +98,7 @@ _SIGS = {
                                        _I32),
     "moe_permute_bwd": ([_DP, _VP, _VP, _VP, _VP], _I32),
     "moe_route_bwd": ([_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I32),
+    "moe_ep_resort": ([_DP, _VP, _VP, _VP, _VP, ctypes.c_int64, _I32, _VP], _I32),
     "moe_layer_forward": ([_DP, ctypes.POINTER(MbBufs), _VP], _I32),
     "moe_layer_backward": ([_DP, ctypes.POINTER(MbBufs), _I32, _VP], _I32),
     "moe_layer_step_host": ([_DP, ctypes.POINTER(MbBufs), _VP, _VP, _VP, _VP, _VP], _I32),
@@ -106,6 +109,7 @@ _SIGS = {
     "moe_sched_create": ([_DP, _VP, _VP, _I32, ctypes.POINTER(_VP)], _I32),
     "moe_sched_step": ([_VP, ctypes.POINTER(MbBufs), _I32, _I32], _I32),
     "moe_sched_flush": ([_VP], _I32),
+    "moe_sched_set_phase_timing": ([_VP, _I32], _I32),
     "moe_sched_timings": ([_VP, ctypes.POINTER(PhaseTime), _I32, ctypes.POINTER(_I32)], _I32),
     "moe_sched_destroy": ([_VP], None),
 }
@@ -170,6 +174,11 @@ def moe_kernel_launches() -> int:
     return int(lib().moe_kernel_launches())
 
 
+def moe_set_barrier_wait_limit_ns(ns: int) -> int:
+    """Grid-barrier wait limit of the fused dispatch (0 = default 2 s); returns the old one."""
+    return int(lib().moe_set_barrier_wait_limit_ns(int(ns)))
+
+
 def moe_kernel_name(kernel: int) -> str:
     return lib().moe_kernel_name(int(kernel)).decode()
 
@@ -203,6 +212,11 @@ def moe_dispatch_layout_static(desc, idx, cnt, off, slot, row_src, cnt_re, rank_
     _check(lib().moe_dispatch_layout_static(_d(desc), _p(idx), _p(cnt), _p(off), _p(slot),
                                             _p(row_src), _p(cnt_re), _p(rank_off), _s(stream)),
            "moe_dispatch_layout_static")
+
+
+def moe_dispatch_layout_static_status(stream=None) -> int:
+    """Status of the last moe_dispatch_layout_static call (synchronises the stream)."""
+    return lib().moe_dispatch_layout_static_status(_s(stream))
 
 
 def moe_permute(desc, x, row_src, x_perm, stream=None):
@@ -264,6 +278,14 @@ def moe_route_bwd(desc, dgates, gates, idx, x, w_r, row_src, off, dx32, dx, dw_r
     _check(lib().moe_route_bwd(_d(desc), _p(dgates), _p(gates), _p(idx), _p(x), _p(w_r),
                                _p(row_src), _p(off), _p(dx32), _p(dx), _p(dw_r), _p(ws),
                                ws.numel() * ws.element_size(), _s(stream)), "moe_route_bwd")
+
+
+def moe_ep_resort(desc, recv_cnt, inp, out, off_local=None, inverse=False, stream=None):
+    """Receive order <-> expert-major re-sort of the EP exchange (include/moe.h)."""
+    _check(lib().moe_ep_resort(_d(desc), _p(recv_cnt), _p(inp), _p(out), _p(off_local),
+                               int(min(inp.shape[0], out.shape[0])), int(bool(inverse)),
+                               _s(stream)),
+           "moe_ep_resort")
 
 
 def moe_layer_forward(desc, bufs: "LayerBuffers", stream=None):
@@ -388,6 +410,11 @@ class Scheduler:
 
     def flush(self):
         _check(lib().moe_sched_flush(self._h), "moe_sched_flush")
+
+    def set_phase_timing(self, on: bool):
+        """Per-phase events on/off (off keeps programmatic dependent launch)."""
+        _check(lib().moe_sched_set_phase_timing(self._h, int(bool(on))),
+               "moe_sched_set_phase_timing")
 
     def timings(self):
         buf = (PhaseTime * 32)()

@@ -8,10 +8,15 @@
 #include <float.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "moe_internal.cuh"
 
 namespace moe {
+
+// Time limit of the fused dispatch's grid-barrier waits, read at each launch.
+constexpr unsigned long long kDefaultBarrierWaitNs = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_barrier_wait_ns{kDefaultBarrierWaitNs};
 
 namespace {
 
@@ -334,7 +339,6 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 // launch is cooperative, so every block is resident and the barrier waits
 // end; each is still bounded, and on expiry the block records the site and
 // returns.
-constexpr uint64_t kDispatchWaitNs = 2000000000ull;
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
@@ -347,9 +351,10 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// All blocks of the grid arrive; true once every block has (false on timeout).
+// All blocks of the grid arrive; true once every block has, false when the
+// wait ran longer than wait_ns (the site is then recorded in the status words).
 __device__ __forceinline__ bool grid_barrier(int* bar, int target, int* status, int site,
-                                             int* s_flag) {
+                                             int* s_flag, uint64_t wait_ns) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
@@ -357,7 +362,7 @@ __device__ __forceinline__ bool grid_barrier(int* bar, int target, int* status, 
     atomicAdd(bar, 1);
     const uint64_t t0 = global_ns();
     while (ld_acquire_gpu(bar) < target) {
-      if (global_ns() - t0 > kDispatchWaitNs) {
+      if (global_ns() - t0 > wait_ns) {
         atomicExch(status + ST_TIMEOUT, site);
         ok = 0;
         break;
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) dispatch_fused_kernel(
     int32_t* __restrict__ cnt, int32_t* __restrict__ off, int32_t* __restrict__ slot,
     int32_t* __restrict__ row_src, int32_t* __restrict__ cnt_re, int32_t* __restrict__ rank_off,
     bf16* __restrict__ x_perm, int* __restrict__ fhist, int* __restrict__ bar,
-    int* __restrict__ status, int T, int H, int E, int k, int R, int forced) {
+    int* __restrict__ status, int T, int H, int E, int k, int R, int forced, uint64_t wait_ns) {
   pdl_wait();
   constexpr int TB = 4 * TPL;
   static_assert(TB <= 32, "one warp holds a tile's tokens");
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) dispatch_fused_kernel(
     for (int e = threadIdx.x; e < E; e += blockDim.x) fhist[(size_t)tile * E + e] = s_hist[e];
     __syncthreads();
   }
-  if (!grid_barrier(bar, gridDim.x, status, 20, s_flag)) return;
+  if (!grid_barrier(bar, gridDim.x, status, 20, s_flag, wait_ns)) return;
 
   // 2. exclusive prefix over tiles, one expert column per block and round;
   // 8 x 32 tiles are loaded before they are scanned
@@ -435,7 +440,7 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) dispatch_fused_kernel(
       if (lane == 0) tot[e] = carry;
     }
   }
-  if (!grid_barrier(bar, 2 * (int)gridDim.x, status, 21, s_flag)) return;
+  if (!grid_barrier(bar, 2 * (int)gridDim.x, status, 21, s_flag, wait_ns)) return;
 
   // 3. expert offsets, then slots and rows tile by tile
   if (warp == 0) {
@@ -886,7 +891,8 @@ cudaError_t launch_fused_t(const moe_layer_desc_t& d, const bf16* x, const bf16*
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, dispatch_fused_kernel<TPL, HC>, x, w_r, bias, z, idx, gates, cnt,
                             off, slot, row_src, cnt_re, rank_off, x_perm, fhist, bar, status,
-                            d.T, d.H, d.E, d.k, d.R, forced);
+                            d.T, d.H, d.E, d.k, d.R, forced,
+                            (uint64_t)g_barrier_wait_ns.load(std::memory_order_relaxed));
 }
 
 template <bool FUSED>
@@ -986,3 +992,7 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
 }
 
 }  // namespace moe
+
+extern "C" uint64_t moe_set_barrier_wait_limit_ns(uint64_t ns) {
+  return moe::g_barrier_wait_ns.exchange(ns ? ns : moe::kDefaultBarrierWaitNs);
+}

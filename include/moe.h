@@ -108,6 +108,17 @@ moe_status_t moe_device_status(const moe_layer_desc_t* d, void* ws, void* stream
 
 /* ------------------------------------------------------------------ diagnostics */
 
+/* Sets the time limit of the grid-barrier waits in moe_dispatch_fused (and in
+ * the layer forward, which uses it) for launches enqueued after this call,
+ * process-wide; ns = 0 restores the default of 2 s. Returns the previous
+ * limit. A graph capture keeps the limit in force at capture time. This is a
+ * diagnostic: with a limit shorter than the blocks take to reach a barrier,
+ * waiting blocks give up, record MOE_ERR_TIMEOUT in the workspace status and
+ * return, leaving the call's outputs incomplete; the next launch starts
+ * clean. It lets a caller check its handling of a device-side timeout without
+ * any wait that cannot end. */
+uint64_t moe_set_barrier_wait_limit_ns(uint64_t ns);
+
 /* Number of kernels this library has launched in the process so far (a graph
  * replay counts its kernel nodes; a capture counts nothing). */
 uint64_t moe_kernel_launches(void);
@@ -172,19 +183,35 @@ moe_status_t moe_dispatch_layout(const moe_layer_desc_t* d, const int32_t* idx, 
  * cudaMalloc is not allowed while the stream is being captured), or a path
  * that must not block on allocator locks. Instead of a caller workspace it
  * uses a fixed scratch array inside the library's device memory, sized for at
- * most T = 65536 tokens and E = 256 experts (256 KB plus 256 bytes, held on
+ * most T = 65536 tokens and E = 256 experts (257 KB plus 256 bytes, held on
  * every GPU that loads the library until the process exits); larger shapes
  * return MOE_ERR_UNSUPPORTED. The pages describe no such call; it exists for
- * these callers only. The first call on each device looks up the scratch
- * array's device address (with that device current), so make that first call
- * before any stream capture. All calls share the one array: calls whose GPU
- * work can overlap (unordered streams) race and must not be issued; calls on
- * one stream are safe. Out-of-range expert indices are skipped (slot = -1).
+ * these callers only. Each call made outside stream capture looks up the
+ * scratch array's device address on the current device (so a reloaded module
+ * or another context of the device is followed); a call made while `stream`
+ * is capturing reuses the address the last such lookup found on that device,
+ * so make the first call on each device before any stream capture (a captured
+ * first call returns MOE_ERR_INVALID_ARG). All calls share the one array:
+ * calls whose GPU work can overlap (unordered streams) race and must not be
+ * issued; calls on one stream are safe. Out-of-range expert indices are
+ * skipped (slot = -1, and the entry has no row in row_src, so off[E] < T*k)
+ * and counted in the array's status words, which the call clears at its
+ * start: moe_dispatch_layout_static_status() reports them until the next call.
  * Outputs and argument meaning as for moe_dispatch_layout. Allocates nothing. */
 moe_status_t moe_dispatch_layout_static(const moe_layer_desc_t* d, const int32_t* idx,
                                         int32_t* cnt, int32_t* off, int32_t* slot,
                                         int32_t* row_src, int32_t* cnt_re, int32_t* rank_off,
                                         void* stream);
+
+/* Status of the last moe_dispatch_layout_static call on the current device:
+ * synchronises `stream` (the stream that call used; not while it is
+ * capturing), reads the scratch array's status words and clears them.
+ * MOE_OK, or MOE_ERR_INVALID_ARG when that call skipped out-of-range expert
+ * indices (moe_last_error() gives how many). Allocates nothing. Like the
+ * layout call it reads the one shared array, so a layout call enqueued in
+ * between on another stream would be what it reports. The pages describe no
+ * such call; it completes moe_dispatch_layout_static. */
+moe_status_t moe_dispatch_layout_static_status(void* stream);
 
 /* Permute = write the EP send buffer: x_perm[s,:] = x[row_src[s] div k, :].
  * x [T,H] bf16, row_src [N] int32, x_perm [N,H] bf16. */
@@ -199,9 +226,12 @@ moe_status_t moe_permute(const moe_layer_desc_t* d, const moe_bf16* x, const int
  *   - after a grid-wide barrier, each expert's counts are scanned over tiles;
  *   - after a second barrier, every block derives the expert offsets, numbers
  *     its own entries in token order, and copies its tokens' rows into x_perm.
- * The barrier waits are bounded (2 s). On expiry the device status reads
- * MOE_ERR_TIMEOUT. Every block is resident by the launch's construction. With
- * E > 128 or T = 0 the three calls run as separate launches.
+ * The barrier waits are bounded (2 s by default, see
+ * moe_set_barrier_wait_limit_ns). On expiry the waiting block records the
+ * site, returns without writing the rest of its outputs, and the device status
+ * reads MOE_ERR_TIMEOUT. Every block is resident by the launch's construction,
+ * so with the default limit the waits end. With E > 128 or T = 0 the three
+ * calls run as separate launches.
  * x [T,H], w_r [E,H] bf16; bias [E] fp32 or NULL; logits [T,E] fp32 or NULL
  * -> idx, gates [T,k]; cnt [E]; off [E+1]; slot [T,k]; row_src [N];
  * cnt_re [R,E/R]; rank_off [R+1]; x_perm [N,H] bf16. */
@@ -294,6 +324,32 @@ moe_status_t moe_route_bwd(const moe_layer_desc_t* d, const float* dgates, const
                            const int32_t* idx, const moe_bf16* x, const moe_bf16* w_r,
                            const int32_t* row_src, const int32_t* off, const float* dx32,
                            moe_bf16* dx, float* dw_r, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ expert parallelism */
+
+/* Receive re-sort of the expert-parallel exchange (the standard all-to-all
+ * dispatcher: the MoE expert-parallel overlap skill card, section "what it
+ * is", dispatcher table; EP16 in its benchmark sections). With R = d->R ranks,
+ * each owning E_l = d->E / R experts (rank d owns experts d*E_l..(d+1)*E_l-1),
+ * a rank receives from sources s = 0..R-1, in that order, recv_cnt[s][l]
+ * rows for each of its local experts l = 0..E_l-1: the chunk rows
+ * rank_off[d]..rank_off[d+1]-1 of source s's send buffer, whose counts are
+ * that source's cnt_re[d][:] (see moe_dispatch_layout). That is "receive
+ * order". The grouped GEMM wants "expert-major" order: expert l's rows
+ * contiguous, sources ascending inside it, each source's own order kept.
+ *   inverse = 0: out (expert-major) <- in (receive order); also writes
+ *                off_local[l] = first row of local expert l, off_local[E_l] =
+ *                total (the off[] the expert calls take for E = E_l);
+ *   inverse = 1: out (receive order) <- in (expert-major), the order the
+ *                return exchange sends o and dx_perm back in.
+ * recv_cnt [R, E_l] int32 on the device (negative counts move nothing);
+ * in, out [n_rows, H] bf16 (H = d->H), distinct buffers; off_local [E_l + 1]
+ * int32 or NULL. Rows the counts place at or beyond n_rows are not moved;
+ * output rows beyond the counts' total are not written. T, k and F of d are
+ * not used. A row copy: no arithmetic. */
+moe_status_t moe_ep_resort(const moe_layer_desc_t* d, const int32_t* recv_cnt, const moe_bf16* in,
+                           moe_bf16* out, int32_t* off_local, int64_t n_rows, int32_t inverse,
+                           void* stream);
 
 /* ------------------------------------------------------------------ whole layer */
 
@@ -419,6 +475,14 @@ moe_status_t moe_sched_create(const moe_layer_desc_t* d, void* stream_comm, void
  * moe_sched_flush(). Outputs are bit-identical to the serial schedule's. */
 moe_status_t moe_sched_step(moe_sched_t* s, const moe_mb_bufs_t* mb, int32_t overlap,
                             int32_t defer_wgrad);
+
+/* Per-phase timing on (default) or off. On, every phase of a step is
+ * bracketed by CUDA events on its stream for moe_sched_timings; those events
+ * sit between the kernels of a stream and stop each kernel's launch from
+ * overlapping the previous kernel's drain (programmatic dependent launch).
+ * Off, a step records only the events of its cross-stream dependencies, and
+ * moe_sched_timings reports no phases. */
+moe_status_t moe_sched_set_phase_timing(moe_sched_t* s, int32_t on);
 
 /* Runs a deferred wgrad, if one is pending, on stream_gemm. */
 moe_status_t moe_sched_flush(moe_sched_t* s);
