@@ -90,8 +90,8 @@ WsLayout ws_layout(const moe_layer_desc_t& d) {
   o += kStatusBytes;
   w.logits = o;
   o = align256(o + (size_t)d.T * d.E * sizeof(float));
-  w.hist = o;
-  o = align256(o + (size_t)nb * d.E * sizeof(int));
+  w.hist = o;  // dispatch layout: per-block expert counts, then a row of totals
+  o = align256(o + (size_t)(nb + 1) * d.E * sizeof(int));
   w.dz = o;
   o = align256(o + (size_t)N * sizeof(float));
   w.dwr_part = o;

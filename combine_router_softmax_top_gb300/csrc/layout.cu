@@ -3,13 +3,19 @@
 // exchanges (the "moe_preprocess" step ahead of dispatch in the EP-overlap
 // skill card, "HybridEP production benchmark").
 //
-// Two kernels, both integer-only and deterministic:
-//   1. count:  block b histograms the experts of its 256 tokens into ws.
-//   2. assign: every block re-derives the global offsets from all histograms,
-//      then numbers its own entries in token order. Within a block each warp
-//      holds 32 tokens; per expert, the warp's tokens that chose it form a
-//      32-bit mask, so the rank of a token among the block's earlier tokens is
-//      (earlier warps' popcounts) + popc(mask & lanes_below).
+// Three kernels, all integer-only and deterministic:
+//   1. count:  block b histograms the experts of its 256 tokens into
+//      hist[b][e] (nb blocks).
+//   2. scan:   block e turns column e of the histograms into exclusive
+//      prefixes over blocks, in place, and writes the column total to
+//      hist[nb][e], so every count is read a fixed, small number of times
+//      whatever the number of blocks.
+//   3. assign: each block reads its own prefixes and the totals, scans the
+//      totals into the expert offsets, then numbers its own entries in token
+//      order. Within a block each warp holds 32 tokens; per expert, the warp's
+//      tokens that chose it form a 32-bit mask, so the rank of a token among
+//      the block's earlier tokens is (earlier warps' popcounts) +
+//      popc(mask & lanes_below).
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -38,6 +44,38 @@ __global__ void __launch_bounds__(kTok) layout_count_kernel(const int32_t* __res
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = s_hist[e];
 }
 
+// Exclusive prefix of column e = blockIdx.x over the nb block histograms, in
+// place, 256 blocks at a time with a carry; the total goes to hist[nb][e].
+__global__ void __launch_bounds__(kTok) layout_scan_kernel(int* __restrict__ hist, int E,
+                                                           int nb) {
+  pdl_wait();
+  __shared__ int s_warp[kWarps];
+  const int e = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int carry = 0;
+  for (int b0 = 0; b0 < nb; b0 += kTok) {
+    const int b = b0 + threadIdx.x;
+    const int c = b < nb ? hist[(size_t)b * E + e] : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int before = carry;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    if (b < nb) hist[(size_t)b * E + e] = before + incl - c;
+    int sum = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) sum += s_warp[w];
+    carry += sum;
+    __syncthreads();  // s_warp is rewritten by the next round
+  }
+  if (threadIdx.x == 0) hist[(size_t)nb * E + e] = carry;
+}
+
 __global__ void __launch_bounds__(kTok) layout_assign_kernel(
     const int32_t* __restrict__ idx, const int* __restrict__ hist, int32_t* __restrict__ cnt,
     int32_t* __restrict__ off, int32_t* __restrict__ slot, int32_t* __restrict__ row_src,
@@ -51,16 +89,10 @@ __global__ void __launch_bounds__(kTok) layout_assign_kernel(
   int* s_pre = reinterpret_cast<int*>(s_mask + kWarps * E);   // [kWarps][E]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // totals over all blocks and the part before this block
+  // totals over all blocks and the part before this block (from the scan)
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int before = 0, total = 0;
-    for (int b = 0; b < nblocks; ++b) {
-      const int h = hist[(size_t)b * E + e];
-      if (b < (int)blockIdx.x) before += h;
-      total += h;
-    }
-    s_cnt[e] = total;
-    s_base[e] = before;
+    s_cnt[e] = hist[(size_t)nblocks * E + e];
+    s_base[e] = hist[(size_t)blockIdx.x * E + e];
   }
   for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) s_mask[i] = 0u;
   __syncthreads();
@@ -143,6 +175,12 @@ moe_status_t launch_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_
              status);
   }
   moe_status_t s = check_launch("layout_count_kernel");
+  if (s != MOE_OK) return s;
+  {
+    LaunchScope _ls(K_LAYOUT_SCAN, st);
+    launch_k(layout_scan_kernel, d.E, kTok, 0, st, hist, d.E, nb);
+  }
+  s = check_launch("layout_scan_kernel");
   if (s != MOE_OK) return s;
   const size_t smem = (size_t)d.E * (2 + 2 * kWarps) * sizeof(int);
   {

@@ -38,7 +38,7 @@ enum KernelId {
   K_COMBINE_BWD, K_PERMUTE_BWD, K_ROUTE_BWD_DX, K_ROUTE_BWD_DWR_PARTIAL, K_ROUTE_BWD_DWR_REDUCE,
   K_GEMM_FC1_FWD, K_GEMM_FC2_FWD, K_GEMM_FC2_DGRAD, K_GEMM_FC1_DGRAD, K_GEMM_WGRAD_W1,
   K_GEMM_WGRAD_W2, K_DISPATCH_BWD, K_GEMM_FFN_FWD, K_GEMM_FFN_DGRAD, K_DISPATCH_FUSED,
-  K_GEMM_WGRAD_W1_ACC, K_GEMM_WGRAD_W2_ACC, K_NUM
+  K_GEMM_WGRAD_W1_ACC, K_GEMM_WGRAD_W2_ACC, K_LAYOUT_SCAN, K_EP_RESORT, K_NUM
 };
 
 // Wraps one kernel launch: counts it and, while profiling is on, brackets it
@@ -111,6 +111,8 @@ moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, con
                                    int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
                                    int32_t* cnt_re, int32_t* rank_off, bf16* x_perm, int* fhist,
                                    int* bar, int* status, cudaStream_t st);
+// Dispatch layout in three launches. hist: (ceil(T/256) + 1) * E ints of
+// scratch (per-block expert counts, then the totals); fully rewritten.
 moe_status_t launch_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_t* cnt,
                            int32_t* off, int32_t* slot, int32_t* row_src, int32_t* cnt_re,
                            int32_t* rank_off, int* hist, int* status, cudaStream_t st);
@@ -131,6 +133,12 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
                               const int32_t* row_src, const int32_t* off, const float* dx32,
                               const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dw_r,
                               float* dz, float* dwr_part, int* status, cudaStream_t st);
+
+// Expert-parallel receive re-sort (receive order <-> expert-major) of n_rows
+// rows of H bf16; recv_cnt [R][E/R] on the device; off_local [E/R + 1] or NULL.
+moe_status_t launch_ep_resort(const moe_layer_desc_t& d, const int32_t* recv_cnt, const bf16* in,
+                              bf16* out, int32_t* off_local, int n_rows, int inverse,
+                              cudaStream_t st);
 
 enum GemmMode {
   GEMM_FC1_FWD = 0,   // a, h = SwiGLU(x_perm @ W1^T)
