@@ -41,6 +41,7 @@ struct moe_sched {
   cudaEvent_t tev[2 * moe::kMaxRecords];
   moe::Record rec[moe::kMaxRecords];
   int nrec;
+  int timing;   // record per-phase events (moe_sched_set_phase_timing)
   int pending;  // micro-batch whose wgrad was deferred, or -1
   moe_mb_bufs_t pending_bufs;
 };
@@ -92,7 +93,7 @@ moe_status_t wait(cudaStream_t st, cudaEvent_t ev) {
 moe_status_t run_phase(moe_sched* s, const moe_mb_bufs_t* b, int mb, int phase, cudaStream_t st,
                        int stream_id, int max_ctas) {
   Record* r = nullptr;
-  SCHK(begin(s, mb, phase, stream_id, st, &r));
+  if (s->timing) SCHK(begin(s, mb, phase, stream_id, st, &r));
   const moe_layer_desc_t& d = s->d;
   switch (phase) {
     case MOE_PHASE_DISPATCH: SCHK(op_dispatch(d, b, st)); break;
@@ -103,7 +104,7 @@ moe_status_t run_phase(moe_sched* s, const moe_mb_bufs_t* b, int mb, int phase, 
     case MOE_PHASE_DISPATCH_BWD: SCHK(op_dispatch_bwd_mb(d, b, st)); break;
     default: SCHK(op_wgrad_mb(d, b, max_ctas, st)); break;
   }
-  return end(r, st);
+  return r ? end(r, st) : MOE_OK;
 }
 
 }  // namespace
@@ -131,6 +132,7 @@ moe_status_t moe_sched_create(const moe_layer_desc_t* d, void* stream_comm, void
   s->sc = static_cast<cudaStream_t>(stream_comm);
   s->sg = static_cast<cudaStream_t>(stream_gemm);
   s->gemm_sms = gemm_sms;
+  s->timing = 1;
   s->pending = -1;
   cudaError_t e = cudaEventCreate(&s->ev_start);
   for (int i = 0; i < 16 && e == cudaSuccess; ++i)
@@ -253,6 +255,15 @@ moe_status_t moe_sched_step(moe_sched_t* s, const moe_mb_bufs_t* mb, int32_t ove
   // join: the comm stream ends the step after all GEMM-stream work
   SCHK(cuda_ok(cudaEventRecord(s->dep[D_SG_END], sg), "cudaEventRecord"));
   return wait(sc, s->dep[D_SG_END]);
+}
+
+moe_status_t moe_sched_set_phase_timing(moe_sched_t* s, int32_t on) {
+  if (!s) {
+    set_error("scheduler is NULL");
+    return MOE_ERR_INVALID_ARG;
+  }
+  s->timing = on != 0;
+  return MOE_OK;
 }
 
 moe_status_t moe_sched_flush(moe_sched_t* s) {
