@@ -42,6 +42,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # kernels whose floor is fp32 FMA arithmetic, not memory (fixed-order fp32 router sums)
 ALU_BOUND = ("route_logits",)
+# kernels whose floor is that arithmetic followed by their writes: the fused
+# dispatch cannot write any x_perm row before the global expert counts exist,
+# which needs every tile's routing, so its writes cannot overlap its FMA phase
+ALU_THEN_WRITE = ("dispatch_fused",)
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -119,7 +123,11 @@ def kernel_stats(agg: dict, algo: dict, pk: dict, wr_gbs: float) -> dict:
         bound = "tensor" if t_tc > t_hbm else "hbm"
         if t_alu > max(t_tc, t_hbm):
             bound = "alu"
-        t_bound = {"tensor": t_tc, "hbm": t_hbm, "alu": t_alu}[bound]
+        if name in ALU_THEN_WRITE:
+            # FMA phase at the fp32 peak, then the writes at the write-only rate
+            t_alu = fl / (FP32_TFLOPS * 1e12) + wr / (wr_gbs * 1e9)
+            bound = "alu+write"
+        t_bound = {"tensor": t_tc, "hbm": t_hbm, "alu": t_alu, "alu+write": t_alu}[bound]
         frac = t_bound / (avg_ms * 1e-3) if avg_ms > 0 else 0.0
         kernels[name] = {"launches": n, "avg_us": round(avg_ms * 1e3, 2),
                          "share": None, "GB_s": round(gbs, 1), "TFLOP_s": round(tfl, 1),
@@ -288,16 +296,33 @@ def emit(obj):
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def oracle_tokens_per_s(workload: str, T_sample: int):
-    """Times the CPU oracle (fwd + bwd) on the first T_sample tokens of the workload."""
-    import moe_synth
-    from oracle import moe_oracle as O
-    inp = moe_synth.workload(workload, T=T_sample)
-    t0 = time.perf_counter()
-    fwd = O.layer_forward(inp)
-    O.layer_backward(inp, fwd)
-    dt = time.perf_counter() - t0
-    return T_sample / dt, dt
+_ORACLE_TIMER = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import moe_synth
+from oracle import moe_oracle as O
+inp = moe_synth.workload(sys.argv[2], T=int(sys.argv[3]))
+t0 = time.perf_counter()
+fwd = O.layer_forward(inp)
+O.layer_backward(inp, fwd)
+print(json.dumps({"seconds": time.perf_counter() - t0}))
+"""
+
+
+def oracle_timing(workload: str, T_sample: int, threads: int) -> dict:
+    """Times the CPU oracle (fwd + bwd) on the first T_sample tokens of the
+    workload in a fresh process limited to `threads` BLAS/OpenMP threads (the
+    limit has to be set before numpy loads, hence the process)."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                "BLIS_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[var] = str(threads)
+    r = subprocess.run([sys.executable, "-c", _ORACLE_TIMER, ROOT, workload, str(T_sample)],
+                       env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle timing failed: {r.stderr[-500:]}")
+    sec = json.loads(r.stdout.strip().splitlines()[-1])["seconds"]
+    return {"tokens_per_s": round(T_sample / sec, 3), "seconds": round(sec, 2), "threads": threads}
 
 
 def cpu_cores() -> int:
@@ -307,7 +332,176 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 # ----------------------------------------------------------------------------- our arm
+def _agg(prof):
+    agg = {}
+    for name, t in prof:
+        a = agg.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += t
+    return agg
+
+
+def timed_steps(step, steps: int, st, groups: int = 10):
+    """Times `steps` calls of step() between CUDA events on st; the events of
+    `groups` equal slices give the step-to-step spread. Returns (ms per step,
+    {min, median, max} ms per step over the slices)."""
+    groups = max(1, min(groups, steps))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(groups + 1)]
+    bounds = [round(i * steps / groups) for i in range(groups + 1)]
+    ev[0].record(st)
+    for g in range(groups):
+        for _ in range(bounds[g + 1] - bounds[g]):
+            step()
+        ev[g + 1].record(st)
+    torch.cuda.synchronize()
+    total = ev[0].elapsed_time(ev[-1]) / steps
+    per = [ev[g].elapsed_time(ev[g + 1]) / max(1, bounds[g + 1] - bounds[g])
+           for g in range(groups)]
+    return total, {"min": round(min(per), 4), "median": round(statistics.median(per), 4),
+                   "max": round(max(per), 4), "groups": groups}
+
+
+def profiled_kernels(moe, step, steps: int, per_step_launches: int, dev):
+    """Per-launch durations of `steps` steps (events around each launch on its
+    own stream), aggregated {kernel: [launches, total ms]}."""
+    cap = per_step_launches * steps + 8
+    moe.moe_profile_start(cap)
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    return _agg(moe.moe_profile_stop(cap))
+
+
+def gemm_summary(kernels: dict, agg: dict, algo: dict, steps: int, pk: dict) -> dict:
+    names = [n for n in kernels if n.startswith("gemm")]
+    ms = sum(agg[n][1] for n in names) / steps
+    fl = sum(algo[n][2] for n in names)
+    tf = fl / (ms * 1e-3) / 1e12 if ms else None
+    pc = [n for n in ("permute", "combine", "combine_bwd", "permute_bwd", "dispatch_bwd")
+          if n in agg]
+    pc_ms = sum(agg[n][1] for n in pc) / steps
+    pc_bytes = sum(algo[n][0] + algo[n][1] for n in pc)
+    return {"grouped_gemm_TFLOP_s": round(tf, 1) if tf else None,
+            "grouped_gemm_frac_of_bf16_sustained": round(tf / pk["bf16_tflops_sustained"], 4)
+            if tf else None,
+            "permute_combine_GB_s": round(pc_bytes / (pc_ms * 1e-3) / 1e9, 1) if pc_ms else None}
+
+
+def measure_workload(moe, wl: str, args, dev, st, pk, wr_gbs, steps: int) -> dict:
+    """One single-micro-batch workload: the layer step timed, then every kernel
+    timed in a profiled pass; the compact figures for the bench line."""
+    import moe_synth
+    inp = moe_synth.workload(wl)
+    shape = inp.shape_dict()
+    d = moe.LayerDesc.of(**shape)
+    b = moe.LayerBuffers(d, dev)
+    b.load_inputs(inp)
+
+    def step():
+        moe.moe_layer_forward(d, b, st)
+        moe.moe_layer_backward(d, b, True, st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    l0 = moe.moe_kernel_launches()
+    step()
+    torch.cuda.synchronize(dev)
+    per_step = moe.moe_kernel_launches() - l0
+    ms, spread = timed_steps(step, steps, st)
+    agg = profiled_kernels(moe, step, min(steps, 20), per_step, dev)
+    status = moe.moe_device_status(d, b.ws, st)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"{wl}: device status {status}: {moe.lib().moe_last_error()}")
+    algo = algorithmic(shape)
+    ks = kernel_stats(agg, algo, pk, wr_gbs)
+    cnt = b.cnt.cpu()
+    out = {"config": {"workload": wl, **shape}, "ms_per_step": round(ms, 4),
+           "tokens_per_s": round(inp.T / (ms / 1e3), 1), "spread_ms_per_step": spread,
+           "steps": steps, "rows_per_expert": {"min": int(cnt.min()), "max": int(cnt.max())},
+           **gemm_summary(ks, agg, algo, min(steps, 20), pk),
+           "kernels": {n: {k: v[k] for k in ("avg_us", "bound", "roofline_frac", "hbm_floor_frac",
+                                             "GB_s", "TFLOP_s")} for n, v in ks.items()}}
+    del b
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_schedule(moe, args, dev, steps: int) -> dict:
+    """Two micro-batches of the balanced 4096-token layer: the serial schedule
+    against the two-stream overlap, all without per-phase events (which would
+    stop programmatic dependent launch between kernels), then one pass of each
+    with the events on for the interval analysis: the union of the dispatch/
+    combine phases, the union of the GEMM phases, and their intersection (the
+    hidden communication), never a sum of durations."""
+    import moe_synth
+    wl = "two_microbatch"
+    i0, i1 = moe_synth.workload(wl, 0), moe_synth.workload(wl, 1)
+    d = moe.LayerDesc.of(**i0.shape_dict())
+    b0 = moe.LayerBuffers(d, dev)
+    b0.load_inputs(i0)
+    b1 = moe.LayerBuffers(d, dev, weights=b0)
+    b1.load_inputs(i1, weights=False)
+    sc = torch.cuda.Stream(device=dev, priority=-1)
+    sg = torch.cuda.Stream(device=dev)
+    res = {}
+
+    def layer_pair():  # the plain layer calls, one micro-batch after the other
+        for b in (b0, b1):
+            moe.moe_layer_forward(d, b, sc)
+            moe.moe_layer_backward(d, b, True, sc)
+
+    for _ in range(args.warmup):
+        layer_pair()
+    ms, spread = timed_steps(layer_pair, steps, sc)
+    res["layer_calls_x2"] = {"ms_per_step": round(ms, 4), "spread_ms_per_step": spread}
+    for name, overlap, defer in (("serial", 0, 0), ("overlap", 1, 0), ("overlap_defer", 1, 1)):
+        s = moe.Scheduler(d, sc, sg)
+        s.set_phase_timing(False)
+        for _ in range(args.warmup):
+            s.step(b0, b1, overlap=bool(overlap), defer_wgrad=bool(defer))
+        ms, spread = timed_steps(lambda: s.step(b0, b1, overlap=bool(overlap),
+                                                defer_wgrad=bool(defer)), steps, sc)
+        s.flush()
+        # one more pass with the phase events on, for the interval analysis
+        s.set_phase_timing(True)
+        s.step(b0, b1, overlap=bool(overlap), defer_wgrad=bool(defer))
+        comm, gemm, hidden = moe.interval_overlap(s.timings())
+        s.flush()
+        torch.cuda.synchronize(dev)
+        s.close()
+        res[name] = {"ms_per_step": round(ms, 4), "spread_ms_per_step": spread,
+                     "timed_pass": {"comm_union_ms": round(comm, 4),
+                                    "gemm_union_ms": round(gemm, 4),
+                                    "hidden_comm_ms": round(hidden, 4)}}
+    for b in (b0, b1):
+        if moe.moe_device_status(d, b.ws) != moe.MOE_OK:
+            raise RuntimeError(f"schedule: device status: {moe.lib().moe_last_error()}")
+    best = min(("overlap", "overlap_defer"), key=lambda n: res[n]["ms_per_step"])
+    out = {"config": {"workload": wl, **i0.shape_dict(), "micro_batches": 2},
+           "steps": steps, "schedules": res, "best_overlap": best,
+           "tokens_per_s_best_overlap": round(2 * i0.T / (res[best]["ms_per_step"] / 1e3), 1),
+           "overlap_vs_serial": round(res["serial"]["ms_per_step"] / res[best]["ms_per_step"], 4),
+           "overlap_vs_layer_calls": round(res["layer_calls_x2"]["ms_per_step"]
+                                           / res[best]["ms_per_step"], 4)}
+    del b0, b1
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local):
     import moe_synth
     import combine_router_softmax_top_gb300 as moe
@@ -334,7 +528,6 @@ def run_ours(args, rank, world, local):
     if status != moe.MOE_OK:
         raise RuntimeError(f"device status {status}: {moe.lib().moe_last_error()}")
     torch.cuda.synchronize(dev)
-    per_step_launches = 0
     l0 = moe.moe_kernel_launches()
     step()
     torch.cuda.synchronize(dev)
@@ -359,13 +552,21 @@ def run_ours(args, rank, world, local):
     ms_local = e0.elapsed_time(e1) / args.steps
     ms = max_over_ranks(ms_local, world)
 
+    # ---- the same step sustained for about a second, in event-timed slices,
+    # with its own clock record: the spread and the clocks under a longer load
+    sustained = None
+    if not args.no_sustained:
+        n_sus = max(args.steps, int(1.0 / max(ms_local * 1e-3, 1e-6)))
+        clocks2 = ClockSampler(local)
+        time.sleep(0.25)
+        sms, spread = timed_steps(step, n_sus, st, groups=20)
+        sustained = {"steps": n_sus, "ms_per_step": round(sms, 4), "spread_ms_per_step": spread,
+                     "clocks": clocks2.stop()}
+
     # ---- per-kernel durations: the same steps again, each launch bracketed by
     # CUDA events on its own stream
-    moe.moe_profile_start(per_step_launches * args.steps + 8)
-    for _ in range(args.steps):
-        step()
-    torch.cuda.synchronize(dev)
-    prof = moe.moe_profile_stop(per_step_launches * args.steps + 8)
+    prof_steps = min(args.steps, 50)
+    agg = profiled_kernels(moe, step, prof_steps, per_step_launches, dev)
     status = moe.moe_device_status(d, b.ws, st)
     if status != moe.MOE_OK:
         raise RuntimeError(f"device status {status}: {moe.lib().moe_last_error()}")
@@ -373,11 +574,6 @@ def run_ours(args, rank, world, local):
 
     # ---- per-kernel figures from the live events
     algo = algorithmic(shape)
-    agg = {}
-    for name, t in prof:
-        a = agg.setdefault(name, [0, 0.0])
-        a[0] += 1
-        a[1] += t
     wr_gbs = hbm_write_gbs(dev)
     kernels = kernel_stats(agg, algo, pk, wr_gbs)
     total = sum(v[1] for v in agg.values())
@@ -400,13 +596,7 @@ def run_ours(args, rank, world, local):
     roof["traffic"] = traffic_for(dom, args.workload)
     roof["kernel"] = dom
     roof["peak_kind"] = pk_kind
-    gemm_names = [n for n in kernels if n.startswith("gemm")]
-    gemm_ms = sum(agg[n][1] for n in gemm_names) / args.steps
-    gemm_fl = sum(algo[n][2] for n in gemm_names)
-    pc_names = [n for n in ("permute", "combine", "combine_bwd", "permute_bwd", "dispatch_bwd")
-                if n in agg]
-    pc_ms = sum(agg[n][1] for n in pc_names) / args.steps
-    pc_bytes = sum(algo[n][0] + algo[n][1] for n in pc_names)
+    gsum = gemm_summary(kernels, agg, algo, prof_steps, pk)
 
     # ---- the same step replayed from one captured CUDA graph
     graph = None
@@ -445,19 +635,14 @@ def run_ours(args, rank, world, local):
         for _ in range(args.warmup):
             accum_call()
         torch.cuda.synchronize(dev)
-        moe.moe_profile_start(2 * args.steps + 8)
-        for _ in range(args.steps):
+        moe.moe_profile_start(2 * prof_steps + 8)
+        for _ in range(prof_steps):
             accum_call()
         torch.cuda.synchronize(dev)
-        aprof = moe.moe_profile_stop(2 * args.steps + 8)
+        aagg = _agg(moe.moe_profile_stop(2 * prof_steps + 8))
         status = moe.moe_device_status(d, b.ws, st)
         if status != moe.MOE_OK:
             raise RuntimeError(f"device status {status}: {moe.lib().moe_last_error()}")
-        aagg = {}
-        for name, t in aprof:
-            a = aagg.setdefault(name, [0, 0.0])
-            a[0] += 1
-            a[1] += t
         accum = kernel_stats(aagg, accum_algorithmic(shape), pk, wr_gbs)
         del m1, m2
 
@@ -473,6 +658,18 @@ def run_ours(args, rank, world, local):
         moe.moe_layer_step_host(d, b, hx, hdy, hy, hdx, st)
     e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world)
     nbytes = inp.T * inp.H * 2
+    del b
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads of the layer: skewed routing, the emulated EP=8
+    # layout, and the two-micro-batch schedule (rank 0 of a single-GPU run)
+    others = {}
+    if rank == 0 and world == 1 and not args.no_configs:
+        sub = max(20, args.steps // 2)
+        others["c3_skewed"] = measure_workload(moe, "qwen3_30b_a3b_skewed", args, dev, st, pk,
+                                               wr_gbs, sub)
+        others["c4_ep8"] = measure_workload(moe, "ep8_emulated", args, dev, st, pk, wr_gbs, sub)
+        others["c5_schedule"] = measure_schedule(moe, args, dev, sub)
 
     out = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
@@ -490,22 +687,29 @@ def run_ours(args, rank, world, local):
         "gpu_launches": int(launches),
         "roofline": roof,
         "clocks": clk,
-        "permute_combine_GB_s": round(pc_bytes / (pc_ms * 1e-3) / 1e9, 1) if pc_ms else None,
-        "grouped_gemm_TFLOP_s": round(gemm_fl / (gemm_ms * 1e-3) / 1e12, 1) if gemm_ms else None,
+        **gsum,
         "kernels": kernels,
     }
+    if sustained is not None:
+        out["sustained"] = sustained
     if graph is not None:
         out["graph_step"] = graph
     if accum is not None:
         out["wgrad_accum_fp32"] = {"note": "weight gradients added into fp32 main gradients, "
                                            "timed separately; not in value",
                                    "kernels": accum}
+    out.update(others)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt = oracle_tokens_per_s(args.workload, args.cpu_sample_tokens)
-        out["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cpu_cores(),
-                               "kind": "oracle",
-                               "sample": f"first {args.cpu_sample_tokens} tokens of the workload, "
-                                         f"one fwd+bwd ({dt:.1f} s), numpy float64 + OpenBLAS"}
+        Ts = args.cpu_sample_tokens
+        cores = cpu_cores()
+        allc = oracle_timing(args.workload, Ts, cores)
+        one = oracle_timing(args.workload, Ts, 1)
+        out["cpu_baseline"] = {
+            "value": allc["tokens_per_s"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": f"first {Ts} tokens of the workload, one fwd+bwd, numpy float64 + BLAS, "
+                      f"{allc['seconds']} s on {cores} threads",
+            "one_thread": one}
     if rank == 0:
         emit(out)
 
@@ -549,61 +753,21 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------------------- schedule
 def run_schedule(args):
-    """Two micro-batches through the scheduler: serial vs overlapped step time and
-    the communication time hidden behind the expert GEMMs (interval analysis)."""
-    import moe_synth
+    """Only the two-micro-batch schedule (serial vs overlap), as its own line."""
     import combine_router_softmax_top_gb300 as moe
     from combine_router_softmax_top_gb300 import build
 
     build.build()
-    wl = "two_microbatch"
-    i0, i1 = moe_synth.workload(wl, 0), moe_synth.workload(wl, 1)
-    d = moe.LayerDesc.of(**i0.shape_dict())
-    b0 = moe.LayerBuffers(d)
-    b0.load_inputs(i0)
-    b1 = moe.LayerBuffers(d, weights=b0)
-    b1.load_inputs(i1, weights=False)
-    sc = torch.cuda.Stream(priority=-1)
-    sg = torch.cuda.Stream()
-    res = {}
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for name, overlap, defer, cap in (("serial", 0, 0, 0), ("overlap", 1, 0, 0),
-                                      ("overlap_defer", 1, 1, 0),
-                                      ("overlap_defer_gemm136", 1, 1, sms - 16),
-                                      ("overlap_defer_gemm120", 1, 1, sms - 32)):
-        s = moe.Scheduler(d, sc, sg, gemm_sms=cap)
-        for _ in range(args.warmup):
-            s.step(b0, b1, overlap=bool(overlap), defer_wgrad=bool(defer))
-        s.flush()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(sc)
-        for _ in range(args.steps):
-            s.step(b0, b1, overlap=bool(overlap), defer_wgrad=bool(defer))
-        e1.record(sc)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / args.steps
-        tm = s.timings()
-        comm, gemm, hidden = moe.interval_overlap(tm)
-        s.flush()
-        torch.cuda.synchronize()
-        s.close()
-        res[name] = {"ms_per_step": round(ms, 4), "comm_union_ms": round(comm, 4),
-                     "gemm_union_ms": round(gemm, 4), "hidden_comm_ms": round(hidden, 4),
-                     "gemm_sms": cap or sms}
-    for b in (b0, b1):
-        assert moe.moe_device_status(d, b.ws) == moe.MOE_OK
-    emit({"metric": "two-micro-batch MoE layer step, serial vs two-stream overlap",
-          "unit": "ms", "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
-          "config": {"workload": wl, **i0.shape_dict(), "micro_batches": 2},
-          "schedules": res,
-          "tokens_per_s_best": round(2 * i0.T / (min(v["ms_per_step"] for v in res.values()) / 1e3), 1)})
+    dev = torch.device("cuda", 0)
+    out = measure_schedule(moe, args, dev, args.steps)
+    emit({"metric": "two-micro-batch MoE layer step, serial vs two-stream overlap", "unit": "ms",
+          "higher_is_better": False, "warmup": args.warmup, **out})
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_30b_a3b_balanced")
@@ -612,10 +776,14 @@ def main(argv=None):
                     help="skip the timing of the step replayed from a CUDA graph")
     ap.add_argument("--no-accum", action="store_true",
                     help="skip the separate timing of the fp32-accumulating weight gradients")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the skewed, EP=8 and two-micro-batch workloads")
+    ap.add_argument("--no-sustained", action="store_true",
+                    help="skip the one-second sustained run with its own clock record")
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
     ap.add_argument("--ref-sample-tokens", type=int, default=64)
     ap.add_argument("--schedule", action="store_true",
-                    help="time the two-micro-batch scheduler (serial vs overlap) instead")
+                    help="time only the two-micro-batch scheduler (serial vs overlap)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps, always
     rank, world, local = dist_setup()
