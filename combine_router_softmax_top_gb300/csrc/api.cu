@@ -224,28 +224,32 @@ moe_status_t op_dgrad(const moe_layer_desc_t& d, const bf16* d_o, const bf16* a,
   return launch_grouped_gemm_chain(d, g, g2, st);
 }
 
+// One weight gradient (GEMM_WGRAD_W1: dW1 from da and x_perm; GEMM_WGRAD_W2:
+// dW2 from d_o and h): stored as bf16 into dw, or, when main is given, added
+// in fp32 into that main gradient (dw unused).
+moe_status_t op_wgrad_one(const moe_layer_desc_t& d, int mode, const bf16* A, const bf16* B,
+                          const int32_t* off, bf16* dw, float* main, void* ws, int max_ctas,
+                          cudaStream_t st) {
+  GemmArgs g = {};
+  g.mode = mode;
+  g.A = A;
+  g.B = B;
+  g.off = off;
+  if (mode == GEMM_WGRAD_W1) g.out0 = main ? nullptr : dw;
+  else g.out1 = main ? nullptr : dw;
+  g.acc = main;
+  g.status = status_of(ws);
+  g.max_ctas = max_ctas;
+  return launch_grouped_gemm(d, g, st);
+}
+
 // Weight gradients: stored as bf16 into dw1/dw2, or, when main_dw1/main_dw2
 // are given, added in fp32 into those main gradients (dw1/dw2 unused).
 moe_status_t op_wgrad(const moe_layer_desc_t& d, const bf16* x_perm, const bf16* h,
                       const bf16* d_o, const bf16* da, const int32_t* off, bf16* dw1, bf16* dw2,
                       float* main_dw1, float* main_dw2, void* ws, int max_ctas, cudaStream_t st) {
-  GemmArgs g = {};
-  g.mode = GEMM_WGRAD_W1;
-  g.A = da;
-  g.B = x_perm;
-  g.off = off;
-  g.out0 = main_dw1 ? nullptr : dw1;
-  g.acc = main_dw1;
-  g.status = status_of(ws);
-  g.max_ctas = max_ctas;
-  MOE_CHECK(launch_grouped_gemm(d, g, st));
-  g.mode = GEMM_WGRAD_W2;
-  g.A = d_o;
-  g.B = h;
-  g.out0 = nullptr;
-  g.out1 = main_dw2 ? nullptr : dw2;
-  g.acc = main_dw2;
-  return launch_grouped_gemm(d, g, st);
+  MOE_CHECK(op_wgrad_one(d, GEMM_WGRAD_W1, da, x_perm, off, dw1, main_dw1, ws, max_ctas, st));
+  return op_wgrad_one(d, GEMM_WGRAD_W2, d_o, h, off, dw2, main_dw2, ws, max_ctas, st);
 }
 
 moe_status_t op_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,
