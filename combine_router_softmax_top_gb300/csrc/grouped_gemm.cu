@@ -154,7 +154,6 @@ struct SmemCtl {
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t epi_done[2];  // pair, odd CTA: its epilogue warps released the accumulator
-  uint64_t tail;
   uint64_t drain;
   uint64_t aux_full;
   uint64_t aux_empty;
@@ -455,8 +454,7 @@ __device__ __forceinline__ bool wait_expert(const KParams& p, int e, int target,
 template <int MODE, int KSTAGES>
 __device__ __forceinline__ bool producer_tile(const Role& R, const KParams& p,
                                               const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                              const Tile& t, int& stage, uint32_t& phase,
-                                              uint32_t& tail_phase) {
+                                              const Tile& t, int& stage, uint32_t& phase) {
   using M = Mode<MODE>;
   SmemCtl& ctl = *R.ctl;
   const int lane = R.lane;
@@ -470,21 +468,16 @@ __device__ __forceinline__ bool producer_tile(const Role& R, const KParams& p,
     uint8_t* sA = R.smem + stage * M::kStageBytes;
     uint8_t* sB = sA + kABytes;
     const int k0 = kt * BK;
-    const bool tail = M::kRagK && (t.rows - k0 < BK);
-    uint64_t* bar = tail ? &ctl.tail : &ctl.full[stage];
+    uint64_t* bar = &ctl.full[stage];
     if (lane == 0) {
       if (M::kRagK) {
         // A: this CTA's own M block. B: slice i of the shared tile is loaded
         // by cluster rank i % kCS and multicast to every CTA of the cluster,
-        // so full[stage] collects all 32 KB of B in every CTA. On the tail
-        // stage A goes to the tail barrier and full[stage] gets its arrival
-        // only after the zeroing below.
-        if (tail) {
-          ptx::mbar_arrive_expect_tx(&ctl.tail, kABytes);
-          ptx::mbar_expect_tx(&ctl.full[stage], M::kBBytes);
-        } else {
-          ptx::mbar_arrive_expect_tx(&ctl.full[stage], M::kStageBytes);
-        }
+        // so full[stage] collects all 32 KB of B in every CTA. In the last K
+        // stage of an expert the rows past its end are the next expert's;
+        // the MMA warp zeroes them in A once the stage has landed, so the
+        // producer never waits for a load.
+        ptx::mbar_arrive_expect_tx(&ctl.full[stage], M::kStageBytes);
         const int r = t.row0 + k0;
         ptx::tma_load_2d(sA, tmA, bar, t.m0, r);
         ptx::tma_load_2d(sA + 8192, tmA, bar, t.m0 + 64, r);
@@ -536,24 +529,6 @@ __device__ __forceinline__ bool producer_tile(const Role& R, const KParams& p,
         }
       }
     }
-    if (tail) {
-      // last K stage of a wgrad tile: zero the A rows past the expert's end
-      if (!ptx::mbar_wait(&ctl.tail, tail_phase, &ctl.abort, kWaitLimitNs)) {
-        if (lane == 0) flag_timeout(ctl, p.status, 2);
-        return false;
-      }
-      tail_phase ^= 1;
-      const int valid = t.rows - k0;       // 1..63
-      const int nzero = (BK - valid) * 8;  // 16-byte chunks per atom
-      for (int i = lane; i < 2 * nzero; i += 32) {
-        const int atom = i / nzero, j = i % nzero;
-        uint4* dst = reinterpret_cast<uint4*>(sA + atom * 8192 + valid * 128) + j;
-        *dst = make_uint4(0, 0, 0, 0);
-      }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ctl.full[stage]);
-    }
     if (++stage == KSTAGES) {
       stage = 0;
       phase ^= 1;
@@ -575,46 +550,77 @@ __device__ __forceinline__ bool mma_tile(const Role& R, const KParams& p, const 
   constexpr uint32_t a_lbo = M::kAMn ? 8192 : 16, b_lbo = M::kBMn ? 8192 : 16;
   constexpr uint32_t a_adv = M::kAMn ? (2048 >> 4) : (32 >> 4);
   constexpr uint32_t b_adv = M::kBMn ? (2048 >> 4) : (32 >> 4);
+  // K-ragged (wgrad) launches run this on all 32 lanes of the MMA warp, the
+  // others on lane 0 alone; one lane issues the MMAs and commits either way
+  const bool issuer = !M::kRagK || R.lane == 0;
+  // (every lane waits and the warp agrees on the outcome, so it stays converged)
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    const bool got = ptx::mbar_wait(bar, parity, &ctl.abort, kWaitLimitNs);
+    return M::kRagK ? __all_sync(0xffffffffu, got) : got;
+  };
   if (t.nk == 0) return true;
-  if (!ptx::mbar_wait(&ctl.tmem_empty[acc], acc_phase ^ 1, &ctl.abort, kWaitLimitNs)) {
+  if (!wait(&ctl.tmem_empty[acc], acc_phase ^ 1)) {
     flag_timeout(ctl, p.status, 3);
     return false;
   }
   ptx::tc_fence_after();
-  trace(p, MODE, 2, ti);
+  if (issuer) trace(p, MODE, 2, ti);
   const uint32_t d_tmem = R.tmem_base + acc * kAccCols;
   for (int kt = 0; kt < t.nk; ++kt) {
-    if (!ptx::mbar_wait(&ctl.full[stage], phase, &ctl.abort, kWaitLimitNs)) {
+    if (!wait(&ctl.full[stage], phase)) {
       flag_timeout(ctl, p.status, 4);
       return false;
     }
     ptx::tc_fence_after();
-    const uint32_t a_addr = ptx::smem_u32(R.smem + stage * M::kStageBytes);
+    uint8_t* sA = R.smem + stage * M::kStageBytes;
+    int nkk = BK / 16;
+    if (M::kRagK && t.rows - kt * BK < BK) {
+      // last K stage of the expert: only the 16-row MMA steps that hold its
+      // rows run, and the rows of the next expert inside the last of them
+      // are zeroed in A (rows are 128 B in both 8 KB atoms, whatever the
+      // swizzle), by the whole warp, before the MMAs read the stage
+      const int valid = t.rows - kt * BK;  // 1..63
+      nkk = (valid + 15) / 16;
+      const int nzero = (nkk * 16 - valid) * 8;  // 16-byte chunks per atom
+      for (int i = R.lane; i < 2 * nzero; i += 32) {
+        const int atom = i / nzero, j = i % nzero;
+        *(reinterpret_cast<uint4*>(sA + atom * 8192 + valid * 128) + j) = make_uint4(0, 0, 0, 0);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      ptx::tc_fence_after();
+    }
+    const uint32_t a_addr = ptx::smem_u32(sA);
     const uint32_t b_addr = a_addr + kABytes;
     const uint64_t adesc = ptx::sdesc_sw128(a_addr, a_lbo, 1024);
     const uint64_t bdesc = ptx::sdesc_sw128(b_addr, b_lbo, 1024);
+    if (issuer) {
 #pragma unroll
-    for (int kk = 0; kk < BK / 16; ++kk) {
-      if (M::kPair)
-        ptx::umma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * a_adv), bdesc + (uint64_t)(kk * b_adv),
-                            idesc, (kt | kk) != 0);
-      else
-        ptx::umma_bf16(d_tmem, adesc + (uint64_t)(kk * a_adv), bdesc + (uint64_t)(kk * b_adv),
-                       idesc, (kt | kk) != 0);
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        if (kk >= nkk) break;
+        if (M::kPair)
+          ptx::umma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * a_adv),
+                              bdesc + (uint64_t)(kk * b_adv), idesc, (kt | kk) != 0);
+        else
+          ptx::umma_bf16(d_tmem, adesc + (uint64_t)(kk * a_adv), bdesc + (uint64_t)(kk * b_adv),
+                         idesc, (kt | kk) != 0);
+      }
+      // the stage is free once every CTA whose shared memory the MMAs read
+      // (pair) or that received the multicast B slices has consumed it
+      if (M::kPair) ptx::umma_commit_pair(&ctl.empty[stage], 3);
+      else if (M::kCS > 1) ptx::umma_commit_multicast(&ctl.empty[stage], R.cmask);
+      else ptx::umma_commit(&ctl.empty[stage]);
     }
-    // the stage is free once every CTA whose shared memory the MMAs read
-    // (pair) or that received the multicast B slices has consumed it
-    if (M::kPair) ptx::umma_commit_pair(&ctl.empty[stage], 3);
-    else if (M::kCS > 1) ptx::umma_commit_multicast(&ctl.empty[stage], R.cmask);
-    else ptx::umma_commit(&ctl.empty[stage]);
     if (++stage == KSTAGES) {
       stage = 0;
       phase ^= 1;
     }
   }
-  trace(p, MODE, 3, ti);
-  if (M::kPair) ptx::umma_commit_pair(&ctl.tmem_full[acc], 3);
-  else ptx::umma_commit(&ctl.tmem_full[acc]);
+  if (issuer) {
+    trace(p, MODE, 3, ti);
+    if (M::kPair) ptx::umma_commit_pair(&ctl.tmem_full[acc], 3);
+    else ptx::umma_commit(&ctl.tmem_full[acc]);
+  }
   if (++acc == 2) {
     acc = 0;
     acc_phase ^= 1;
@@ -847,7 +853,6 @@ __global__ void __launch_bounds__(Fuse<MODE, MODE2>::kWarps * 32, 1)
       ptx::mbar_init(&ctl.tmem_empty[b], F::kPair ? 9 : 8);
       ptx::mbar_init(&ctl.epi_done[b], 8);
     }
-    ptx::mbar_init(&ctl.tail, 1);
     ptx::mbar_init(&ctl.drain, 1);
     ptx::mbar_init(&ctl.aux_full, 1);
     ptx::mbar_init(&ctl.aux_empty, 256);
@@ -908,14 +913,14 @@ __global__ void __launch_bounds__(Fuse<MODE, MODE2>::kWarps * 32, 1)
   if (warp == 0) {
     // ================================================================ producer
     int stage = 0;
-    uint32_t phase = 0, tail_phase = 0;
+    uint32_t phase = 0;
     int ti = 0;
     for (int tile = first; tile < total; tile += stride, ++ti) {
       bool ok;
       if (!F::kHas2 || tile < total1) {
         const Tile t = tile1(tile);
         if (lane == 0) trace(p, MODE, 0, ti);
-        ok = producer_tile<MODE, KS>(R, p, &tmA, &tmB, t, stage, phase, tail_phase);
+        ok = producer_tile<MODE, KS>(R, p, &tmA, &tmB, t, stage, phase);
       } else {
         const Tile t = tile2(tile);
         // the A operand of this tile is the first mode's output for expert t.e
@@ -925,7 +930,7 @@ __global__ void __launch_bounds__(Fuse<MODE, MODE2>::kWarps * 32, 1)
           if (!ok) flag_timeout(ctl, p.status, 10);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) ok = producer_tile<MODE_B, KS>(R, p2, &tmA2, &tmB2, t, stage, phase, tail_phase);
+        if (ok) ok = producer_tile<MODE_B, KS>(R, p2, &tmA2, &tmB2, t, stage, phase);
       }
       if (lane == 0) trace(p, MODE, 1, ti);
       if (!ok) break;
@@ -933,7 +938,9 @@ __global__ void __launch_bounds__(Fuse<MODE, MODE2>::kWarps * 32, 1)
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     // (pair mode: only the even CTA issues, for both CTAs)
-    if (lane == 0 && !(F::kPair && R.crank != 0)) {
+    // (K-ragged launches: the whole warp, which zeroes the tail rows of A)
+    constexpr bool kWarpMma = Mode<MODE>::kRagK && !F::kHas2;
+    if ((kWarpMma || lane == 0) && !(F::kPair && R.crank != 0)) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       int ti = -1;
@@ -947,8 +954,10 @@ __global__ void __launch_bounds__(Fuse<MODE, MODE2>::kWarps * 32, 1)
         if (!ok) break;
       }
       // make sure no MMA is still running before TMEM is released
-      if (F::kPair) ptx::umma_commit_pair(&ctl.drain, 1);
-      else ptx::umma_commit(&ctl.drain);
+      if (lane == 0) {
+        if (F::kPair) ptx::umma_commit_pair(&ctl.drain, 1);
+        else ptx::umma_commit(&ctl.drain);
+      }
       if (!ptx::mbar_wait(&ctl.drain, 0, &ctl.abort, kWaitLimitNs)) {
         // abort already flagged: wait once more with the abort flag ignored
         int dummy = 0;
