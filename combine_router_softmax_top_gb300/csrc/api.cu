@@ -41,6 +41,7 @@ moe_status_t check_launch(const char* what) {
 struct CopyLane {
   cudaStream_t stream = nullptr;
   cudaEvent_t start = nullptr, dy_in = nullptr, fwd_done = nullptr, y_out = nullptr;
+  cudaEvent_t dx_ready = nullptr;
   // moe_layer_backward's side stream: the weight gradients run on it beside
   // the dispatch backward (they depend on the dgrad only, not on each other)
   cudaStream_t side = nullptr;
@@ -62,7 +63,8 @@ CopyLane* copy_lane() {
   if (!l.stream) {
     cudaError_t e = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&l.side, cudaStreamNonBlocking);
-    for (cudaEvent_t* ev : {&l.start, &l.dy_in, &l.fwd_done, &l.y_out, &l.fork, &l.join})
+    for (cudaEvent_t* ev : {&l.start, &l.dy_in, &l.fwd_done, &l.y_out, &l.dx_ready, &l.fork,
+                            &l.join})
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) {
       set_error("copy stream setup: %s", cudaGetErrorString(e));
@@ -528,17 +530,33 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b
   return op_combine_mb(*d, b, S(stream));
 }
 
-moe_status_t moe_layer_backward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
-                                int32_t run_wgrad, void* stream) {
-  MOE_CHECK(validate(d));
-  MOE_CHECK(check_mb(*d, b, true));
-  cudaStream_t st = S(stream);
+}  // extern "C"
+
+// The layer backward on `st`. When dx_ready is given, it is recorded on `st`
+// as soon as dx is complete (after the dispatch backward, before the weight
+// gradients are joined), so that a caller can start copying dx out while the
+// weight gradients still run.
+static moe_status_t layer_backward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
+                                   int32_t run_wgrad, cudaStream_t st, cudaEvent_t dx_ready) {
+  auto mark_dx = [&]() -> moe_status_t {
+    if (!dx_ready) return MOE_OK;
+    const cudaError_t e = cudaEventRecord(dx_ready, st);
+    if (e != cudaSuccess) {
+      set_error("cudaEventRecord: %s", cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  };
   MOE_CHECK(op_combine_bwd_mb(*d, b, st));
   MOE_CHECK(op_dgrad_mb(*d, b, 0, st));
-  if (!run_wgrad) return op_dispatch_bwd_mb(*d, b, st);
+  if (!run_wgrad) {
+    MOE_CHECK(op_dispatch_bwd_mb(*d, b, st));
+    return mark_dx();
+  }
   if (profiling_active()) {
     // per-launch timing: every launch in order on `stream`, each timed alone
     MOE_CHECK(op_dispatch_bwd_mb(*d, b, st));
+    MOE_CHECK(mark_dx());
     return op_wgrad_mb(*d, b, 0, st);
   }
   // fork: the weight gradients (write-bound) on the side stream beside the
@@ -559,13 +577,23 @@ moe_status_t moe_layer_backward(const moe_layer_desc_t* d, const moe_mb_bufs_t* 
     set_error("side stream: %s", cudaGetErrorString(e));
     return MOE_ERR_CUDA;
   }
-  const moe_status_t s = op_dispatch_bwd_mb(*d, b, st);
+  moe_status_t s = op_dispatch_bwd_mb(*d, b, st);
+  if (s == MOE_OK) s = mark_dx();
   e = cudaStreamWaitEvent(st, cl->join, 0);
   if (e != cudaSuccess) {
     set_error("side stream: %s", cudaGetErrorString(e));
     return MOE_ERR_CUDA;
   }
   return s;
+}
+
+extern "C" {
+
+moe_status_t moe_layer_backward(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
+                                int32_t run_wgrad, void* stream) {
+  MOE_CHECK(validate(d));
+  MOE_CHECK(check_mb(*d, b, true));
+  return layer_backward(d, b, run_wgrad, S(stream), nullptr);
 }
 
 moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
@@ -607,8 +635,13 @@ moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t*
     set_error("copy stream: %s", cudaGetErrorString(e));
     return MOE_ERR_CUDA;
   }
-  MOE_CHECK(moe_layer_backward(d, b, 1, stream));
-  e = cudaMemcpyAsync(host_dx, b->dx, bytes, cudaMemcpyDeviceToHost, st);
+  // dx comes out on the copy stream as soon as the dispatch backward has
+  // written it, while the weight gradients still run
+  MOE_CHECK(layer_backward(d, b, 1, st, cl->dx_ready));
+  e = cudaStreamWaitEvent(cl->stream, cl->dx_ready, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(host_dx, b->dx, bytes, cudaMemcpyDeviceToHost, cl->stream);
+  if (e == cudaSuccess) e = cudaEventRecord(cl->y_out, cl->stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(st, cl->y_out, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {

@@ -389,9 +389,11 @@ moe_status_t moe_layer_backward(const moe_layer_desc_t* d, const moe_mb_bufs_t* 
  * forward and the backward (with wgrad), and copies y and dx back into host_y
  * and host_dx. Host buffers should be pinned. The dy upload and the y download
  * run on a library-owned copy stream (one per device, created by the first
- * call with that device current), overlapping the forward and the backward;
- * everything is ordered after the work already on `stream`. Returns once all
- * four copies are done (synchronises `stream`). */
+ * call with that device current), overlapping the forward and the backward,
+ * and dx goes out on that stream as soon as the dispatch backward has written
+ * it, beside the weight gradients; everything is ordered after the work
+ * already on `stream`. Returns once all four copies and the weight gradients
+ * are done (synchronises `stream`). */
 moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
                                  const moe_bf16* host_x, const moe_bf16* host_dy,
                                  moe_bf16* host_y, moe_bf16* host_dx, void* stream);
