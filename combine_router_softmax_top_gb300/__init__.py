@@ -102,6 +102,9 @@ _SIGS = {
     "moe_layer_forward": ([_DP, ctypes.POINTER(MbBufs), _VP], _I32),
     "moe_layer_backward": ([_DP, ctypes.POINTER(MbBufs), _I32, _VP], _I32),
     "moe_layer_step_host": ([_DP, ctypes.POINTER(MbBufs), _VP, _VP, _VP, _VP, _VP], _I32),
+    "moe_layer_steps_host": ([_DP, ctypes.POINTER(MbBufs), _I32, ctypes.POINTER(_VP),
+                              ctypes.POINTER(_VP), ctypes.POINTER(_VP), ctypes.POINTER(_VP), _VP],
+                             _I32),
     "moe_graph_capture": ([_DP, ctypes.POINTER(MbBufs), _I32, _VP, ctypes.POINTER(_VP)], _I32),
     "moe_graph_launch": ([_VP, _VP], _I32),
     "moe_graph_kernel_count": ([_VP], _I32),
@@ -302,6 +305,19 @@ def moe_layer_step_host(desc, bufs: "LayerBuffers", host_x, host_dy, host_y, hos
     _check(lib().moe_layer_step_host(_d(desc), ctypes.byref(bufs.struct()), _p(host_x),
                                      _p(host_dy), _p(host_y), _p(host_dx), _s(stream)),
            "moe_layer_step_host")
+
+
+def moe_layer_steps_host(desc, bufs0: "LayerBuffers", bufs1: "LayerBuffers", host_x, host_dy,
+                         host_y, host_dx, stream=None):
+    """n pipelined steps from host memory (lists of n pinned CPU tensors each)."""
+    n = len(host_x)
+    if not (len(host_dy) == len(host_y) == len(host_dx) == n):
+        raise ValueError("host lists must have the same length")
+    arr = (MbBufs * 2)(bufs0.struct(), bufs1.struct())
+    ptrs = lambda ts: (_VP * max(n, 1))(*[t.data_ptr() for t in ts])  # noqa: E731
+    _check(lib().moe_layer_steps_host(_d(desc), arr, n, ptrs(host_x), ptrs(host_dy),
+                                      ptrs(host_y), ptrs(host_dx), _s(stream)),
+           "moe_layer_steps_host")
 
 
 # ----------------------------------------------------------------------------- buffers

@@ -42,6 +42,10 @@ struct CopyLane {
   cudaStream_t stream = nullptr;
   cudaEvent_t start = nullptr, dy_in = nullptr, fwd_done = nullptr, y_out = nullptr;
   cudaEvent_t dx_ready = nullptr;
+  // moe_layer_steps_host: a second copy stream (device to host) and, per
+  // input slot, the events of its pipeline
+  cudaStream_t d2h = nullptr;
+  cudaEvent_t in_ready[2] = {}, fwd_s[2] = {}, dx_s[2] = {}, step_done[2] = {}, out_done[2] = {};
   // moe_layer_backward's side stream: the weight gradients run on it beside
   // the dispatch backward (they depend on the dgrad only, not on each other)
   cudaStream_t side = nullptr;
@@ -63,6 +67,11 @@ CopyLane* copy_lane() {
   if (!l.stream) {
     cudaError_t e = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&l.side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&l.d2h, cudaStreamNonBlocking);
+    for (int s = 0; s < 2; ++s)
+      for (cudaEvent_t* ev : {&l.in_ready[s], &l.fwd_s[s], &l.dx_s[s], &l.step_done[s],
+                              &l.out_done[s]})
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     for (cudaEvent_t* ev : {&l.start, &l.dy_in, &l.fwd_done, &l.y_out, &l.dx_ready, &l.fork,
                             &l.join})
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
@@ -646,6 +655,85 @@ moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t*
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     set_error("device to host copy: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_steps_host(const moe_layer_desc_t* d, const moe_mb_bufs_t* b,
+                                  int32_t n, const moe_bf16* const* host_x,
+                                  const moe_bf16* const* host_dy, moe_bf16* const* host_y,
+                                  moe_bf16* const* host_dx, void* stream) {
+  MOE_CHECK(validate(d));
+  if (!b) {
+    set_error("buffer structs are NULL");
+    return MOE_ERR_INVALID_ARG;
+  }
+  MOE_CHECK(check_mb(*d, &b[0], true));
+  MOE_CHECK(check_mb(*d, &b[1], true));
+  if (n < 0 || (n > 0 && (!host_x || !host_dy || !host_y || !host_dx))) {
+    set_error("n must be >= 0 and the host pointer arrays given");
+    return MOE_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n; ++i) {
+    if (!host_x[i] || !host_dy[i] || !host_y[i] || !host_dx[i]) {
+      set_error("host buffer of step %d is NULL", i);
+      return MOE_ERR_INVALID_ARG;
+    }
+  }
+  if (b[0].x == b[1].x || b[0].dy == b[1].dy || b[0].y == b[1].y || b[0].dx == b[1].dx) {
+    set_error("the two buffer sets need their own x, dy, y and dx");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (n == 0) return MOE_OK;
+  const size_t bytes = (size_t)d->T * d->H * sizeof(moe_bf16);
+  cudaStream_t st = S(stream);
+  CopyLane* cl = copy_lane();
+  if (!cl) return MOE_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  auto ok = [&](cudaError_t r) {
+    if (e == cudaSuccess) e = r;
+    return e == cudaSuccess;
+  };
+  // step i uses slot i % 2: its x, dy go in on the copy stream while step i-1
+  // computes (after step i-2, the slot's last user, has finished reading
+  // them), and its y, dx come out on the second copy stream while step i+1
+  // computes; step i waits for its inputs and for step i-2's outputs to have
+  // left the slot's y and dx
+  auto upload = [&](int i) {
+    const int s = i & 1;
+    if (i >= 2) ok(cudaStreamWaitEvent(cl->stream, cl->step_done[s], 0));
+    ok(cudaMemcpyAsync(const_cast<moe_bf16*>(b[s].x), host_x[i], bytes, cudaMemcpyHostToDevice,
+                       cl->stream));
+    ok(cudaMemcpyAsync(const_cast<moe_bf16*>(b[s].dy), host_dy[i], bytes,
+                       cudaMemcpyHostToDevice, cl->stream));
+    ok(cudaEventRecord(cl->in_ready[s], cl->stream));
+  };
+  ok(cudaEventRecord(cl->start, st));
+  ok(cudaStreamWaitEvent(cl->stream, cl->start, 0));
+  ok(cudaStreamWaitEvent(cl->d2h, cl->start, 0));
+  upload(0);
+  for (int i = 0; i < n && e == cudaSuccess; ++i) {
+    const int s = i & 1;
+    if (i + 1 < n) upload(i + 1);
+    ok(cudaStreamWaitEvent(st, cl->in_ready[s], 0));
+    if (i >= 2) ok(cudaStreamWaitEvent(st, cl->out_done[s], 0));
+    if (e != cudaSuccess) break;
+    MOE_CHECK(moe_layer_forward(d, &b[s], stream));
+    ok(cudaEventRecord(cl->fwd_s[s], st));
+    ok(cudaStreamWaitEvent(cl->d2h, cl->fwd_s[s], 0));
+    ok(cudaMemcpyAsync(host_y[i], b[s].y, bytes, cudaMemcpyDeviceToHost, cl->d2h));
+    if (e != cudaSuccess) break;
+    MOE_CHECK(layer_backward(d, &b[s], 1, st, cl->dx_s[s]));
+    ok(cudaStreamWaitEvent(cl->d2h, cl->dx_s[s], 0));
+    ok(cudaMemcpyAsync(host_dx[i], b[s].dx, bytes, cudaMemcpyDeviceToHost, cl->d2h));
+    ok(cudaEventRecord(cl->out_done[s], cl->d2h));
+    ok(cudaEventRecord(cl->step_done[s], st));
+  }
+  for (int s = 0; s < 2 && s < n; ++s) ok(cudaStreamWaitEvent(st, cl->out_done[s], 0));
+  ok(cudaStreamSynchronize(st));
+  if (e != cudaSuccess) {
+    set_error("moe_layer_steps_host: %s", cudaGetErrorString(e));
     return MOE_ERR_CUDA;
   }
   return MOE_OK;

@@ -398,6 +398,25 @@ moe_status_t moe_layer_step_host(const moe_layer_desc_t* d, const moe_mb_bufs_t*
                                  const moe_bf16* host_x, const moe_bf16* host_dy,
                                  moe_bf16* host_y, moe_bf16* host_dx, void* stream);
 
+/* n training steps of the layer from host memory, pipelined. Step i copies
+ * host_x[i] and host_dy[i] in, runs the forward and the backward (with
+ * wgrad) and copies y and dx out into host_y[i] and host_dx[i], as
+ * moe_layer_step_host does, on the buffer set b[i % 2]. Step i+1's inputs go
+ * in on a library-owned copy stream while step i computes, and step i's
+ * outputs come out on a second one while step i+1 computes, so the copies
+ * leave the critical path; the computation of the steps runs one after the
+ * other on `stream`. The two buffer sets need their own x, dy, y and dx (all
+ * writable device buffers); every other pointer may be shared between them
+ * (weights, workspace, intermediates, gradients), since no two steps compute
+ * at once. Each step's weight gradients go where its set says (overwritten,
+ * or added under MOE_FLAG_WGRAD_ACCUM_FP32 in step order). The host arrays
+ * hold n pointers each; host buffers should be pinned. Returns once every
+ * step is done and every copy has landed (synchronises `stream`). */
+moe_status_t moe_layer_steps_host(const moe_layer_desc_t* d, const moe_mb_bufs_t* b /*[2]*/,
+                                  int32_t n, const moe_bf16* const* host_x,
+                                  const moe_bf16* const* host_dy, moe_bf16* const* host_y,
+                                  moe_bf16* const* host_dx, void* stream);
+
 /* ------------------------------------------------------------------ CUDA graphs */
 
 /* Capture scopes. The skill card's production benchmark (section "HybridEP

@@ -150,3 +150,42 @@ def test_graph_capture_checks_arguments_before_any_cuda_call(L):
     assert L.moe_graph_launch(None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_graph_kernel_count(None) == 0
     L.moe_graph_destroy(None)  # a no-op
+
+
+def test_expert_parallel_and_pipelined_entry_points_check_arguments(L):
+    d = moe.LayerDesc.of(T=16, H=128, E=8, k=2, F=256, R=2)
+    p = ctypes.c_void_p(4096)
+    # the EP re-sort: NULL counts, a negative row count, in place, a bad direction
+    assert L.moe_ep_resort(ctypes.byref(d), None, p, ctypes.c_void_p(8192), None, 4, 0,
+                           None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_ep_resort(ctypes.byref(d), p, p, ctypes.c_void_p(8192), None, -1, 0,
+                           None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_ep_resort(ctypes.byref(d), p, p, p, None, 4, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert b"in place" in L.moe_last_error()
+    assert L.moe_ep_resort(ctypes.byref(d), p, p, ctypes.c_void_p(8192), None, 4, 2,
+                           None) == moe.MOE_ERR_INVALID_ARG
+    # the pipelined host steps: the two buffer sets must not share x, dy, y or dx
+    b = _fake_bufs(d)
+    arr = (moe.MbBufs * 2)(b, b)
+    ptrs = (ctypes.c_void_p * 1)(4096)
+    st = L.moe_layer_steps_host(ctypes.byref(d), arr, 1, ptrs, ptrs, ptrs, ptrs, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"own x" in L.moe_last_error()
+    b2 = _fake_bufs(d)
+    b2.x, b2.dy, b2.y, b2.dx = 8192, 8192 + 4096, 8192 + 8192, 8192 + 12288
+    arr = (moe.MbBufs * 2)(b, b2)
+    assert L.moe_layer_steps_host(ctypes.byref(d), arr, -1, ptrs, ptrs, ptrs,
+                                  ptrs, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_layer_steps_host(ctypes.byref(d), arr, 0, None, None, None, None,
+                                  None) == moe.MOE_OK  # nothing to do
+    nul = (ctypes.c_void_p * 1)(None)
+    st = L.moe_layer_steps_host(ctypes.byref(d), arr, 1, ptrs, nul, ptrs, ptrs, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"step 0" in L.moe_last_error()
+
+
+def test_barrier_wait_limit_round_trips(L):
+    old = moe.moe_set_barrier_wait_limit_ns(12345)
+    try:
+        assert moe.moe_set_barrier_wait_limit_ns(0) == 12345
+        assert moe.moe_set_barrier_wait_limit_ns(0) == 2_000_000_000  # 0 restores the default
+    finally:
+        moe.moe_set_barrier_wait_limit_ns(old)

@@ -186,6 +186,36 @@ def test_host_step_matches_device_path():
     assert np.array_equal(np64(hdx), g["dx"])
 
 
+def test_pipelined_host_steps_match_single_steps():
+    """moe_layer_steps_host over five different inputs (two buffer sets that
+    share every buffer but x, dy, y and dx): each step's y and dx are the bits
+    of the device path on that input, and the last step's weight gradients
+    are that step's."""
+    inps = [moe_synth.make_inputs(T=256, H=256, E=8, k=2, F=256, seed=25, microbatch=m)
+            for m in range(5)]
+    want = [run_layer(inp) for inp in inps]
+    d = desc_of(inps[0])
+    b0 = moe.LayerBuffers(d)
+    b0.load_inputs(inps[0])
+    b1 = moe.LayerBuffers(d, weights=b0)
+    for name in ("logits", "idx", "gates", "cnt", "off", "slot", "row_src", "cnt_re", "rank_off",
+                 "x_perm", "a", "h", "o", "d_o", "dgates", "da", "dx_perm", "dx32", "dw_r", "dw1",
+                 "dw2", "ws"):
+        setattr(b1, name, getattr(b0, name))  # shared intermediates and gradients
+    hx = [inp.x.clone().pin_memory() for inp in inps]
+    hdy = [inp.dy.clone().pin_memory() for inp in inps]
+    hy = [torch.empty_like(t).pin_memory() for t in hx]
+    hdx = [torch.empty_like(t).pin_memory() for t in hx]
+    moe.moe_layer_steps_host(d, b0, b1, hx, hdy, hy, hdx)
+    for i in range(5):
+        assert np.array_equal(np64(hy[i]), want[i]["y"]), i
+        assert np.array_equal(np64(hdx[i]), want[i]["dx"]), i
+    assert np.array_equal(np64(b0.dw1), want[4]["dw1"])
+    assert moe.moe_device_status(d, b0.ws) == moe.MOE_OK
+    with pytest.raises(moe.MoeError):  # the two sets must not share their inputs
+        moe.moe_layer_steps_host(d, b0, b0, hx, hdy, hy, hdx)
+
+
 @pytest.mark.parametrize("k", [3, 8, 12])
 def test_fused_dispatch_bwd_matches_two_calls(k):
     """The layer path fuses the permute backward into the router's dx pass; it
