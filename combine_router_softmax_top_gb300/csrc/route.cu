@@ -539,65 +539,93 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) dispatch_fused_kernel(
 // ------------------------------------------------------------------ backward
 // dz_j = g_j (dg_j - <g, dg>) on the chosen set;
 // dx = bf16(dx32 + sum_j dz_j * w_r[i_j]), j ascending.
-// A block owns kDxTok tokens x one 64-column slice of the row: the slice of
-// w_r (E x 64) is staged in shared memory once, so the k expert rows a token
-// adds come from shared memory instead of k gathers through L2. Thread
-// (token lane, chunk) = (tid / 8, tid % 8) handles one 16-byte chunk of the
-// slice for 32 tokens at a time; the 8 threads of a token read its routing
-// state (the same addresses, from L1) and each works out dz itself.
+// A block owns kDxTok tokens x one slice of COLS columns of the row: the
+// slice of w_r (E x COLS) is staged in shared memory once, so the k expert
+// rows a token adds come from shared memory instead of k gathers through L2.
+// The block's routing state (k experts, slots, gates and gate gradients of
+// each token: a contiguous range of the [T, k] arrays) is staged with
+// coalesced loads in one round trip, and one thread per token works out its
+// dz there. Then COLS / 8 threads per token each handle one 16-byte chunk of
+// the slice, with the token's k row loads in flight together and no
+// routing-state load between one token and the next.
 // FUSED: the dispatch backward is done in the same pass and dx32 is never
 // stored: the row sum dx32[t] = sum_j dx_perm[slot[t,j]] (fp32, j ascending,
 // from 0) is formed in registers exactly as the standalone permute backward
 // forms it, then the router term is added in the same order as above, so the
 // two paths give the same bits.
-constexpr int kDxTok = 128;                 // tokens per block
-constexpr int kDxPitchB = 64 * 2 + 16;      // bytes per staged w_r slice row
+// Measured on the 4096-token layer: 128-column slices of 64 tokens take 40 us,
+// 64-column slices of 128 tokens 43 us, 256 x 64 56 us, and the earlier form,
+// whose threads loaded each token's routing state themselves, 46 us. Two
+// tokens' row loads in flight per thread took 61 us: the registers they need
+// cut the blocks per SM from four to two.
+constexpr int kDxTok = 64;  // tokens per block
+constexpr int kDxCols = 128;  // columns per slice when H allows (else 64)
+// bytes per staged w_r slice row, for a slice of COLS columns
+__host__ __device__ constexpr int dx_pitch(int cols) { return cols * 2 + 16; }
 
-template <int KMAX, bool FUSED>
+// dynamic shared memory of the dx kernel: the w_r slice, then per routed
+// entry of the block's tokens its expert, slot, gate and dz
+__host__ __device__ constexpr size_t dx_smem_bytes(int cols, int E, int k) {
+  return (size_t)E * dx_pitch(cols) + (size_t)kDxTok * k * 16;
+}
+
+template <int KMAX, bool FUSED, int COLS>
 __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     const float* __restrict__ dgates, const float* __restrict__ gates,
     const int32_t* __restrict__ idx, const bf16* __restrict__ w_r, const float* __restrict__ dx32,
     const bf16* __restrict__ dx_perm, const int32_t* __restrict__ slot, bf16* __restrict__ dx,
     float* __restrict__ dz, int T, int H, int E, int k, int* status) {
   pdl_wait();
-  constexpr int KB = KMAX < 8 ? KMAX : 8;  // rows in flight per batch
-  extern __shared__ __align__(16) uint8_t s_wr[];  // [E][kDxPitchB]
+  constexpr int KB = KMAX < 8 ? KMAX : 8;  // row loads per batch
+  constexpr int LANES = COLS / 8;            // threads per token: 16 bytes of the slice each
+  constexpr int TPP = 256 / LANES;           // tokens per pass of the block
+  constexpr int PITCH = dx_pitch(COLS);
+  extern __shared__ __align__(16) uint8_t s_wr[];  // [E][PITCH], then the routing state
+  int* s_e = reinterpret_cast<int*>(s_wr + (size_t)E * PITCH);  // [kDxTok * k]
+  int* s_slot = s_e + kDxTok * k;
+  float* s_g = reinterpret_cast<float*>(s_slot + kDxTok * k);
+  float* s_dz = s_g + kDxTok * k;  // dg while staged, then dz
+  const int t0 = blockIdx.y * kDxTok;
+  const int nt = min(kDxTok, T - t0);
+  const int nent = nt * k;
+  const size_t tk0 = (size_t)t0 * k;
+  const long long N = (long long)T * k;
   // slices vary fastest across the grid: blocks resident together read
   // different column windows of the rows
-  const int c = blockIdx.x * 8 + (threadIdx.x & 7);  // 16-byte chunk of the row
-  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) {
-    const int e = i >> 3, q = i & 7;
-    *reinterpret_cast<uint4*>(s_wr + e * kDxPitchB + q * 16) =
-        __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)e * H) + blockIdx.x * 8 + q);
+  const int c = blockIdx.x * LANES + (threadIdx.x % LANES);  // 16-byte chunk of the row
+  for (int i = threadIdx.x; i < E * LANES; i += blockDim.x) {
+    const int e = i / LANES, q = i % LANES;
+    *reinterpret_cast<uint4*>(s_wr + e * PITCH + q * 16) =
+        __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)e * H) + blockIdx.x * LANES + q);
+  }
+  for (int i = threadIdx.x; i < nent; i += blockDim.x) {
+    const int e = __ldg(idx + tk0 + i);
+    s_e[i] = (unsigned)e < (unsigned)E ? e : -1;
+    if (FUSED) {
+      const int sv = __ldg(slot + tk0 + i);
+      s_slot[i] = sv >= 0 && sv < N ? sv : -1;
+    }
+    s_g[i] = __ldg(gates + tk0 + i);
+    s_dz[i] = __ldg(dgates + tk0 + i);
   }
   __syncthreads();
-  const long long N = (long long)T * k;
-  const bool writer = blockIdx.x == 0 && (threadIdx.x & 7) == 0;
-  for (int tl = threadIdx.x >> 3; tl < kDxTok; tl += 32) {
-    const int t = blockIdx.y * kDxTok + tl;
-    if (t >= T) break;
-    const size_t tk = (size_t)t * k;
-    float dzj[KMAX];
-    int ej[KMAX], sj[KMAX];
+  if ((int)threadIdx.x < nt) {
+    const int b = threadIdx.x * k;
     float inner = 0.f;
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      ej[j] = -1;
-      sj[j] = -1;
-      if (j < k) {
-        const int e = __ldg(idx + tk + j);
-        ej[j] = (unsigned)e < (unsigned)E ? e : -1;
-        if (FUSED) {
-          const int sv = __ldg(slot + tk + j);
-          sj[j] = sv >= 0 && sv < N ? sv : -1;
-        }
-        inner = fmaf(__ldg(gates + tk + j), __ldg(dgates + tk + j), inner);
+    for (int j = 0; j < k; ++j) inner = fmaf(s_g[b + j], s_dz[b + j], inner);
+    const bool writer = blockIdx.x == 0;
+    for (int j = 0; j < k; ++j) {
+      const float v = s_g[b + j] * (s_dz[b + j] - inner);
+      s_dz[b + j] = v;
+      if (writer) {
+        dz[tk0 + b + j] = v;
+        if (s_e[b + j] < 0) atomicAdd(status + ST_BAD_INDEX, 1);
       }
     }
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j)
-      dzj[j] = j < k ? __ldg(gates + tk + j) * (__ldg(dgates + tk + j) - inner) : 0.f;
-
+  }
+  __syncthreads();
+  const uint8_t* wchunk = s_wr + (threadIdx.x % LANES) * 16;
+  for (int tl = threadIdx.x / LANES; tl < nt; tl += TPP) {
     float acc[8];
     if (FUSED) {
 #pragma unroll
@@ -608,9 +636,9 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
 #pragma unroll
         for (int u = 0; u < KB; ++u) {
           const int j = j0 + u;
-          v[u] = (j < k && sj[j] >= 0)
-                     ? __ldcs(reinterpret_cast<const uint4*>(dx_perm + (size_t)sj[j] * H) + c)
-                     : make_uint4(0, 0, 0, 0);
+          const int sv = j < k ? s_slot[tl * k + j] : -1;
+          v[u] = sv >= 0 ? __ldcs(reinterpret_cast<const uint4*>(dx_perm + (size_t)sv * H) + c)
+                         : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < KB; ++u) {
@@ -623,21 +651,24 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
         }
       }
     } else {
-      const float4* src = reinterpret_cast<const float4*>(dx32 + (size_t)t * H + c * 8);
+      const float4* src = reinterpret_cast<const float4*>(dx32 + (size_t)(t0 + tl) * H + c * 8);
       const float4 p0 = src[0], p1 = src[1];
       acc[0] = p0.x; acc[1] = p0.y; acc[2] = p0.z; acc[3] = p0.w;
       acc[4] = p1.x; acc[5] = p1.y; acc[6] = p1.z; acc[7] = p1.w;
     }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      if (j < k && ej[j] >= 0) {
-        const uint4 wv =
-            *reinterpret_cast<const uint4*>(s_wr + ej[j] * kDxPitchB + (threadIdx.x & 7) * 16);
-        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+      if (j < k) {
+        const int e = s_e[tl * k + j];
+        if (e >= 0) {
+          const float dzj = s_dz[tl * k + j];
+          const uint4 wv = *reinterpret_cast<const uint4*>(wchunk + e * PITCH);
+          const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[2 * q] = fmaf(dzj[j], bf16_bits_to_f32(w[q] & 0xFFFFu), acc[2 * q]);
-          acc[2 * q + 1] = fmaf(dzj[j], bf16_bits_to_f32(w[q] >> 16), acc[2 * q + 1]);
+          for (int q = 0; q < 4; ++q) {
+            acc[2 * q] = fmaf(dzj, bf16_bits_to_f32(w[q] & 0xFFFFu), acc[2 * q]);
+            acc[2 * q + 1] = fmaf(dzj, bf16_bits_to_f32(w[q] >> 16), acc[2 * q + 1]);
+          }
         }
       }
     }
@@ -648,16 +679,7 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
       __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
       o[q] = *reinterpret_cast<uint32_t*>(&b2);
     }
-    *reinterpret_cast<uint4*>(dx + (size_t)t * H + c * 8) = out;
-    if (writer) {
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
-          dz[tk + j] = dzj[j];
-          if (ej[j] < 0) atomicAdd(status + ST_BAD_INDEX, 1);
-        }
-      }
-    }
+    *reinterpret_cast<uint4*>(dx + (size_t)(t0 + tl) * H + c * 8) = out;
   }
 }
 
@@ -895,24 +917,50 @@ cudaError_t launch_fused_t(const moe_layer_desc_t& d, const bf16* x, const bf16*
                             (uint64_t)g_barrier_wait_ns.load(std::memory_order_relaxed));
 }
 
+template <int KMAX, bool FUSED, int COLS>
+cudaError_t launch_dx_c(const moe_layer_desc_t& d, const float* dgates, const float* gates,
+                        const int32_t* idx, const bf16* w_r, const float* dx32,
+                        const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dz,
+                        int* status, cudaStream_t st) {
+  const dim3 g(d.H / COLS, ceil_div(d.T, kDxTok));
+  const size_t smem = dx_smem_bytes(COLS, d.E, d.k);
+  // E <= 256, k <= 32: allow the largest once per instantiation
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      route_bwd_dx_kernel<KMAX, FUSED, COLS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)dx_smem_bytes(COLS, 256, 32));
+  if (attr != cudaSuccess) return attr;
+  return launch_k(route_bwd_dx_kernel<KMAX, FUSED, COLS>, g, 256, smem, st, dgates, gates, idx,
+                  w_r, dx32, dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
+}
+
+// slices of kDxCols columns when H allows, else of 64 (H is a multiple of 64)
+template <int KMAX, bool FUSED>
+cudaError_t launch_dx_t(const moe_layer_desc_t& d, const float* dgates, const float* gates,
+                        const int32_t* idx, const bf16* w_r, const float* dx32,
+                        const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dz,
+                        int* status, cudaStream_t st) {
+  if (d.H % kDxCols == 0)
+    return launch_dx_c<KMAX, FUSED, kDxCols>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx,
+                                             dz, status, st);
+  return launch_dx_c<KMAX, FUSED, 64>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz,
+                                      status, st);
+}
+
 template <bool FUSED>
-void launch_dx(const moe_layer_desc_t& d, const float* dgates, const float* gates,
-               const int32_t* idx, const bf16* w_r, const float* dx32, const bf16* dx_perm,
-               const int32_t* slot, bf16* dx, float* dz, int* status, cudaStream_t st) {
-  const dim3 g(d.H / 64, ceil_div(d.T, kDxTok));
-  const size_t smem = (size_t)d.E * kDxPitchB;
+cudaError_t launch_dx(const moe_layer_desc_t& d, const float* dgates, const float* gates,
+                      const int32_t* idx, const bf16* w_r, const float* dx32, const bf16* dx_perm,
+                      const int32_t* slot, bf16* dx, float* dz, int* status, cudaStream_t st) {
   if (d.k <= 4)
-    launch_k(route_bwd_dx_kernel<4, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
-             dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
-  else if (d.k <= 8)
-    launch_k(route_bwd_dx_kernel<8, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
-             dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
-  else if (d.k <= 16)
-    launch_k(route_bwd_dx_kernel<16, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
-             dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
-  else
-    launch_k(route_bwd_dx_kernel<32, FUSED>, g, 256, smem, st, dgates, gates, idx, w_r, dx32,
-             dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
+    return launch_dx_t<4, FUSED>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status,
+                                 st);
+  if (d.k <= 8)
+    return launch_dx_t<8, FUSED>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status,
+                                 st);
+  if (d.k <= 16)
+    return launch_dx_t<16, FUSED>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status,
+                                  st);
+  return launch_dx_t<32, FUSED>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status,
+                                st);
 }
 
 moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
@@ -961,12 +1009,17 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
   const bool fused = dx_perm != nullptr;
   const int cpr = d.H / 8;
   if (d.T > 0) {
+    cudaError_t e;
     {
       LaunchScope _ls(fused ? K_DISPATCH_BWD : K_ROUTE_BWD_DX, st);
       if (fused)
-        launch_dx<true>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status, st);
+        e = launch_dx<true>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status, st);
       else
-        launch_dx<false>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status, st);
+        e = launch_dx<false>(d, dgates, gates, idx, w_r, dx32, dx_perm, slot, dx, dz, status, st);
+    }
+    if (e != cudaSuccess) {
+      set_error("route_bwd_dx_kernel launch: %s", cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
     }
     moe_status_t s = check_launch("route_bwd_dx_kernel");
     if (s != MOE_OK) return s;
