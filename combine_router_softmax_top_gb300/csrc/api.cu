@@ -189,9 +189,12 @@ moe_status_t op_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_t* c
                        ws_at<int>(ws, ws_layout(d).hist), status_of(ws), st);
 }
 
+// counters_zeroed: the chain's per-expert counters in ws were cleared by the
+// launch just before it on the stream (the layer path's fused dispatch, or
+// combine backward for the dgrad chain), so the chain needs no memset.
 moe_status_t op_ffn_fwd(const moe_layer_desc_t& d, const bf16* x_perm, const int32_t* off,
                         const bf16* w1, const bf16* w2, bf16* a, bf16* h, bf16* o, void* ws,
-                        int max_ctas, cudaStream_t st) {
+                        int max_ctas, cudaStream_t st, bool counters_zeroed = false) {
   GemmArgs g = {};
   g.mode = GEMM_FC1_FWD;
   g.A = x_perm;
@@ -209,12 +212,13 @@ moe_status_t op_ffn_fwd(const moe_layer_desc_t& d, const bf16* x_perm, const int
   g2.out0 = o;
   g2.out1 = nullptr;
   // FC2 tiles of an expert start as soon as its FC1 tiles are stored
-  return launch_grouped_gemm_chain(d, g, g2, st);
+  return launch_grouped_gemm_chain(d, g, g2, st, counters_zeroed);
 }
 
 moe_status_t op_dgrad(const moe_layer_desc_t& d, const bf16* d_o, const bf16* a,
                       const int32_t* off, const bf16* w1, const bf16* w2, bf16* da,
-                      bf16* dx_perm, void* ws, int max_ctas, cudaStream_t st) {
+                      bf16* dx_perm, void* ws, int max_ctas, cudaStream_t st,
+                      bool counters_zeroed = false) {
   GemmArgs g = {};
   g.mode = GEMM_FC2_DGRAD;
   g.A = d_o;
@@ -232,7 +236,7 @@ moe_status_t op_dgrad(const moe_layer_desc_t& d, const bf16* d_o, const bf16* a,
   g2.out0 = dx_perm;
   g2.aux = nullptr;
   // FC1 dgrad tiles of an expert start as soon as its da is stored
-  return launch_grouped_gemm_chain(d, g, g2, st);
+  return launch_grouped_gemm_chain(d, g, g2, st, counters_zeroed);
 }
 
 // One weight gradient (GEMM_WGRAD_W1: dW1 from da and x_perm; GEMM_WGRAD_W2:
@@ -284,9 +288,10 @@ moe_status_t op_dispatch_all(const moe_layer_desc_t& d, const bf16* x, const bf1
   if (d.T > 0 && d.E <= 128) {
     const WsLayout w = ws_layout(d);
     float* z = logits ? logits : ws_at<float>(ws, w.logits);
+    // it also clears the forward chain's counters (op_ffn_fwd_mb relies on it)
     return launch_dispatch_fused(d, x, w_r, bias, z, idx, gates, cnt, off, slot, row_src, cnt_re,
                                  rank_off, x_perm, ws_at<int>(ws, w.fhist), ws_at<int>(ws, w.bar),
-                                 status_of(ws), st);
+                                 status_of(ws), st, ws_at<int>(ws, w.dep), d.E);
   }
   MOE_CHECK(op_route(d, x, w_r, bias, logits, idx, gates, ws, st));
   MOE_CHECK(op_layout(d, idx, cnt, off, slot, row_src, cnt_re, rank_off, ws, st));
@@ -302,10 +307,12 @@ moe_status_t op_dispatch(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cuda
 
 moe_status_t op_ffn_fwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
                            cudaStream_t st) {
+  // the fused dispatch (T > 0, E <= 128) that precedes this phase has cleared
+  // the chain's counters; the three-launch dispatch has not
   return op_ffn_fwd(d, reinterpret_cast<const bf16*>(b->x_perm), b->off,
                     reinterpret_cast<const bf16*>(b->w1), reinterpret_cast<const bf16*>(b->w2),
                     reinterpret_cast<bf16*>(b->a), reinterpret_cast<bf16*>(b->h),
-                    reinterpret_cast<bf16*>(b->o), b->ws, max_ctas, st);
+                    reinterpret_cast<bf16*>(b->o), b->ws, max_ctas, st, d.T > 0 && d.E <= 128);
 }
 
 moe_status_t op_combine_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st) {
@@ -315,9 +322,11 @@ moe_status_t op_combine_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cu
 
 moe_status_t op_combine_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b,
                                cudaStream_t st) {
+  // it also clears the dgrad chain's counters (op_dgrad_mb relies on it)
   return launch_combine_bwd(d, reinterpret_cast<const bf16*>(b->dy),
                             reinterpret_cast<const bf16*>(b->o), b->slot, b->gates,
-                            reinterpret_cast<bf16*>(b->d_o), b->dgates, st);
+                            reinterpret_cast<bf16*>(b->d_o), b->dgates, st,
+                            ws_at<int>(b->ws, ws_layout(d).dep), d.E);
 }
 
 moe_status_t op_dgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
@@ -325,7 +334,8 @@ moe_status_t op_dgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int 
   return op_dgrad(d, reinterpret_cast<const bf16*>(b->d_o), reinterpret_cast<const bf16*>(b->a),
                   b->off, reinterpret_cast<const bf16*>(b->w1),
                   reinterpret_cast<const bf16*>(b->w2), reinterpret_cast<bf16*>(b->da),
-                  reinterpret_cast<bf16*>(b->dx_perm), b->ws, max_ctas, st);
+                  reinterpret_cast<bf16*>(b->dx_perm), b->ws, max_ctas, st,
+                  /*counters_zeroed=*/true);
 }
 
 moe_status_t op_dispatch_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b,

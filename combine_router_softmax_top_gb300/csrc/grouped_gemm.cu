@@ -1317,7 +1317,8 @@ moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, c
 }
 
 moe_status_t launch_grouped_gemm_chain(const moe_layer_desc_t& d, const GemmArgs& g1,
-                                       const GemmArgs& g2, cudaStream_t st) {
+                                       const GemmArgs& g2, cudaStream_t st,
+                                       bool counters_zeroed) {
   const long long N = (long long)d.T * d.k;
   if (N == 0) return MOE_OK;
   const bool fwd = g1.mode == GEMM_FC1_FWD && g2.mode == GEMM_FC2_FWD;
@@ -1335,11 +1336,14 @@ moe_status_t launch_grouped_gemm_chain(const moe_layer_desc_t& d, const GemmArgs
   long long b1 = 0, b2 = 0;
   if (!mode_setup(d, g1, m1, p1, b1) || !mode_setup(d, g2, m2, p2, b2)) return MOE_ERR_CUDA;
   p2.dep = p1.dep;
-  // the counters start at zero for every launch
-  cudaError_t e = cudaMemsetAsync(g1.dep, 0, (size_t)d.E * sizeof(int), st);
-  if (e != cudaSuccess) {
-    set_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
-    return MOE_ERR_CUDA;
+  // the counters start at zero for every launch: cleared here unless the
+  // launch just before on the stream has done it
+  if (!counters_zeroed) {
+    cudaError_t e = cudaMemsetAsync(g1.dep, 0, (size_t)d.E * sizeof(int), st);
+    if (e != cudaSuccess) {
+      set_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
+    }
   }
   const int grid = grid_for(g1, b1 + b2);
   if (fwd)

@@ -105,12 +105,14 @@ moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* 
                           int* status, cudaStream_t st);
 // Route + dispatch layout + permute in one cooperative launch (E <= 128, T > 0;
 // MOE_ERR_UNSUPPORTED otherwise). fhist: ws area of (ceil(T/4) + 1) * E ints;
-// bar: one int, zeroed by the launcher.
+// bar: one int, zeroed by the launcher. zero/nzero: as for launch_combine_bwd
+// (the layer path clears there the counters of the forward chain that follows).
 moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
                                    const float* bias, float* z, int32_t* idx, float* gates,
                                    int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
                                    int32_t* cnt_re, int32_t* rank_off, bf16* x_perm, int* fhist,
-                                   int* bar, int* status, cudaStream_t st);
+                                   int* bar, int* status, cudaStream_t st, int* zero = nullptr,
+                                   int nzero = 0);
 // Dispatch layout in three launches. hist: (ceil(T/256) + 1) * E ints of
 // scratch (per-block expert counts, then the totals); fully rewritten.
 moe_status_t launch_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_t* cnt,
@@ -120,9 +122,14 @@ moe_status_t launch_permute(const moe_layer_desc_t& d, const bf16* x, const int3
                             bf16* x_perm, cudaStream_t st);
 moe_status_t launch_combine(const moe_layer_desc_t& d, const bf16* o, const int32_t* slot,
                             const float* gates, bf16* y, cudaStream_t st);
+// zero/nzero: nzero ints that block 0 sets to 0 once the previous launch on
+// the stream has completed; the layer path clears there the counters of the
+// dgrad chain that follows, in place of a memset between the two launches
+// (which would stop the chain's launch from overlapping this one's drain).
 moe_status_t launch_combine_bwd(const moe_layer_desc_t& d, const bf16* dy, const bf16* o,
                                 const int32_t* slot, const float* gates, bf16* d_o,
-                                float* dgates, cudaStream_t st);
+                                float* dgates, cudaStream_t st, int* zero = nullptr,
+                                int nzero = 0);
 moe_status_t launch_permute_bwd(const moe_layer_desc_t& d, const bf16* dx_perm,
                                 const int32_t* slot, float* dx32, cudaStream_t st);
 // Router backward. With dx_perm (and slot) given, the dispatch backward is
@@ -165,8 +172,12 @@ struct GemmArgs {
 moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, cudaStream_t st);
 // Two dependent GEMMs in one persistent launch: FC1 fwd then FC2 fwd, or FC2
 // dgrad then FC1 dgrad. A tile of the second reads the first's output of its
-// expert and waits for it through the per-expert counters g1.dep (zeroed here).
+// expert and waits for it through the per-expert counters g1.dep (zeroed here,
+// unless counters_zeroed).
+// counters_zeroed: g1.dep is already zero (cleared by the launch just before
+// on the stream), so no memset is issued between the two launches.
 moe_status_t launch_grouped_gemm_chain(const moe_layer_desc_t& d, const GemmArgs& g1,
-                                       const GemmArgs& g2, cudaStream_t st);
+                                       const GemmArgs& g2, cudaStream_t st,
+                                       bool counters_zeroed = false);
 
 }  // namespace moe

@@ -129,8 +129,11 @@ template <int KMAX>
 __global__ void __launch_bounds__(256, KMAX <= 8 ? 3 : 1) combine_bwd_kernel(
     const bf16* __restrict__ dy, const bf16* __restrict__ o, const int32_t* __restrict__ slot,
     const float* __restrict__ gates, bf16* __restrict__ d_o, float* __restrict__ dgates, int T,
-    int H, int k, long long N, int tpr) {
+    int H, int k, long long N, int tpr, int* __restrict__ zero, int nzero) {
   pdl_wait();
+  // the next launch's counters (see launch_combine_bwd)
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   __shared__ float s_part[8][KMAX];
   const RowMap m = row_map(tpr);
   const bool active = m.t < T;
@@ -290,7 +293,7 @@ moe_status_t launch_combine(const moe_layer_desc_t& d, const bf16* o, const int3
 
 moe_status_t launch_combine_bwd(const moe_layer_desc_t& d, const bf16* dy, const bf16* o,
                                 const int32_t* slot, const float* gates, bf16* d_o,
-                                float* dgates, cudaStream_t st) {
+                                float* dgates, cudaStream_t st, int* zero, int nzero) {
   if (d.T == 0) return MOE_OK;
   const int tpr = threads_per_row(d.H);
   const dim3 grid(ceil_div(d.T, 256 / tpr));
@@ -299,31 +302,31 @@ moe_status_t launch_combine_bwd(const moe_layer_desc_t& d, const bf16* dy, const
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
       launch_k(combine_bwd_kernel<2>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
-               d.k, N, tpr);
+               d.k, N, tpr, zero, nzero);
     }
   else if (d.k <= 4)
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
       launch_k(combine_bwd_kernel<4>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
-               d.k, N, tpr);
+               d.k, N, tpr, zero, nzero);
     }
   else if (d.k <= 8)
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
       launch_k(combine_bwd_kernel<8>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
-               d.k, N, tpr);
+               d.k, N, tpr, zero, nzero);
     }
   else if (d.k <= 16)
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
       launch_k(combine_bwd_kernel<16>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
-               d.k, N, tpr);
+               d.k, N, tpr, zero, nzero);
     }
   else
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
       launch_k(combine_bwd_kernel<32>, grid, 256, 0, st, dy, o, slot, gates, d_o, dgates, d.T, d.H,
-               d.k, N, tpr);
+               d.k, N, tpr, zero, nzero);
     }
   return check_launch("combine_bwd_kernel");
 }

@@ -386,8 +386,12 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) dispatch_fused_kernel(
     int32_t* __restrict__ cnt, int32_t* __restrict__ off, int32_t* __restrict__ slot,
     int32_t* __restrict__ row_src, int32_t* __restrict__ cnt_re, int32_t* __restrict__ rank_off,
     bf16* __restrict__ x_perm, int* __restrict__ fhist, int* __restrict__ bar,
-    int* __restrict__ status, int T, int H, int E, int k, int R, int forced, uint64_t wait_ns) {
+    int* __restrict__ status, int T, int H, int E, int k, int R, int forced, uint64_t wait_ns,
+    int* __restrict__ zero, int nzero) {
   pdl_wait();
+  // the next launch's counters (see launch_dispatch_fused)
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   constexpr int TB = 4 * TPL;
   static_assert(TB <= 32, "one warp holds a tile's tokens");
   extern __shared__ __align__(16) uint8_t route_smem[];
@@ -880,7 +884,7 @@ cudaError_t launch_fused_t(const moe_layer_desc_t& d, const bf16* x, const bf16*
                            const float* bias, float* z, int32_t* idx, float* gates, int32_t* cnt,
                            int32_t* off, int32_t* slot, int32_t* row_src, int32_t* cnt_re,
                            int32_t* rank_off, bf16* x_perm, int* fhist, int* bar, int* status,
-                           cudaStream_t st) {
+                           cudaStream_t st, int* zero, int nzero) {
   const int forced = d.mode == MOE_ROUTE_FORCED_BALANCED;
   const size_t smem = route_tile_smem<TPL, HC>() + kFusedExtraInts * sizeof(int);
   // resident blocks per SM, looked up once (with the shared-memory attribute)
@@ -914,7 +918,8 @@ cudaError_t launch_fused_t(const moe_layer_desc_t& d, const bf16* x, const bf16*
   return cudaLaunchKernelEx(&cfg, dispatch_fused_kernel<TPL, HC>, x, w_r, bias, z, idx, gates, cnt,
                             off, slot, row_src, cnt_re, rank_off, x_perm, fhist, bar, status,
                             d.T, d.H, d.E, d.k, d.R, forced,
-                            (uint64_t)g_barrier_wait_ns.load(std::memory_order_relaxed));
+                            (uint64_t)g_barrier_wait_ns.load(std::memory_order_relaxed), zero,
+                            nzero);
 }
 
 template <int KMAX, bool FUSED, int COLS>
@@ -967,7 +972,7 @@ moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, con
                                    const float* bias, float* z, int32_t* idx, float* gates,
                                    int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
                                    int32_t* cnt_re, int32_t* rank_off, bf16* x_perm, int* fhist,
-                                   int* bar, int* status, cudaStream_t st) {
+                                   int* bar, int* status, cudaStream_t st, int* zero, int nzero) {
   if (d.T == 0 || d.E > kRouteEb) return MOE_ERR_UNSUPPORTED;
   // tokens per lane as for the router alone: about one wave of one block per SM
   const int per_sm = ceil_div(d.T, 4 * device_sm_count());
@@ -979,9 +984,11 @@ moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, con
   case n:                                                                                     \
     e = d.H % 128 == 0                                                                        \
             ? launch_fused_t<n, 128>(d, x, w_r, bias, z, idx, gates, cnt, off, slot, row_src, \
-                                     cnt_re, rank_off, x_perm, fhist, bar, status, st)        \
+                                     cnt_re, rank_off, x_perm, fhist, bar, status, st, zero,  \
+                                     nzero)                                                   \
             : launch_fused_t<n, 64>(d, x, w_r, bias, z, idx, gates, cnt, off, slot, row_src,  \
-                                    cnt_re, rank_off, x_perm, fhist, bar, status, st);        \
+                                    cnt_re, rank_off, x_perm, fhist, bar, status, st, zero,   \
+                                    nzero);                                                   \
     break;
     switch (tpl) {
       MOE_FUSED_CASE(1)
