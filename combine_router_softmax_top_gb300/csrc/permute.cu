@@ -84,47 +84,86 @@ __device__ __forceinline__ RowMap row_map(int tpr) {
 constexpr int kMaxKBatch = 8;
 
 // y[t] = bf16(sum_j g[t,j] * o[slot[t,j]]), fp32 in ascending j.
+// A block takes groups of 256/tpr tokens in turn (grid-stride). The routing
+// state of a group (slots and gates) is staged in shared memory, and the next
+// group's is loaded while the current group's rows are in flight, so a token
+// costs one round trip to memory instead of a routing-state load followed by
+// the row loads that depend on it.
+template <int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(const bf16* __restrict__ o,
                                                       const int32_t* __restrict__ slot,
                                                       const float* __restrict__ gates,
                                                       bf16* __restrict__ y, int T, int H, int k,
                                                       long long N, int tpr) {
   pdl_wait();
-  const RowMap m = row_map(tpr);
-  if (m.t >= T) return;
+  constexpr int KB = KMAX < kMaxKBatch ? KMAX : kMaxKBatch;
+  __shared__ int s_slot[2][32 * KMAX];  // tpr >= 8 (H >= 64): at most 32 tokens a group
+  __shared__ float s_g[2][32 * KMAX];
+  const int tpb = blockDim.x / tpr;  // tokens per group
+  const int lt = threadIdx.x / tpr, sub = threadIdx.x % tpr;
   const int cpr = H / 8;
-  for (int c = m.sub; c < cpr; c += tpr) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j0 = 0; j0 < k; j0 += kMaxKBatch) {
-      const int nj = min(kMaxKBatch, k - j0);
-      uint4 v[kMaxKBatch];
-      float g[kMaxKBatch];
-#pragma unroll
-      for (int u = 0; u < kMaxKBatch; ++u) {
-        v[u] = make_uint4(0, 0, 0, 0);
-        g[u] = 0.f;
-        if (u < nj) {
-          const int s = slot[(size_t)m.t * k + j0 + u];
-          g[u] = gates[(size_t)m.t * k + j0 + u];
-          if (s >= 0 && s < N) v[u] = __ldcs(reinterpret_cast<const uint4*>(o + (size_t)s * H) + c);
-        }
+  const int ngroups = (T + tpb - 1) / tpb;
+  const int nent = tpb * k;
+  auto stage = [&](int buf, int grp) {
+    const long long e0 = (long long)grp * tpb * k;
+    for (int i = threadIdx.x; i < nent; i += blockDim.x) {
+      const long long e = e0 + i;
+      int sv = -1;
+      float gv = 0.f;
+      if (grp < ngroups && e < N) {
+        sv = slot[e];
+        gv = gates[e];
       }
-#pragma unroll
-      for (int u = 0; u < kMaxKBatch; ++u) {
-        if (u < nj) {
-          float f[8];
-          unpack8(v[u], f);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = fmaf(g[u], f[q], acc[q]);
-        }
-      }
+      s_slot[buf][i] = sv >= 0 && sv < N ? sv : -1;
+      s_g[buf][i] = gv;
     }
-    reinterpret_cast<uint4*>(y + (size_t)m.t * H)[c] = pack8(acc);
+  };
+  int buf = 0;
+  stage(0, blockIdx.x);
+  __syncthreads();
+  for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x, buf ^= 1) {
+    const int t = grp * tpb + lt;
+    const int* sl = s_slot[buf] + lt * k;
+    const float* gl = s_g[buf] + lt * k;
+    bool next_staged = false;
+    for (int c = sub; c < cpr; c += tpr) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+      for (int j0 = 0; j0 < KMAX; j0 += KB) {
+        uint4 v[KB];
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          const int j = j0 + u;
+          const int sv = (t < T && j < k) ? sl[j] : -1;
+          v[u] = sv >= 0 ? __ldcs(reinterpret_cast<const uint4*>(o + (size_t)sv * H) + c)
+                         : make_uint4(0, 0, 0, 0);
+        }
+        if (!next_staged) {  // the next group's routing state, beside the row loads
+          stage(buf ^ 1, grp + gridDim.x);
+          next_staged = true;
+        }
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          const int j = j0 + u;
+          if (j < k) {
+            float f[8];
+            unpack8(v[u], f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = fmaf(gl[j], f[q], acc[q]);
+          }
+        }
+      }
+      if (t < T) reinterpret_cast<uint4*>(y + (size_t)t * H)[c] = pack8(acc);
+    }
+    if (!next_staged) stage(buf ^ 1, grp + gridDim.x);
+    __syncthreads();
   }
 }
 
 // d_o[slot[t,j]] = bf16(g[t,j] * dy[t]); dgates[t,j] = <dy[t], o[slot[t,j]]>.
 // The dot product is reduced over the token's threads in a fixed tree order.
+// Token groups are taken in turn with their routing state staged in shared
+// memory, the next group's loaded beside the current rows (as in combine).
 template <int KMAX>
 __global__ void __launch_bounds__(256, KMAX <= 8 ? 3 : 1) combine_bwd_kernel(
     const bf16* __restrict__ dy, const bf16* __restrict__ o, const int32_t* __restrict__ slot,
@@ -135,85 +174,111 @@ __global__ void __launch_bounds__(256, KMAX <= 8 ? 3 : 1) combine_bwd_kernel(
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   __shared__ float s_part[8][KMAX];
-  const RowMap m = row_map(tpr);
-  const bool active = m.t < T;
+  __shared__ int s_slot[2][32 * KMAX];  // tpr >= 8 (H >= 64): at most 32 tokens a group
+  __shared__ float s_g[2][32 * KMAX];
+  const int tpb = blockDim.x / tpr;
+  const int lt = threadIdx.x / tpr, sub = threadIdx.x % tpr;
   const int cpr = H / 8;
-  float dot[KMAX];
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) dot[j] = 0.f;
-  int sj[KMAX];
-  float gj[KMAX];
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    sj[j] = -1;
-    gj[j] = 0.f;
-    if (active && j < k) {
-      const int s = slot[(size_t)m.t * k + j];
-      sj[j] = (s >= 0 && s < N) ? s : -1;
-      gj[j] = gates[(size_t)m.t * k + j];
+  const int ngroups = (T + tpb - 1) / tpb;
+  const int nent = tpb * k;
+  auto stage = [&](int buf, int grp) {
+    const long long e0 = (long long)grp * tpb * k;
+    for (int i = threadIdx.x; i < nent; i += blockDim.x) {
+      const long long e = e0 + i;
+      int sv = -1;
+      float gv = 0.f;
+      if (grp < ngroups && e < N) {
+        sv = slot[e];
+        gv = gates[e];
+      }
+      s_slot[buf][i] = sv >= 0 && sv < N ? sv : -1;
+      s_g[buf][i] = gv;
     }
-  }
-  if (active) {
-    for (int c = m.sub; c < cpr; c += tpr) {
-      float fy[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(dy + (size_t)m.t * H) + c), fy);
+  };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int buf = 0;
+  stage(0, blockIdx.x);
+  __syncthreads();
+  for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x, buf ^= 1) {
+    const int t = grp * tpb + lt;
+    const bool active = t < T;
+    const int* sl = s_slot[buf] + lt * k;
+    const float* gl = s_g[buf] + lt * k;
+    float dot[KMAX];
 #pragma unroll
-      for (int j0 = 0; j0 < KMAX; j0 += kMaxKBatch) {  // 8 rows of o in flight
-        uint4 ov[kMaxKBatch];
+    for (int j = 0; j < KMAX; ++j) dot[j] = 0.f;
+    bool next_staged = false;
+    if (active) {
+      for (int c = sub; c < cpr; c += tpr) {
+        float fy[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dy + (size_t)t * H) + c), fy);
 #pragma unroll
-        for (int u = 0; u < kMaxKBatch; ++u) {
-          const int j = j0 + u;
-          ov[u] = (j < KMAX && sj[j < KMAX ? j : 0] >= 0 && j < k)
-                      ? __ldcs(reinterpret_cast<const uint4*>(o + (size_t)sj[j] * H) + c)
-                      : make_uint4(0, 0, 0, 0);
-        }
+        for (int j0 = 0; j0 < KMAX; j0 += kMaxKBatch) {  // 8 rows of o in flight
+          uint4 ov[kMaxKBatch];
 #pragma unroll
-        for (int u = 0; u < kMaxKBatch; ++u) {
-          const int j = j0 + u;
-          if (j < KMAX && j < k && sj[j] >= 0) {
-            float fo[8], prod[8];
-            unpack8(ov[u], fo);
-            float d = 0.f;
+          for (int u = 0; u < kMaxKBatch; ++u) {
+            const int j = j0 + u;
+            const int sv = (j < KMAX && j < k) ? sl[j] : -1;
+            ov[u] = sv >= 0 ? __ldcs(reinterpret_cast<const uint4*>(o + (size_t)sv * H) + c)
+                            : make_uint4(0, 0, 0, 0);
+          }
+          if (!next_staged) {  // the next group's routing state, beside the row loads
+            stage(buf ^ 1, grp + gridDim.x);
+            next_staged = true;
+          }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              d = fmaf(fy[q], fo[q], d);
-              prod[q] = gj[j] * fy[q];
+          for (int u = 0; u < kMaxKBatch; ++u) {
+            const int j = j0 + u;
+            if (j < KMAX && j < k) {
+              const int sv = sl[j];
+              if (sv >= 0) {
+                float fo[8], prod[8];
+                unpack8(ov[u], fo);
+                float d = 0.f;
+                const float gj = gl[j];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  d = fmaf(fy[q], fo[q], d);
+                  prod[q] = gj * fy[q];
+                }
+                dot[j] += d;
+                __stcs(reinterpret_cast<uint4*>(d_o + (size_t)sv * H) + c, pack8(prod));
+              }
             }
-            dot[j] += d;
-            __stcs(reinterpret_cast<uint4*>(d_o + (size_t)sj[j] * H) + c, pack8(prod));
           }
         }
       }
     }
-  }
-  // reduce dot[] over the tpr threads of the token
-  const int width = tpr < 32 ? tpr : 32;
+    if (!next_staged) stage(buf ^ 1, grp + gridDim.x);
+    // reduce dot[] over the tpr threads of the token
+    const int width = tpr < 32 ? tpr : 32;
 #pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
 #pragma unroll
-    for (int o2 = 16; o2; o2 >>= 1)
-      if (o2 < width) dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], o2, width);
-  }
-  if (tpr <= 32) {
-    if (active && m.sub == 0) {
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (j < k) dgates[(size_t)m.t * k + j] = dot[j];
+      for (int o2 = 16; o2; o2 >>= 1)
+        if (o2 < width) dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], o2, width);
     }
-    return;
-  }
-  // tpr > 32: the token's tpr/32 warps combine their sums in warp order
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
+    if (tpr <= 32) {
+      if (active && sub == 0) {
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) s_part[warp][j] = dot[j];
-  }
-  __syncthreads();
-  const int wbase = (threadIdx.x / tpr) * (tpr / 32);
-  if (active && m.sub < k) {
-    float sum = 0.f;
-    for (int w = 0; w < tpr / 32; ++w) sum += s_part[wbase + w][m.sub];
-    dgates[(size_t)m.t * k + m.sub] = sum;
+        for (int j = 0; j < KMAX; ++j)
+          if (j < k) dgates[(size_t)t * k + j] = dot[j];
+      }
+    } else {
+      // tpr > 32: the token's tpr/32 warps combine their sums in warp order
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) s_part[warp][j] = dot[j];
+      }
+      __syncthreads();
+      const int wbase = lt * (tpr / 32);
+      if (active && sub < k) {
+        float sum = 0.f;
+        for (int w = 0; w < tpr / 32; ++w) sum += s_part[wbase + w][sub];
+        dgates[(size_t)t * k + sub] = sum;
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -279,14 +344,39 @@ moe_status_t launch_permute(const moe_layer_desc_t& d, const bf16* x, const int3
   return check_launch("permute_kernel");
 }
 
+// One wave of resident blocks (looked up once per instantiation), each taking
+// token groups in turn.
+template <int KMAX>
+cudaError_t launch_combine_t(const moe_layer_desc_t& d, int groups, const bf16* o,
+                             const int32_t* slot, const float* gates, bf16* y, long long N,
+                             int tpr, cudaStream_t st) {
+  static int per_sm = 0;
+  static const cudaError_t occ =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<KMAX>, 256, 0);
+  if (occ != cudaSuccess) return occ;
+  const int grid = std::min(groups, std::max(per_sm, 1) * device_sm_count());
+  return launch_k(combine_kernel<KMAX>, grid, 256, 0, st, o, slot, gates, y, d.T, d.H, d.k, N,
+                  tpr);
+}
+
 moe_status_t launch_combine(const moe_layer_desc_t& d, const bf16* o, const int32_t* slot,
                             const float* gates, bf16* y, cudaStream_t st) {
   if (d.T == 0) return MOE_OK;
   const int tpr = threads_per_row(d.H);
+  const long long N = (long long)d.T * d.k;
+  const int groups = ceil_div(d.T, 256 / tpr);
+  cudaError_t e;
   {
     LaunchScope _ls(K_COMBINE, st);
-    launch_k(combine_kernel, ceil_div(d.T, 256 / tpr), 256, 0, st, o, slot, gates, y, d.T, d.H, d.k,
-             (long long)d.T * d.k, tpr);
+    if (d.k <= 2) e = launch_combine_t<2>(d, groups, o, slot, gates, y, N, tpr, st);
+    else if (d.k <= 4) e = launch_combine_t<4>(d, groups, o, slot, gates, y, N, tpr, st);
+    else if (d.k <= 8) e = launch_combine_t<8>(d, groups, o, slot, gates, y, N, tpr, st);
+    else if (d.k <= 16) e = launch_combine_t<16>(d, groups, o, slot, gates, y, N, tpr, st);
+    else e = launch_combine_t<32>(d, groups, o, slot, gates, y, N, tpr, st);
+  }
+  if (e != cudaSuccess) {
+    set_error("combine_kernel launch: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
   }
   return check_launch("combine_kernel");
 }
@@ -296,8 +386,11 @@ moe_status_t launch_combine_bwd(const moe_layer_desc_t& d, const bf16* dy, const
                                 float* dgates, cudaStream_t st, int* zero, int nzero) {
   if (d.T == 0) return MOE_OK;
   const int tpr = threads_per_row(d.H);
-  const dim3 grid(ceil_div(d.T, 256 / tpr));
   const long long N = (long long)d.T * d.k;
+  // one wave of resident blocks (3 per SM for k <= 8, else 1), each taking
+  // token groups in turn
+  const int groups = ceil_div(d.T, 256 / tpr);
+  const dim3 grid(std::min(groups, (d.k <= 8 ? 3 : 1) * device_sm_count()));
   if (d.k <= 2)
     {
       LaunchScope _ls(K_COMBINE_BWD, st);
