@@ -86,8 +86,8 @@ def algorithmic(d) -> dict:
         "route_bwd_dx": (T * H * b4 + E * H * b2 + 3 * N * b4, T * H * b2, 2.0 * N * H),
         # permute backward fused with the router's dx pass (the layer path)
         "dispatch_bwd": (N * H * b2 + 3 * N * b4 + E * H * b2, T * H * b2 + N * b4, 3.0 * N * H),
-        "route_bwd_dwr_partial": (T * H * b2 + 2 * N * b4, 0, 2.0 * N * H),
-        "route_bwd_dwr_reduce": (E * H * b4, 0, 0.0),
+        # dW_r: chunk partials and their per-expert sum in one launch
+        "route_bwd_dwr": (T * H * b2 + 2 * N * b4, E * H * b4, 2.0 * N * H),
         "gemm_fc1_fwd": (N * H * b2 + E * 2 * F * H * b2, N * 2 * F * b2 + N * F * b2,
                          2.0 * N * H * 2 * F),
         "gemm_fc2_fwd": (N * F * b2 + E * H * F * b2, N * H * b2, 2.0 * N * F * H),

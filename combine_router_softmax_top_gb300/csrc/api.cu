@@ -91,6 +91,9 @@ int device_sm_count() {
   return n > 0 ? n : 1;
 }
 
+// ints of the ws counter area (see WsLayout::dep)
+int dep_ints(const moe_layer_desc_t& d) { return d.E + d.E * ceil_div(d.H / 8, 256); }
+
 WsLayout ws_layout(const moe_layer_desc_t& d) {
   WsLayout w;
   const long long N = (long long)d.T * d.k;
@@ -108,7 +111,7 @@ WsLayout ws_layout(const moe_layer_desc_t& d) {
   w.dwr_part = o;
   o = align256(o + (size_t)chunks * d.H * sizeof(float));
   w.dep = o;
-  o = align256(o + (size_t)d.E * sizeof(int));
+  o = align256(o + (size_t)dep_ints(d) * sizeof(int));
   w.fhist = o;  // fused dispatch: per-tile expert counts (tiles of >= 4 tokens) + totals
   o = align256(o + ((size_t)(d.T + 3) / 4 + 1) * d.E * sizeof(int));
   w.bar = o;
@@ -267,15 +270,17 @@ moe_status_t op_wgrad(const moe_layer_desc_t& d, const bf16* x_perm, const bf16*
   return op_wgrad_one(d, GEMM_WGRAD_W2, d_o, h, off, dw2, main_dw2, ws, max_ctas, st);
 }
 
+// cnt_zeroed: dW_r's chunk counters in ws were cleared by an earlier launch
+// on the stream (the layer path's combine backward), so no memset is issued.
 moe_status_t op_route_bwd(const moe_layer_desc_t& d, const float* dgates, const float* gates,
                           const int32_t* idx, const bf16* x, const bf16* w_r,
                           const int32_t* row_src, const int32_t* off, const float* dx32,
                           const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dw_r,
-                          void* ws, cudaStream_t st) {
+                          void* ws, cudaStream_t st, bool cnt_zeroed = false) {
   const WsLayout w = ws_layout(d);
   return launch_route_bwd(d, dgates, gates, idx, x, w_r, row_src, off, dx32, dx_perm, slot, dx,
                           dw_r, ws_at<float>(ws, w.dz), ws_at<float>(ws, w.dwr_part),
-                          status_of(ws), st);
+                          ws_at<int>(ws, w.dep) + d.E, cnt_zeroed, status_of(ws), st);
 }
 
 // Route + dispatch layout + permute: one cooperative launch when the block
@@ -322,11 +327,12 @@ moe_status_t op_combine_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cu
 
 moe_status_t op_combine_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b,
                                cudaStream_t st) {
-  // it also clears the dgrad chain's counters (op_dgrad_mb relies on it)
+  // it also clears the dgrad chain's counters and dW_r's chunk counters
+  // (op_dgrad_mb and op_dispatch_bwd_mb rely on it)
   return launch_combine_bwd(d, reinterpret_cast<const bf16*>(b->dy),
                             reinterpret_cast<const bf16*>(b->o), b->slot, b->gates,
                             reinterpret_cast<bf16*>(b->d_o), b->dgates, st,
-                            ws_at<int>(b->ws, ws_layout(d).dep), d.E);
+                            ws_at<int>(b->ws, ws_layout(d).dep), dep_ints(d));
 }
 
 moe_status_t op_dgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
@@ -345,7 +351,8 @@ moe_status_t op_dispatch_bwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* 
   return op_route_bwd(d, b->dgates, b->gates, b->idx, reinterpret_cast<const bf16*>(b->x),
                       reinterpret_cast<const bf16*>(b->w_r), b->row_src, b->off, nullptr,
                       reinterpret_cast<const bf16*>(b->dx_perm), b->slot,
-                      reinterpret_cast<bf16*>(b->dx), b->dw_r, b->ws, st);
+                      reinterpret_cast<bf16*>(b->dx), b->dw_r, b->ws, st,
+                      /*cnt_zeroed=*/true);
 }
 
 moe_status_t op_wgrad_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,

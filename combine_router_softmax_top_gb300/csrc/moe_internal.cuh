@@ -26,6 +26,8 @@ constexpr int kLayoutTokensPerBlock = 256;
 constexpr int kRouteBwdRowsPerChunk = 64;
 
 struct WsLayout {
+  // dep: the GEMM chains' per-expert counters [E], then dW_r's per-expert,
+  // per-column-block chunk counters [E * ceil(H / 2048)]
   size_t status, logits, hist, dz, dwr_part, dep, fhist, bar, total;
 };
 WsLayout ws_layout(const moe_layer_desc_t& d);
@@ -35,7 +37,7 @@ inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 // ---------------------------------------------------------------- launch accounting
 enum KernelId {
   K_ROUTE_LOGITS = 0, K_ROUTE_TOPK, K_LAYOUT_COUNT, K_LAYOUT_ASSIGN, K_PERMUTE, K_COMBINE,
-  K_COMBINE_BWD, K_PERMUTE_BWD, K_ROUTE_BWD_DX, K_ROUTE_BWD_DWR_PARTIAL, K_ROUTE_BWD_DWR_REDUCE,
+  K_COMBINE_BWD, K_PERMUTE_BWD, K_ROUTE_BWD_DX, K_ROUTE_BWD_DWR,
   K_GEMM_FC1_FWD, K_GEMM_FC2_FWD, K_GEMM_FC2_DGRAD, K_GEMM_FC1_DGRAD, K_GEMM_WGRAD_W1,
   K_GEMM_WGRAD_W2, K_DISPATCH_BWD, K_GEMM_FFN_FWD, K_GEMM_FFN_DGRAD, K_DISPATCH_FUSED,
   K_GEMM_WGRAD_W1_ACC, K_GEMM_WGRAD_W2_ACC, K_LAYOUT_SCAN, K_EP_RESORT, K_NUM
@@ -139,7 +141,8 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
                               const int32_t* idx, const bf16* x, const bf16* w_r,
                               const int32_t* row_src, const int32_t* off, const float* dx32,
                               const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dw_r,
-                              float* dz, float* dwr_part, int* status, cudaStream_t st);
+                              float* dz, float* dwr_part, int* dwr_cnt, bool cnt_zeroed,
+                              int* status, cudaStream_t st);
 
 // Expert-parallel receive re-sort (receive order <-> expert-major) of n_rows
 // rows of H bf16; recv_cnt [R][E/R] on the device; off_local [E/R + 1] or NULL.

@@ -728,20 +728,58 @@ __device__ int find_chunk(const int32_t* __restrict__ off, int E, int chunk, int
   return 1;
 }
 
-// Pass A: partial[chunk][h] = sum over the chunk's rows s (ascending) of
-// dz[row_src[s]] * x[row_src[s] div k][h]. The chunk's sources and weights are
-// staged in shared memory first, so each thread then has 8 independent x-row
-// loads in flight instead of a chain of dependent loads per row.
-__global__ void __launch_bounds__(256) route_bwd_dwr_partial_kernel(
+// dW_r, in one launch. A block takes one chunk of an expert's rows and one
+// column block of 2048 columns: partial[chunk][h] = sum over the chunk's rows s
+// (ascending) of dz[row_src[s]] * x[row_src[s] div k][h]. The chunk's sources
+// and weights are staged in shared memory first, so each thread then has 8
+// independent x-row loads in flight instead of a chain of dependent loads per
+// row. The block that completes an expert (a per-expert, per-column-block
+// counter, counted after each block's partial is visible) then adds the
+// expert's partials in chunk order: dW_r[e][h] = sum_i partial[first + i][h],
+// a fixed order whatever the order in which the chunks finish, and resets the
+// counter. Blocks past the last chunk write zeros for the experts without
+// rows, one each (there are always enough of them: the grid has
+// ceil(N / 64) + E blocks along x).
+__global__ void __launch_bounds__(256) route_bwd_dwr_kernel(
     const int32_t* __restrict__ off, const int32_t* __restrict__ row_src,
-    const float* __restrict__ dz, const bf16* __restrict__ x, float* __restrict__ part, int T,
-    int H, int E, int k, int* status) {
+    const float* __restrict__ dz, const bf16* __restrict__ x, float* __restrict__ part,
+    float* __restrict__ dw_r, int* __restrict__ cnt, int T, int H, int E, int k,
+    int* status) {
   pdl_wait();
   extern __shared__ int s_prefix[];
   __shared__ int s_tok[kRouteBwdRowsPerChunk];
   __shared__ float s_w[kRouteBwdRowsPerChunk];
+  __shared__ int s_sel;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;  // 16-byte chunk of the row
+  const bool col_ok = c * 8 < H;
   int e, r0, r1;
-  if (!find_chunk(off, E, blockIdx.x, &e, &r0, &r1, s_prefix)) return;
+  if (!find_chunk(off, E, blockIdx.x, &e, &r0, &r1, s_prefix)) {
+    // a spare block: the j-th expert without rows, if there is one, gets zeros
+    const int j = blockIdx.x - s_prefix[E];
+    if (threadIdx.x < 32) {
+      int seen = 0, pick = -1;
+      for (int base = 0; base < E && pick < 0; base += 32) {
+        const int ee = base + threadIdx.x;
+        const bool empty = ee < E && off[ee + 1] == off[ee];
+        const unsigned m = __ballot_sync(0xffffffffu, empty);
+        const int n = __popc(m);
+        if (j >= seen && j < seen + n) {
+          unsigned mm = m;
+          for (int q = 0; q < j - seen; ++q) mm &= mm - 1;  // drop the lower empties
+          pick = base + __ffs(mm) - 1;
+        }
+        seen += n;
+      }
+      if (threadIdx.x == 0) s_sel = pick;
+    }
+    __syncthreads();
+    if (s_sel >= 0 && col_ok) {
+      float4* dst = reinterpret_cast<float4*>(dw_r + (size_t)s_sel * H + c * 8);
+      dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
   const long long N = (long long)T * k;
   const int n = r1 - r0;
   if ((int)threadIdx.x < n) {
@@ -751,66 +789,58 @@ __global__ void __launch_bounds__(256) route_bwd_dwr_partial_kernel(
     s_w[threadIdx.x] = ok ? dz[src] : 0.f;
   }
   __syncthreads();
-  const int c = blockIdx.y * blockDim.x + threadIdx.x;  // 16-byte chunk of the row
-  if (c * 8 >= H) return;
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int s0 = 0; s0 < n; s0 += 8) {
-    uint4 v[8];
+  if (col_ok) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int s0 = 0; s0 < n; s0 += 8) {
+      uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int tok = s0 + u < n ? s_tok[s0 + u] : -1;
-      v[u] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H) + c)
-                      : make_uint4(0, 0, 0, 0);
-    }
+      for (int u = 0; u < 8; ++u) {
+        const int tok = s0 + u < n ? s_tok[s0 + u] : -1;
+        v[u] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H) + c)
+                        : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (s0 + u < n) {
-        const float w = s_w[s0 + u];
-        const uint32_t q4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      for (int u = 0; u < 8; ++u) {
+        if (s0 + u < n) {
+          const float w = s_w[s0 + u];
+          const uint32_t q4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[2 * q] = fmaf(w, bf16_bits_to_f32(q4[q] & 0xFFFFu), acc[2 * q]);
-          acc[2 * q + 1] = fmaf(w, bf16_bits_to_f32(q4[q] >> 16), acc[2 * q + 1]);
+          for (int q = 0; q < 4; ++q) {
+            acc[2 * q] = fmaf(w, bf16_bits_to_f32(q4[q] & 0xFFFFu), acc[2 * q]);
+            acc[2 * q + 1] = fmaf(w, bf16_bits_to_f32(q4[q] >> 16), acc[2 * q + 1]);
+          }
         }
       }
     }
+    float4* dst = reinterpret_cast<float4*>(part + (size_t)blockIdx.x * H + c * 8);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
-  float4* dst = reinterpret_cast<float4*>(part + (size_t)blockIdx.x * H + c * 8);
-  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-}
-
-// Pass B: dW_r[e][h] = sum of expert e's chunk partials in chunk order (0 if none).
-__global__ void __launch_bounds__(256) route_bwd_dwr_reduce_kernel(
-    const int32_t* __restrict__ off, const float* __restrict__ part, float* __restrict__ dw_r,
-    int H, int E) {
-  pdl_wait();
-  __shared__ int s_first, s_n;
-  const int e = blockIdx.x;
-  if (threadIdx.x < 32) {
-    // chunks of experts 0..e-1, summed by one warp
-    int sum = 0;
-    for (int i = threadIdx.x; i < e; i += 32)
-      sum += (off[i + 1] - off[i] + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (threadIdx.x == 0) {
-      s_first = sum;
-      s_n = (off[e + 1] - off[e] + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk;
-    }
-  }
+  // publish this partial; the expert's last chunk to finish sums them all
+  __threadfence();
   __syncthreads();
-  const int c = blockIdx.y * blockDim.x + threadIdx.x;
-  if (c * 4 >= H) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = 0; i < s_n; ++i) {
-    const float4 p = *reinterpret_cast<const float4*>(part + (size_t)(s_first + i) * H + c * 4);
-    acc.x += p.x;
-    acc.y += p.y;
-    acc.z += p.z;
-    acc.w += p.w;
+  const int first = s_prefix[e];
+  const int nch = (n > 0 ? (off[e + 1] - off[e] + kRouteBwdRowsPerChunk - 1) /
+                               kRouteBwdRowsPerChunk
+                         : 0);
+  int* ctr = cnt + (size_t)e * gridDim.y + blockIdx.y;
+  if (threadIdx.x == 0) s_sel = atomicAdd(ctr, 1) == nch - 1;
+  __syncthreads();
+  if (!s_sel) return;
+  __threadfence();
+  if (col_ok) {
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    for (int i = 0; i < nch; ++i) {
+      const float4* p4 = reinterpret_cast<const float4*>(part + (size_t)(first + i) * H + c * 8);
+      const float4 p0 = __ldcg(p4), p1 = __ldcg(p4 + 1);
+      a0.x += p0.x; a0.y += p0.y; a0.z += p0.z; a0.w += p0.w;
+      a1.x += p1.x; a1.y += p1.y; a1.z += p1.z; a1.w += p1.w;
+    }
+    float4* dst = reinterpret_cast<float4*>(dw_r + (size_t)e * H + c * 8);
+    dst[0] = a0;
+    dst[1] = a1;
   }
-  *reinterpret_cast<float4*>(dw_r + (size_t)e * H + c * 4) = acc;
+  if (threadIdx.x == 0) *ctr = 0;  // ready for the next launch
 }
 
 }  // namespace
@@ -1014,7 +1044,8 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
                               const int32_t* idx, const bf16* x, const bf16* w_r,
                               const int32_t* row_src, const int32_t* off, const float* dx32,
                               const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dw_r,
-                              float* dz, float* dwr_part, int* status, cudaStream_t st) {
+                              float* dz, float* dwr_part, int* dwr_cnt, bool cnt_zeroed,
+                              int* status, cudaStream_t st) {
   const bool fused = dx_perm != nullptr;
   const int cpr = d.H / 8;
   if (d.T > 0) {
@@ -1035,22 +1066,21 @@ moe_status_t launch_route_bwd(const moe_layer_desc_t& d, const float* dgates, co
   }
   const long long N = (long long)d.T * d.k;
   const int max_chunks = (int)((N + kRouteBwdRowsPerChunk - 1) / kRouteBwdRowsPerChunk) + d.E;
-  if (N > 0) {
-    dim3 ga(max_chunks, ceil_div(cpr, 256));
-    {
-      LaunchScope _ls(K_ROUTE_BWD_DWR_PARTIAL, st);
-      launch_k(route_bwd_dwr_partial_kernel, ga, 256, (d.E + 1) * sizeof(int), st, off, row_src, dz,
-               x, dwr_part, d.T, d.H, d.E, d.k, status);
+  const int ncb = ceil_div(cpr, 256);  // column blocks of 2048 columns
+  if (!cnt_zeroed) {
+    cudaError_t e = cudaMemsetAsync(dwr_cnt, 0, (size_t)d.E * ncb * sizeof(int), st);
+    if (e != cudaSuccess) {
+      set_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
     }
-    moe_status_t s = check_launch("route_bwd_dwr_partial_kernel");
-    if (s != MOE_OK) return s;
   }
-  dim3 gb(d.E, ceil_div(d.H / 4, 256));
+  dim3 ga(max_chunks, ncb);
   {
-    LaunchScope _ls(K_ROUTE_BWD_DWR_REDUCE, st);
-    launch_k(route_bwd_dwr_reduce_kernel, gb, 256, 0, st, off, dwr_part, dw_r, d.H, d.E);
+    LaunchScope _ls(K_ROUTE_BWD_DWR, st);
+    launch_k(route_bwd_dwr_kernel, ga, 256, (d.E + 1) * sizeof(int), st, off, row_src, dz, x,
+             dwr_part, dw_r, dwr_cnt, d.T, d.H, d.E, d.k, status);
   }
-  return check_launch("route_bwd_dwr_reduce_kernel");
+  return check_launch("route_bwd_dwr_kernel");
 }
 
 }  // namespace moe
