@@ -45,7 +45,7 @@ struct CopyLane {
   // moe_layer_steps_host: a second copy stream (device to host) and, per
   // input slot, the events of its pipeline
   cudaStream_t d2h = nullptr;
-  cudaEvent_t in_ready[2] = {}, fwd_s[2] = {}, dx_s[2] = {}, step_done[2] = {}, out_done[2] = {};
+  cudaEvent_t in_ready[2] = {}, step_done[2] = {}, out_done[2] = {};
   // moe_layer_backward's side stream: the weight gradients run on it beside
   // the dispatch backward (they depend on the dgrad only, not on each other)
   cudaStream_t side = nullptr;
@@ -69,7 +69,7 @@ CopyLane* copy_lane() {
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&l.side, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&l.d2h, cudaStreamNonBlocking);
     for (int s = 0; s < 2; ++s)
-      for (cudaEvent_t* ev : {&l.in_ready[s], &l.fwd_s[s], &l.dx_s[s], &l.step_done[s],
+      for (cudaEvent_t* ev : {&l.in_ready[s], &l.step_done[s],
                               &l.out_done[s]})
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     for (cudaEvent_t* ev : {&l.start, &l.dy_in, &l.fwd_done, &l.y_out, &l.dx_ready, &l.fork,
@@ -716,7 +716,10 @@ moe_status_t moe_layer_steps_host(const moe_layer_desc_t* d, const moe_mb_bufs_t
   // computes (after step i-2, the slot's last user, has finished reading
   // them), and its y, dx come out on the second copy stream while step i+1
   // computes; step i waits for its inputs and for step i-2's outputs to have
-  // left the slot's y and dx
+  // left the slot's y and dx. The outputs go out once the whole step is done:
+  // an event recorded between two of the step's kernels (as soon as y, or dx,
+  // is written) would stop the next kernel's launch from overlapping the
+  // previous one's drain, and the copies overlap the next step anyway.
   auto upload = [&](int i) {
     const int s = i & 1;
     if (i >= 2) ok(cudaStreamWaitEvent(cl->stream, cl->step_done[s], 0));
@@ -737,15 +740,12 @@ moe_status_t moe_layer_steps_host(const moe_layer_desc_t* d, const moe_mb_bufs_t
     if (i >= 2) ok(cudaStreamWaitEvent(st, cl->out_done[s], 0));
     if (e != cudaSuccess) break;
     MOE_CHECK(moe_layer_forward(d, &b[s], stream));
-    ok(cudaEventRecord(cl->fwd_s[s], st));
-    ok(cudaStreamWaitEvent(cl->d2h, cl->fwd_s[s], 0));
+    MOE_CHECK(layer_backward(d, &b[s], 1, st, nullptr));
+    ok(cudaEventRecord(cl->step_done[s], st));
+    ok(cudaStreamWaitEvent(cl->d2h, cl->step_done[s], 0));
     ok(cudaMemcpyAsync(host_y[i], b[s].y, bytes, cudaMemcpyDeviceToHost, cl->d2h));
-    if (e != cudaSuccess) break;
-    MOE_CHECK(layer_backward(d, &b[s], 1, st, cl->dx_s[s]));
-    ok(cudaStreamWaitEvent(cl->d2h, cl->dx_s[s], 0));
     ok(cudaMemcpyAsync(host_dx[i], b[s].dx, bytes, cudaMemcpyDeviceToHost, cl->d2h));
     ok(cudaEventRecord(cl->out_done[s], cl->d2h));
-    ok(cudaEventRecord(cl->step_done[s], st));
   }
   for (int s = 0; s < 2 && s < n; ++s) ok(cudaStreamWaitEvent(st, cl->out_done[s], 0));
   ok(cudaStreamSynchronize(st));
