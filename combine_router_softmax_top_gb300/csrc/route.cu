@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) dispatch_fused_kernel(
 // ------------------------------------------------------------------ backward
 // dz_j = g_j (dg_j - <g, dg>) on the chosen set;
 // dx = bf16(dx32 + sum_j dz_j * w_r[i_j]), j ascending.
-// A block owns kDxTok tokens x one slice of COLS columns of the row: the
+// A block owns `tok` tokens x one slice of COLS columns of the row: the
 // slice of w_r (E x COLS) is staged in shared memory once, so the k expert
 // rows a token adds come from shared memory instead of k gathers through L2.
 // The block's routing state (k experts, slots, gates and gate gradients of
@@ -563,16 +563,20 @@ __global__ void __launch_bounds__(kRouteNw * 32, 1) dispatch_fused_kernel(
 // tokens' row loads in flight per thread took 61 us: the registers they need
 // cut the blocks per SM from four to two. Blocks that kept their slice and
 // took token blocks in turn, with the next one's routing state loaded beside
-// the current rows (as the combine kernels do), took 45 us.
-constexpr int kDxTok = 64;  // tokens per block
+// the current rows (as the combine kernels do), took 45 us. The launcher picks
+// the tokens per block that fill whole waves of resident blocks (112 there:
+// 592 blocks on 608 slots, 37 us), since a partly filled last wave costs more
+// than longer blocks: 64 tokens per block (1.7 waves) took 41 us, 96 and 128
+// (1.1 and 0.84 waves) 47 us.
+constexpr int kDxTokMax = 128;  // tokens per block, at most
 constexpr int kDxCols = 128;  // columns per slice when H allows (else 64)
 // bytes per staged w_r slice row, for a slice of COLS columns
 __host__ __device__ constexpr int dx_pitch(int cols) { return cols * 2 + 16; }
 
 // dynamic shared memory of the dx kernel: the w_r slice, then per routed
 // entry of the block's tokens its expert, slot, gate and dz
-__host__ __device__ constexpr size_t dx_smem_bytes(int cols, int E, int k) {
-  return (size_t)E * dx_pitch(cols) + (size_t)kDxTok * k * 16;
+__host__ __device__ constexpr size_t dx_smem_bytes(int cols, int E, int k, int tok) {
+  return (size_t)E * dx_pitch(cols) + (size_t)tok * k * 16;
 }
 
 template <int KMAX, bool FUSED, int COLS>
@@ -580,19 +584,19 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     const float* __restrict__ dgates, const float* __restrict__ gates,
     const int32_t* __restrict__ idx, const bf16* __restrict__ w_r, const float* __restrict__ dx32,
     const bf16* __restrict__ dx_perm, const int32_t* __restrict__ slot, bf16* __restrict__ dx,
-    float* __restrict__ dz, int T, int H, int E, int k, int* status) {
+    float* __restrict__ dz, int T, int H, int E, int k, int* status, int tok) {
   pdl_wait();
   constexpr int KB = KMAX < 8 ? KMAX : 8;  // row loads per batch
   constexpr int LANES = COLS / 8;            // threads per token: 16 bytes of the slice each
   constexpr int TPP = 256 / LANES;           // tokens per pass of the block
   constexpr int PITCH = dx_pitch(COLS);
   extern __shared__ __align__(16) uint8_t s_wr[];  // [E][PITCH], then the routing state
-  int* s_e = reinterpret_cast<int*>(s_wr + (size_t)E * PITCH);  // [kDxTok * k]
-  int* s_slot = s_e + kDxTok * k;
-  float* s_g = reinterpret_cast<float*>(s_slot + kDxTok * k);
-  float* s_dz = s_g + kDxTok * k;  // dg while staged, then dz
-  const int t0 = blockIdx.y * kDxTok;
-  const int nt = min(kDxTok, T - t0);
+  int* s_e = reinterpret_cast<int*>(s_wr + (size_t)E * PITCH);  // [tok * k]
+  int* s_slot = s_e + tok * k;
+  float* s_g = reinterpret_cast<float*>(s_slot + tok * k);
+  float* s_dz = s_g + tok * k;  // dg while staged, then dz
+  const int t0 = blockIdx.y * tok;
+  const int nt = min(tok, T - t0);
   const int nent = nt * k;
   const size_t tk0 = (size_t)t0 * k;
   const long long N = (long long)T * k;
@@ -959,15 +963,29 @@ cudaError_t launch_dx_c(const moe_layer_desc_t& d, const float* dgates, const fl
                         const int32_t* idx, const bf16* w_r, const float* dx32,
                         const bf16* dx_perm, const int32_t* slot, bf16* dx, float* dz,
                         int* status, cudaStream_t st) {
-  const dim3 g(d.H / COLS, ceil_div(d.T, kDxTok));
-  const size_t smem = dx_smem_bytes(COLS, d.E, d.k);
   // E <= 256, k <= 32: allow the largest once per instantiation
   static const cudaError_t attr = cudaFuncSetAttribute(
       route_bwd_dx_kernel<KMAX, FUSED, COLS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)dx_smem_bytes(COLS, 256, 32));
+      (int)dx_smem_bytes(COLS, 256, 32, kDxTokMax));
   if (attr != cudaSuccess) return attr;
+  // tokens per block: the fewest waves of resident blocks that hold the layer
+  // with at most kDxTokMax tokens a block, then the fewest whole passes of
+  // the block's threads (TPP tokens each) that fill those waves
+  constexpr int TPP = 256 / (COLS / 8);  // tokens per pass
+  int per_sm = 0;
+  const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, route_bwd_dx_kernel<KMAX, FUSED, COLS>, 256,
+      dx_smem_bytes(COLS, d.E, d.k, kDxTokMax));
+  if (oe != cudaSuccess) return oe;
+  const int slices = d.H / COLS;
+  const int per_slice = std::max(1, std::max(per_sm, 1) * device_sm_count() / slices);
+  const int waves = ceil_div(d.T, per_slice * kDxTokMax);
+  int tok = ceil_div(ceil_div(d.T, waves * per_slice), TPP) * TPP;
+  tok = std::min(std::max(tok, TPP), kDxTokMax);
+  const dim3 g(slices, ceil_div(d.T, tok));
+  const size_t smem = dx_smem_bytes(COLS, d.E, d.k, tok);
   return launch_k(route_bwd_dx_kernel<KMAX, FUSED, COLS>, g, 256, smem, st, dgates, gates, idx,
-                  w_r, dx32, dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status);
+                  w_r, dx32, dx_perm, slot, dx, dz, d.T, d.H, d.E, d.k, status, tok);
 }
 
 // slices of kDxCols columns when H allows, else of 64 (H is a multiple of 64)
