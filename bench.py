@@ -97,9 +97,11 @@ def algorithmic(d) -> dict:
         "gemm_wgrad_w1": (N * 2 * F * b2 + N * H * b2, E * 2 * F * H * b2, 2.0 * N * 2 * F * H),
         "gemm_wgrad_w2": (N * H * b2 + N * F * b2, E * H * F * b2, 2.0 * N * H * F),
     }
-    # FC1 then FC2 forward, and FC2 then FC1 dgrad, as one chained launch each
+    # FC1 then FC2 forward, FC2 then FC1 dgrad, and the two weight gradients,
+    # as one launch each
     for chain, (m1, m2) in (("gemm_ffn_fwd", ("gemm_fc1_fwd", "gemm_fc2_fwd")),
-                            ("gemm_ffn_dgrad", ("gemm_fc2_dgrad", "gemm_fc1_dgrad"))):
+                            ("gemm_ffn_dgrad", ("gemm_fc2_dgrad", "gemm_fc1_dgrad")),
+                            ("gemm_wgrad", ("gemm_wgrad_w1", "gemm_wgrad_w2"))):
         out[chain] = tuple(x + y for x, y in zip(out[m1], out[m2]))
     return out
 

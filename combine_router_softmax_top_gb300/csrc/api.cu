@@ -266,6 +266,24 @@ moe_status_t op_wgrad_one(const moe_layer_desc_t& d, int mode, const bf16* A, co
 moe_status_t op_wgrad(const moe_layer_desc_t& d, const bf16* x_perm, const bf16* h,
                       const bf16* d_o, const bf16* da, const int32_t* off, bf16* dw1, bf16* dw2,
                       float* main_dw1, float* main_dw2, void* ws, int max_ctas, cudaStream_t st) {
+  if (!main_dw1 && !main_dw2 && (long long)d.T * d.k > 0) {
+    // both weight gradients in one persistent launch (bf16 outputs)
+    GemmArgs g1 = {};
+    g1.mode = GEMM_WGRAD_W1;
+    g1.A = da;
+    g1.B = x_perm;
+    g1.off = off;
+    g1.out0 = dw1;
+    g1.status = status_of(ws);
+    g1.max_ctas = max_ctas;
+    GemmArgs g2 = g1;
+    g2.mode = GEMM_WGRAD_W2;
+    g2.A = d_o;
+    g2.B = h;
+    g2.out0 = nullptr;
+    g2.out1 = dw2;
+    return launch_grouped_gemm_chain(d, g1, g2, st);
+  }
   MOE_CHECK(op_wgrad_one(d, GEMM_WGRAD_W1, da, x_perm, off, dw1, main_dw1, ws, max_ctas, st));
   return op_wgrad_one(d, GEMM_WGRAD_W2, d_o, h, off, dw2, main_dw2, ws, max_ctas, st);
 }

@@ -374,6 +374,9 @@ struct Fuse {
   using A = Mode<MODE>;
   using B = Mode<(MODE2 >= 0 ? MODE2 : MODE)>;
   static constexpr bool kHas2 = MODE2 >= 0;
+  // the second mode reads the first mode's output (forward and dgrad chains);
+  // the two weight gradients of a wgrad launch are independent of each other
+  static constexpr bool kDep = kHas2 && !A::kRagK;
   static constexpr bool kAux = A::kAux || (kHas2 && B::kAux);
   static constexpr int kStages = A::kStages < B::kStages ? A::kStages : B::kStages;
   static constexpr int kStageBytes = A::kStageBytes;
@@ -953,7 +956,8 @@ __global__ void __launch_bounds__(Fuse<MODE, MODE2>::kWarps * 32, 1)
       } else {
         const Tile t = tile2(tile);
         // the A operand of this tile is the first mode's output for expert t.e
-        if (lane == 0) {
+        ok = true;
+        if (F::kDep && lane == 0) {
           const int target = 8 * F::kCS * (ctl.tstart[t.e + 1] - ctl.tstart[t.e]);
           ok = wait_expert(p, t.e, target, &ctl.abort);
           if (!ok) flag_timeout(ctl, p.status, 10);
@@ -968,7 +972,7 @@ __global__ void __launch_bounds__(Fuse<MODE, MODE2>::kWarps * 32, 1)
     // ================================================================ MMA issuer
     // (pair mode: only the even CTA issues, for both CTAs)
     // (K-ragged launches: the whole warp, which zeroes the tail rows of A)
-    constexpr bool kWarpMma = Mode<MODE>::kRagK && !F::kHas2;
+    constexpr bool kWarpMma = Mode<MODE>::kRagK;
     if ((kWarpMma || lane == 0) && !(F::kPair && R.crank != 0)) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
@@ -1043,7 +1047,7 @@ __global__ void __launch_bounds__(Fuse<MODE, MODE2>::kWarps * 32, 1)
       ++ti;
       bool ok;
       if (!F::kHas2 || tile < total1)
-        ok = epilogue_tile<MODE, KS, F::kAuxBytes, F::kHas2, ACC>(R, p, &tmD, tile1(tile), acc,
+        ok = epilogue_tile<MODE, KS, F::kAuxBytes, F::kDep, ACC>(R, p, &tmD, tile1(tile), acc,
                                                                acc_phase, aux_phase, ew, ti);
       else
         ok = epilogue_tile<MODE_B, KS, F::kAuxBytes, false, false>(R, p2, &tmD2, tile2(tile), acc,
@@ -1323,17 +1327,24 @@ moe_status_t launch_grouped_gemm_chain(const moe_layer_desc_t& d, const GemmArgs
   if (N == 0) return MOE_OK;
   const bool fwd = g1.mode == GEMM_FC1_FWD && g2.mode == GEMM_FC2_FWD;
   const bool dgrad = g1.mode == GEMM_FC2_DGRAD && g2.mode == GEMM_FC1_DGRAD;
-  if (!fwd && !dgrad) {
+  const bool wgrad = g1.mode == GEMM_WGRAD_W1 && g2.mode == GEMM_WGRAD_W2 && !g1.acc && !g2.acc;
+  if (!fwd && !dgrad && !wgrad) {
     set_error("unsupported grouped GEMM chain %d -> %d", g1.mode, g2.mode);
-    return MOE_ERR_INVALID_ARG;
-  }
-  if (!g1.dep) {
-    set_error("a grouped GEMM chain needs its per-expert counters");
     return MOE_ERR_INVALID_ARG;
   }
   CUtensorMap m1[4], m2[4];
   KParams p1, p2;
   long long b1 = 0, b2 = 0;
+  if (wgrad) {
+    // two independent weight gradients: W2's tiles fill W1's last round
+    if (!mode_setup(d, g1, m1, p1, b1) || !mode_setup(d, g2, m2, p2, b2)) return MOE_ERR_CUDA;
+    return launch_mode<GEMM_WGRAD_W1, GEMM_WGRAD_W2>(m1, m2, p1, p2, grid_for(g1, b1 + b2),
+                                                     K_GEMM_WGRAD, st);
+  }
+  if (!g1.dep) {
+    set_error("a grouped GEMM chain needs its per-expert counters");
+    return MOE_ERR_INVALID_ARG;
+  }
   if (!mode_setup(d, g1, m1, p1, b1) || !mode_setup(d, g2, m2, p2, b2)) return MOE_ERR_CUDA;
   p2.dep = p1.dep;
   // the counters start at zero for every launch: cleared here unless the

@@ -40,7 +40,7 @@ enum KernelId {
   K_COMBINE_BWD, K_PERMUTE_BWD, K_ROUTE_BWD_DX, K_ROUTE_BWD_DWR,
   K_GEMM_FC1_FWD, K_GEMM_FC2_FWD, K_GEMM_FC2_DGRAD, K_GEMM_FC1_DGRAD, K_GEMM_WGRAD_W1,
   K_GEMM_WGRAD_W2, K_DISPATCH_BWD, K_GEMM_FFN_FWD, K_GEMM_FFN_DGRAD, K_DISPATCH_FUSED,
-  K_GEMM_WGRAD_W1_ACC, K_GEMM_WGRAD_W2_ACC, K_LAYOUT_SCAN, K_EP_RESORT, K_NUM
+  K_GEMM_WGRAD_W1_ACC, K_GEMM_WGRAD_W2_ACC, K_LAYOUT_SCAN, K_EP_RESORT, K_GEMM_WGRAD, K_NUM
 };
 
 // Wraps one kernel launch: counts it and, while profiling is on, brackets it
@@ -173,10 +173,12 @@ struct GemmArgs {
   float* acc;         // wgrad: fp32 gradient to add the result into (out0/out1 unused), else NULL
 };
 moe_status_t launch_grouped_gemm(const moe_layer_desc_t& d, const GemmArgs& g, cudaStream_t st);
-// Two dependent GEMMs in one persistent launch: FC1 fwd then FC2 fwd, or FC2
-// dgrad then FC1 dgrad. A tile of the second reads the first's output of its
-// expert and waits for it through the per-expert counters g1.dep (zeroed here,
-// unless counters_zeroed).
+// Two GEMMs in one persistent launch: FC1 fwd then FC2 fwd, or FC2 dgrad then
+// FC1 dgrad (dependent), or the weight gradients W1 then W2 (independent; bf16
+// outputs only, and N > 0: for an empty layer the single-mode launches write
+// the zero gradients). A tile of a dependent second GEMM reads the first's
+// output of its expert and waits for it through the per-expert counters
+// g1.dep (zeroed here, unless counters_zeroed).
 // counters_zeroed: g1.dep is already zero (cleared by the launch just before
 // on the stream), so no memset is issued between the two launches.
 moe_status_t launch_grouped_gemm_chain(const moe_layer_desc_t& d, const GemmArgs& g1,

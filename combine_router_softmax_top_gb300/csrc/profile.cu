@@ -17,7 +17,7 @@ const char* const kNames[K_NUM] = {
     "combine", "combine_bwd", "permute_bwd", "route_bwd_dx", "route_bwd_dwr", "gemm_fc1_fwd", "gemm_fc2_fwd", "gemm_fc2_dgrad",
     "gemm_fc1_dgrad", "gemm_wgrad_w1", "gemm_wgrad_w2", "dispatch_bwd", "gemm_ffn_fwd",
     "gemm_ffn_dgrad", "dispatch_fused", "gemm_wgrad_w1_accum", "gemm_wgrad_w2_accum",
-    "layout_scan", "ep_resort"};
+    "layout_scan", "ep_resort", "gemm_wgrad"};
 
 std::atomic<unsigned long long> g_launches{0};
 
