@@ -114,8 +114,9 @@ def kernel_stats(agg: dict, algo: dict, pk: dict, wr_gbs: float) -> dict:
         avg_ms = tot / n
         rd, wr, fl = algo.get(name, (0.0, 0.0, 0.0))
         by = rd + wr
-        # HBM floor with writes counted at the write-only rate: a kernel that
-        # mostly writes (the weight gradients) cannot reach the copy bandwidth
+        # HBM floor: all bytes at the copy rate, or the written bytes at the
+        # live write-only rate where that takes longer (a write-only stream is
+        # faster than a copy on this part, so for these kernels it never does)
         t_floor = max(by / (pk["hbm_gbs"] * 1e9), wr / (wr_gbs * 1e9))
         gbs = by / (avg_ms * 1e-3) / 1e9 if avg_ms > 0 else 0.0
         tfl = fl / (avg_ms * 1e-3) / 1e12 if avg_ms > 0 else 0.0
@@ -151,8 +152,10 @@ def accum_algorithmic(d) -> dict:
 
 
 def hbm_write_gbs(dev) -> float:
-    """Write-only HBM bandwidth, measured live: best of 5 zero-fills of 1 GiB."""
-    buf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    """Write-only HBM bandwidth, measured live: best of 5 zero-fills of 1 GiB in
+    8-byte elements (a fill of 1-byte elements issues narrow stores and reaches
+    only about half the rate on this part)."""
+    buf = torch.empty(1 << 27, dtype=torch.int64, device=dev)
     best = float("inf")
     for i in range(8):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -411,6 +414,7 @@ def measure_workload(moe, wl: str, args, dev, st, pk, wr_gbs, steps: int) -> dic
     d = moe.LayerDesc.of(**shape)
     b = moe.LayerBuffers(d, dev)
     b.load_inputs(inp)
+    torch.cuda.synchronize(dev)  # the loads ran on torch's stream, the steps run on st
 
     def step():
         moe.moe_layer_forward(d, b, st)
@@ -437,9 +441,92 @@ def measure_workload(moe, wl: str, args, dev, st, pk, wr_gbs, steps: int) -> dic
            **gemm_summary(ks, agg, algo, min(steps, 20), pk),
            "kernels": {n: {k: v[k] for k in ("avg_us", "bound", "roofline_frac", "hbm_floor_frac",
                                              "GB_s", "TFLOP_s")} for n, v in ks.items()}}
+    out["experts_by_rows"] = rows_histogram(cnt)
     del b
     torch.cuda.empty_cache()
     return out
+
+
+BUCKET_ROWS = (64, 128, 256, 512, 1024, 2048, 4096)
+
+
+def rows_histogram(cnt) -> dict:
+    """Experts and their rows per bucket [M, 2M) of BUCKET_ROWS (the first
+    bucket also takes fewer rows, the last more)."""
+    hist = {}
+    for i, m in enumerate(BUCKET_ROWS):
+        lo = 0 if i == 0 else m
+        hi = BUCKET_ROWS[i + 1] if i + 1 < len(BUCKET_ROWS) else 1 << 30
+        sel = (cnt >= lo) & (cnt < hi)
+        hist[str(m)] = {"experts": int(sel.sum()), "rows": int(cnt[sel].sum())}
+    return hist
+
+
+def measure_expert_buckets(moe, args, dev, st, pk, wr_gbs, skew_hist=None) -> dict:
+    """Grouped-GEMM efficiency by rows per expert: all 128 experts of the
+    Qwen3-30B-A3B-shaped layer (H=2048, F=768, k=8) with M rows each
+    (T = 16 M tokens), for M in BUCKET_ROWS. The forward chain, the dgrad chain
+    and the weight gradients are each timed through their C-ABI calls with
+    CUDA events, on random operands, and rated against the same rooflines as
+    in the layer step. The skewed workload's experts are counted into the same
+    buckets, so its GEMM time can be read against these rates."""
+    E, H, F, k = 128, 2048, 768, 8
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    rows = []
+    for M in BUCKET_ROWS:
+        T = E * M // k
+        shape = {"T": T, "H": H, "E": E, "k": k, "F": F, "R": 1, "mode": 1}
+        d = moe.LayerDesc.of(T=T, H=H, E=E, k=k, F=F)
+        b = moe.LayerBuffers(d, dev)
+        for t, std in ((b.x_perm, 1.0), (b.w1, 0.02), (b.w2, 0.02), (b.d_o, 0.01)):
+            t.copy_(torch.randn(t.shape, generator=gen, device=dev, dtype=torch.float32) * std)
+        b.off.copy_(torch.arange(E + 1, device=dev, dtype=torch.int32) * M)
+        torch.cuda.synchronize(dev)  # the fills ran on torch's stream, the calls run on st
+        calls = {
+            "gemm_ffn_fwd": lambda: moe.moe_expert_ffn_fwd(d, b.x_perm, b.off, b.w1, b.w2, b.a, b.h,
+                                                           b.o, b.ws, st),
+            "gemm_ffn_dgrad": lambda: moe.moe_expert_ffn_bwd_dgrad(d, b.d_o, b.a, b.off, b.w1, b.w2,
+                                                                   b.da, b.dx_perm, b.ws, st),
+            "gemm_wgrad": lambda: moe.moe_expert_ffn_bwd_wgrad(d, b.x_perm, b.h, b.d_o, b.da, b.off,
+                                                               b.dw1, b.dw2, b.ws, st),
+        }
+        n = max(3, 20 // max(1, M // 512))
+        agg = {}
+        for name, call in calls.items():  # in this order: each reads what the one before wrote
+            for _ in range(max(args.warmup, 3)):
+                call()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(n):
+                call()
+            e1.record(st)
+            torch.cuda.synchronize(dev)
+            agg[name] = [n, e0.elapsed_time(e1)]
+        status = moe.moe_device_status(d, b.ws, st)
+        if status != moe.MOE_OK:
+            raise RuntimeError(f"buckets M={M}: device status {status}: "
+                               f"{moe.lib().moe_last_error()}")
+        algo = algorithmic(shape)
+        ks = kernel_stats(agg, algo, pk, wr_gbs)
+        ms = sum(v[1] / v[0] for v in agg.values())
+        fl = sum(algo[nm][2] for nm in agg)
+        row = {"rows_per_expert": M, "T": T,
+               "TFLOP_s": round(fl / (ms * 1e-3) / 1e12, 1),
+               "frac_of_bf16_sustained": round(fl / (ms * 1e-3) / 1e12
+                                               / pk["bf16_tflops_sustained"], 3),
+               "calls": {nm: {x: ks[nm][x] for x in ("avg_us", "bound", "roofline_frac",
+                                                     "hbm_floor_frac", "TFLOP_s")}
+                         for nm in agg}}
+        if skew_hist is not None:
+            row["skewed_layer"] = skew_hist[str(M)]
+        rows.append(row)
+        del b, calls
+        torch.cuda.empty_cache()
+    return {"note": "all 128 experts at M rows (T = 16 M); 'skewed_layer' counts the experts of "
+                    "the skewed workload with rows in [M, 2M) (the first bucket also takes "
+                    "fewer rows, the last more)",
+            "buckets": rows}
 
 
 def measure_schedule(moe, args, dev, steps: int) -> dict:
@@ -457,6 +544,7 @@ def measure_schedule(moe, args, dev, steps: int) -> dict:
     b0.load_inputs(i0)
     b1 = moe.LayerBuffers(d, dev, weights=b0)
     b1.load_inputs(i1, weights=False)
+    torch.cuda.synchronize(dev)  # the loads ran on torch's stream, the steps run on others
     sc = torch.cuda.Stream(device=dev, priority=-1)
     sg = torch.cuda.Stream(device=dev)
     res = {}
@@ -518,6 +606,7 @@ def run_ours(args, rank, world, local):
     d = moe.LayerDesc.of(**shape)
     b = moe.LayerBuffers(d, dev)
     b.load_inputs(inp)
+    torch.cuda.synchronize(dev)  # the loads ran on torch's stream, the steps run on st
     st = torch.cuda.Stream(device=dev)
 
     def step():
@@ -592,7 +681,8 @@ def run_ours(args, rank, world, local):
     else:
         roof = {"bound": "hbm", "achieved": kd["GB_s"], "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    # the same kernel against its HBM floor with writes at the write-only rate
+    # the same kernel against its HBM floor with the writes at the live
+    # write-only rate where that is the longer of the two
     roof["write_aware"] = {"hbm_write_gbs_live": round(wr_gbs, 1), "floor_us": kd["hbm_floor_us"],
                            "frac": kd["hbm_floor_frac"]}
     roof["traffic"] = traffic_for(dom, args.workload)
@@ -696,6 +786,8 @@ def run_ours(args, rank, world, local):
         sub = max(20, args.steps // 2)
         others["c3_skewed"] = measure_workload(moe, "qwen3_30b_a3b_skewed", args, dev, st, pk,
                                                wr_gbs, sub)
+        others["c3_expert_buckets"] = measure_expert_buckets(
+            moe, args, dev, st, pk, wr_gbs, others["c3_skewed"]["experts_by_rows"])
         others["c4_ep8"] = measure_workload(moe, "ep8_emulated", args, dev, st, pk, wr_gbs, sub)
         others["c5_schedule"] = measure_schedule(moe, args, dev, sub)
 
@@ -741,6 +833,16 @@ def run_ours(args, rank, world, local):
             "sample": f"first {Ts} tokens of the workload, one fwd+bwd, numpy float64 + BLAS, "
                       f"{allc['seconds']} s on {cores} threads",
             "one_thread": one}
+        if not args.no_configs:
+            # the other workloads' oracle, all threads: the small one whole, the
+            # others on the same token prefix (the two-micro-batch workload is
+            # two of the balanced layer, so its rate per token is the one above)
+            per = {}
+            for wl in ("tiny", "qwen3_30b_a3b_skewed", "ep8_emulated"):
+                import moe_synth
+                n = min(Ts, moe_synth.WORKLOADS[wl]["T"])
+                per[wl] = {**oracle_timing(wl, n, cores), "sample_tokens": n}
+            out["cpu_baseline"]["other_workloads"] = per
     if rank == 0:
         emit(out)
 
