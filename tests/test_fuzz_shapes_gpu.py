@@ -1,8 +1,9 @@
 """GPU parity over seeded random layer shapes: the whole layer and each stage of
 the CUDA path (through the C ABI) against the CPU oracle, as for the fixed
 cases, on shapes drawn from a fixed seed so that combinations the named cases
-do not cover (T, H, E, k, F, R and the routing mode together) get exercised.
-Each shape is in the test's id, so a failure can be rerun by itself."""
+do not cover (T, H, E, k, F, R and the routing mode together) get exercised,
+including token counts that give each block of the fused dispatch several
+tiles. Each shape is in the test's id, so a failure can be rerun by itself."""
 import numpy as np
 import pytest
 import torch
@@ -34,7 +35,28 @@ def _shapes(n=12, seed=2026):
     return out
 
 
-SHAPES = _shapes()
+def _shapes_many_tiles(n=6, seed=2027):
+    """Token counts past one tile per block of the fused dispatch (147 blocks
+    of 28 tokens), so blocks route, count and permute several tiles; small
+    hidden sizes keep the oracle quick."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.choice([8, 16, 32, 64, 96, 128]))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        T = int(rng.integers(4200, 12001))
+        H = 64 * int(rng.integers(1, 5))
+        F = 64 * int(rng.integers(1, 4))
+        forced = rng.random() < 0.3
+        bias = None if forced else rng.choice([None, "zipf_linear", "zipf_logrank"])
+        out.append(dict(T=T, H=H, E=E, k=k, F=F, R=1,
+                        mode=moe_synth.ROUTE_FORCED_BALANCED if forced
+                        else moe_synth.ROUTE_SOFTMAX_TOPK,
+                        bias=None if bias is None else str(bias), seed=200 + i))
+    return out
+
+
+SHAPES = _shapes() + _shapes_many_tiles()
 
 
 def _id(s):
