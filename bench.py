@@ -558,29 +558,37 @@ def measure_schedule(moe, args, dev, steps: int) -> dict:
         layer_pair()
     ms, spread = timed_steps(layer_pair, steps, sc)
     res["layer_calls_x2"] = {"ms_per_step": round(ms, 4), "spread_ms_per_step": spread}
-    for name, overlap, defer in (("serial", 0, 0), ("overlap", 1, 0), ("overlap_defer", 1, 1)):
-        s = moe.Scheduler(d, sc, sg)
+    # overlap = 2 overlaps only micro-batch 1's dispatch with micro-batch 0's
+    # expert forward; "_split" gives that forward 96 of the SMs and the
+    # dispatch the rest (the best split measured on this layer)
+    for name, overlap, defer, gemm_sms in (("serial", 0, 0, 0), ("overlap", 1, 0, 0),
+                                           ("overlap_defer", 1, 1, 0),
+                                           ("overlap_dispatch", 2, 0, 0),
+                                           ("overlap_dispatch_split", 2, 0, 96)):
+        s = moe.Scheduler(d, sc, sg, gemm_sms=gemm_sms)
         s.set_phase_timing(False)
         for _ in range(args.warmup):
-            s.step(b0, b1, overlap=bool(overlap), defer_wgrad=bool(defer))
-        ms, spread = timed_steps(lambda: s.step(b0, b1, overlap=bool(overlap),
+            s.step(b0, b1, overlap=overlap, defer_wgrad=bool(defer))
+        ms, spread = timed_steps(lambda: s.step(b0, b1, overlap=overlap,
                                                 defer_wgrad=bool(defer)), steps, sc)
         s.flush()
         # one more pass with the phase events on, for the interval analysis
         s.set_phase_timing(True)
-        s.step(b0, b1, overlap=bool(overlap), defer_wgrad=bool(defer))
+        s.step(b0, b1, overlap=overlap, defer_wgrad=bool(defer))
         comm, gemm, hidden = moe.interval_overlap(s.timings())
         s.flush()
         torch.cuda.synchronize(dev)
         s.close()
         res[name] = {"ms_per_step": round(ms, 4), "spread_ms_per_step": spread,
+                     "gemm_sms": gemm_sms,
                      "timed_pass": {"comm_union_ms": round(comm, 4),
                                     "gemm_union_ms": round(gemm, 4),
                                     "hidden_comm_ms": round(hidden, 4)}}
     for b in (b0, b1):
         if moe.moe_device_status(d, b.ws) != moe.MOE_OK:
             raise RuntimeError(f"schedule: device status: {moe.lib().moe_last_error()}")
-    best = min(("overlap", "overlap_defer"), key=lambda n: res[n]["ms_per_step"])
+    best = min(("overlap", "overlap_defer", "overlap_dispatch", "overlap_dispatch_split"),
+               key=lambda n: res[n]["ms_per_step"])
     out = {"config": {"workload": wl, **i0.shape_dict(), "micro_batches": 2},
            "steps": steps, "schedules": res, "best_overlap": best,
            "tokens_per_s_best_overlap": round(2 * i0.T / (res[best]["ms_per_step"] / 1e3), 1),

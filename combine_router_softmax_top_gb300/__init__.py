@@ -420,7 +420,7 @@ class Scheduler:
                                       ctypes.byref(h)), "moe_sched_create")
         self._h = h
 
-    def step(self, mb0: LayerBuffers, mb1: LayerBuffers, overlap: bool, defer_wgrad: bool):
+    def step(self, mb0: LayerBuffers, mb1: LayerBuffers, overlap, defer_wgrad: bool):
         arr = (MbBufs * 2)(mb0.struct(), mb1.struct())
         _check(lib().moe_sched_step(self._h, arr, int(overlap), int(defer_wgrad)), "moe_sched_step")
 

@@ -307,25 +307,26 @@ moe_status_t op_dispatch_all(const moe_layer_desc_t& d, const bf16* x, const bf1
                              const float* bias, float* logits, int32_t* idx, float* gates,
                              int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
                              int32_t* cnt_re, int32_t* rank_off, bf16* x_perm, void* ws,
-                             cudaStream_t st) {
+                             cudaStream_t st, int max_ctas = 0) {
   if (d.T > 0 && d.E <= 128) {
     const WsLayout w = ws_layout(d);
     float* z = logits ? logits : ws_at<float>(ws, w.logits);
     // it also clears the forward chain's counters (op_ffn_fwd_mb relies on it)
     return launch_dispatch_fused(d, x, w_r, bias, z, idx, gates, cnt, off, slot, row_src, cnt_re,
                                  rank_off, x_perm, ws_at<int>(ws, w.fhist), ws_at<int>(ws, w.bar),
-                                 status_of(ws), st, ws_at<int>(ws, w.dep), d.E);
+                                 status_of(ws), st, ws_at<int>(ws, w.dep), d.E, max_ctas);
   }
   MOE_CHECK(op_route(d, x, w_r, bias, logits, idx, gates, ws, st));
   MOE_CHECK(op_layout(d, idx, cnt, off, slot, row_src, cnt_re, rank_off, ws, st));
   return launch_permute(d, x, row_src, x_perm, st);
 }
 
-moe_status_t op_dispatch(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st) {
+moe_status_t op_dispatch(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st,
+                         int max_ctas) {
   return op_dispatch_all(d, reinterpret_cast<const bf16*>(b->x),
                          reinterpret_cast<const bf16*>(b->w_r), b->bias, b->logits, b->idx,
                          b->gates, b->cnt, b->off, b->slot, b->row_src, b->cnt_re, b->rank_off,
-                         reinterpret_cast<bf16*>(b->x_perm), b->ws, st);
+                         reinterpret_cast<bf16*>(b->x_perm), b->ws, st, max_ctas);
 }
 
 moe_status_t op_ffn_fwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,

@@ -109,12 +109,14 @@ moe_status_t launch_route(const moe_layer_desc_t& d, const bf16* x, const bf16* 
 // MOE_ERR_UNSUPPORTED otherwise). fhist: ws area of (ceil(T/4) + 1) * E ints;
 // bar: one int, zeroed by the launcher. zero/nzero: as for launch_combine_bwd
 // (the layer path clears there the counters of the forward chain that follows).
+// max_ctas > 0 caps the grid (blocks then take several token tiles each), so
+// the launch can share the GPU with a kernel on the other SMs.
 moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, const bf16* w_r,
                                    const float* bias, float* z, int32_t* idx, float* gates,
                                    int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
                                    int32_t* cnt_re, int32_t* rank_off, bf16* x_perm, int* fhist,
                                    int* bar, int* status, cudaStream_t st, int* zero = nullptr,
-                                   int nzero = 0);
+                                   int nzero = 0, int max_ctas = 0);
 // Dispatch layout in three launches. hist: (ceil(T/256) + 1) * E ints of
 // scratch (per-block expert counts, then the totals); fully rewritten.
 moe_status_t launch_layout(const moe_layer_desc_t& d, const int32_t* idx, int32_t* cnt,

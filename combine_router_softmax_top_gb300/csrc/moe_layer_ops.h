@@ -13,8 +13,9 @@ struct CopyLane;
 CopyLane* copy_lane();
 moe_status_t check_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, bool bwd);
 
-// route + dispatch layout + permute
-moe_status_t op_dispatch(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st);
+// route + dispatch layout + permute; max_ctas > 0 caps the fused launch's grid
+moe_status_t op_dispatch(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st,
+                         int max_ctas = 0);
 moe_status_t op_ffn_fwd_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, int max_ctas,
                            cudaStream_t st);
 moe_status_t op_combine_mb(const moe_layer_desc_t& d, const moe_mb_bufs_t* b, cudaStream_t st);

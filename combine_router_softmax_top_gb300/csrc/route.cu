@@ -920,7 +920,7 @@ cudaError_t launch_fused_t(const moe_layer_desc_t& d, const bf16* x, const bf16*
                            const float* bias, float* z, int32_t* idx, float* gates, int32_t* cnt,
                            int32_t* off, int32_t* slot, int32_t* row_src, int32_t* cnt_re,
                            int32_t* rank_off, bf16* x_perm, int* fhist, int* bar, int* status,
-                           cudaStream_t st, int* zero, int nzero) {
+                           cudaStream_t st, int* zero, int nzero, int max_ctas) {
   const int forced = d.mode == MOE_ROUTE_FORCED_BALANCED;
   const size_t smem = route_tile_smem<TPL, HC>() + kFusedExtraInts * sizeof(int);
   // resident blocks per SM, looked up once (with the shared-memory attribute)
@@ -938,7 +938,8 @@ cudaError_t launch_fused_t(const moe_layer_desc_t& d, const bf16* x, const bf16*
   cudaError_t e;
   // every block must be resident: at most one wave
   const int ntiles = ceil_div(d.T, 4 * TPL);
-  const int grid = std::min(ntiles, per_sm * device_sm_count());
+  int grid = std::min(ntiles, per_sm * device_sm_count());
+  if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   e = cudaMemsetAsync(bar, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1022,7 +1023,8 @@ moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, con
                                    const float* bias, float* z, int32_t* idx, float* gates,
                                    int32_t* cnt, int32_t* off, int32_t* slot, int32_t* row_src,
                                    int32_t* cnt_re, int32_t* rank_off, bf16* x_perm, int* fhist,
-                                   int* bar, int* status, cudaStream_t st, int* zero, int nzero) {
+                                   int* bar, int* status, cudaStream_t st, int* zero, int nzero,
+                                   int max_ctas) {
   if (d.T == 0 || d.E > kRouteEb) return MOE_ERR_UNSUPPORTED;
   // tokens per lane as for the router alone: about one wave of one block per SM
   const int per_sm = ceil_div(d.T, 4 * device_sm_count());
@@ -1035,10 +1037,10 @@ moe_status_t launch_dispatch_fused(const moe_layer_desc_t& d, const bf16* x, con
     e = d.H % 128 == 0                                                                        \
             ? launch_fused_t<n, 128>(d, x, w_r, bias, z, idx, gates, cnt, off, slot, row_src, \
                                      cnt_re, rank_off, x_perm, fhist, bar, status, st, zero,  \
-                                     nzero)                                                   \
+                                     nzero, max_ctas)                                         \
             : launch_fused_t<n, 64>(d, x, w_r, bias, z, idx, gates, cnt, off, slot, row_src,  \
                                     cnt_re, rank_off, x_perm, fhist, bar, status, st, zero,   \
-                                    nzero);                                                   \
+                                    nzero, max_ctas);                                         \
     break;
     switch (tpl) {
       MOE_FUSED_CASE(1)

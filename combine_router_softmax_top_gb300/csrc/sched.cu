@@ -15,6 +15,8 @@
 // order comes only from events on real data dependencies, so the results are
 // bit-identical to the serial order.
 #include <stdlib.h>
+
+#include <algorithm>
 #include <string.h>
 
 #include "moe_layer_ops.h"
@@ -96,7 +98,7 @@ moe_status_t run_phase(moe_sched* s, const moe_mb_bufs_t* b, int mb, int phase, 
   if (s->timing) SCHK(begin(s, mb, phase, stream_id, st, &r));
   const moe_layer_desc_t& d = s->d;
   switch (phase) {
-    case MOE_PHASE_DISPATCH: SCHK(op_dispatch(d, b, st)); break;
+    case MOE_PHASE_DISPATCH: SCHK(op_dispatch(d, b, st, max_ctas)); break;
     case MOE_PHASE_FFN_FWD: SCHK(op_ffn_fwd_mb(d, b, max_ctas, st)); break;
     case MOE_PHASE_COMBINE: SCHK(op_combine_mb(d, b, st)); break;
     case MOE_PHASE_COMBINE_BWD: SCHK(op_combine_bwd_mb(d, b, st)); break;
@@ -205,6 +207,49 @@ moe_status_t moe_sched_step(moe_sched_t* s, const moe_mb_bufs_t* mb, int32_t ove
 
   const int gs = s->gemm_sms;
   SCHK(wait(sg, s->ev_start));
+  if (overlap == 2) {
+    // Only micro-batch 1's dispatch runs beside micro-batch 0's work: its
+    // router phase is bound by FMA arithmetic and reads little, so it is the
+    // one phase that gains beside an HBM-bound GEMM. Everything else keeps the
+    // plain layer order F0 B0 F1 B1 on the GEMM stream, so consecutive
+    // kernels there keep their programmatic dependent launch; each weight
+    // gradient runs on the comm stream beside its dispatch backward, as
+    // moe_layer_backward runs it on its side stream. With gemm_sms > 0 the
+    // GPU is split for the one overlapped pair: expert forward 0 on gemm_sms
+    // SMs, dispatch 1 on the others; every other phase takes the whole GPU.
+    const int fwd0_ctas = gs > 0 ? gs : 0;
+    const int disp1_ctas = gs > 0 ? std::max(1, device_sm_count() - gs) : 0;
+    if (pend >= 0) {
+      SCHK(run_phase(s, &pend_bufs, pend, MOE_PHASE_WGRAD, sg, 1, 0));
+      SCHK(cuda_ok(cudaEventRecord(s->dep[D_WGPREV], sg), "cudaEventRecord"));
+    }
+    SCHK(run_phase(s, &mb[0], 0, MOE_PHASE_DISPATCH, sc, 0, 0));
+    SCHK(cuda_ok(cudaEventRecord(s->dep[D_DISP0], sc), "cudaEventRecord"));
+    // dispatch(1) rewrites micro-batch 1's saved tensors, which a deferred
+    // wgrad still reads
+    if (pend >= 0) SCHK(wait(sc, s->dep[D_WGPREV]));
+    SCHK(run_phase(s, &mb[1], 1, MOE_PHASE_DISPATCH, sc, 0, disp1_ctas));
+    SCHK(cuda_ok(cudaEventRecord(s->dep[D_DISP1], sc), "cudaEventRecord"));
+    for (int m = 0; m < 2; ++m) {
+      SCHK(wait(sg, s->dep[m == 0 ? D_DISP0 : D_DISP1]));
+      SCHK(run_phase(s, &mb[m], m, MOE_PHASE_FFN_FWD, sg, 1, m == 0 ? fwd0_ctas : 0));
+      SCHK(run_phase(s, &mb[m], m, MOE_PHASE_COMBINE, sg, 1, 0));
+      SCHK(run_phase(s, &mb[m], m, MOE_PHASE_COMBINE_BWD, sg, 1, 0));
+      SCHK(run_phase(s, &mb[m], m, MOE_PHASE_DGRAD, sg, 1, 0));
+      const Dep dg = m == 0 ? D_DGRAD0 : D_DGRAD1;
+      SCHK(cuda_ok(cudaEventRecord(s->dep[dg], sg), "cudaEventRecord"));
+      if (m == 1 && defer_wgrad) {
+        s->pending = 1;
+        s->pending_bufs = mb[1];
+      } else {
+        SCHK(wait(sc, s->dep[dg]));
+        SCHK(run_phase(s, &mb[m], m, MOE_PHASE_WGRAD, sc, 0, 0));
+      }
+      SCHK(run_phase(s, &mb[m], m, MOE_PHASE_DISPATCH_BWD, sg, 1, 0));
+    }
+    SCHK(cuda_ok(cudaEventRecord(s->dep[D_SG_END], sg), "cudaEventRecord"));
+    return wait(sc, s->dep[D_SG_END]);
+  }
   // t0: dispatch(0) on the comm stream; a deferred wgrad beside it
   SCHK(run_phase(s, &mb[0], 0, MOE_PHASE_DISPATCH, sc, 0, 0));
   SCHK(cuda_ok(cudaEventRecord(s->dep[D_DISP0], sc), "cudaEventRecord"));

@@ -479,8 +479,10 @@ typedef struct moe_sched moe_sched_t;
 
 /* Creates a scheduler for two micro-batches of shape d on two caller-owned
  * streams (stream_comm runs route/dispatch/combine and their backward,
- * stream_gemm the grouped GEMMs). gemm_sms caps the persistent GEMM grid while
- * overlapping (0 = all SMs). Allocates CUDA events only. */
+ * stream_gemm the grouped GEMMs). gemm_sms (0 = no cap): under overlap = 1 it
+ * caps every persistent GEMM grid; under overlap = 2 it splits the GPU for the
+ * one overlapped pair, micro-batch 0's expert forward on gemm_sms SMs and
+ * micro-batch 1's fused dispatch on the rest. Allocates CUDA events only. */
 moe_status_t moe_sched_create(const moe_layer_desc_t* d, void* stream_comm, void* stream_gemm,
                               int32_t gemm_sms, moe_sched_t** out);
 
@@ -489,9 +491,13 @@ moe_status_t moe_sched_create(const moe_layer_desc_t* d, void* stream_comm, void
  * the fp32 main gradients under MOE_FLAG_WGRAD_ACCUM_FP32, must not be, so
  * that the order of the fp32 additions does not depend on the schedule).
  * overlap = 0: every phase on stream_comm in the order F0 F1 B0 B1.
- * overlap = 1: phases spread over the two streams so one micro-batch's
- * dispatch/combine runs beside the other's GEMMs, ordered by events on data
- * dependencies only. defer_wgrad = 1: micro-batch 1's wgrad is not run in this
+ * overlap = 1 (or any value but 0 and 2): phases spread over the two streams
+ * so one micro-batch's dispatch/combine runs beside the other's GEMMs, ordered
+ * by events on data dependencies only.
+ * overlap = 2: only micro-batch 1's dispatch (its router phase is FMA-bound)
+ * runs beside micro-batch 0's work; the rest keeps the layer order
+ * F0 B0 F1 B1 on stream_gemm, each weight gradient on stream_comm beside its
+ * dispatch backward. defer_wgrad = 1: micro-batch 1's wgrad is not run in this
  * step but at the start of the next one (beside micro-batch 0's dispatch), or by
  * moe_sched_flush(). Outputs are bit-identical to the serial schedule's. */
 moe_status_t moe_sched_step(moe_sched_t* s, const moe_mb_bufs_t* mb, int32_t overlap,

@@ -57,7 +57,7 @@ def test_overlap_is_bit_identical_to_serial_and_matches_oracle():
     d, inps, bufs = make_pair(**SMALL)
     run(d, bufs, overlap=False, defer=False)
     ref = [collect(b, i) for b, i in zip(bufs, inps)]
-    for overlap, defer in ((True, False), (True, True), (False, True)):
+    for overlap, defer in ((True, False), (True, True), (False, True), (2, False), (2, True)):
         for b in bufs:
             for n in ("y", "dx", "dw1", "dw2", "dw_r", "a", "h", "o", "da", "d_o"):
                 getattr(b, n).zero_()
@@ -85,31 +85,54 @@ def test_timings_cover_every_phase_and_streams():
     assert comm > 0 and gemm > 0 and hidden >= 0
 
 
+def test_dispatch_only_overlap_timings():
+    # overlap = 2: both dispatches on the comm stream first, the rest of each
+    # micro-batch on the GEMM stream in layer order, each wgrad on the comm stream
+    d, inps, bufs = make_pair(**SMALL)
+    tm = run(d, bufs, overlap=2, defer=False, steps=1)
+    assert len(tm) == 14
+    for t in tm:
+        on_comm = t["phase"] in ("dispatch", "wgrad")
+        assert t["stream"] == (0 if on_comm else 1), t
+    order = [(t["mb"], t["phase"]) for t in tm if t["stream"] == 1]
+    assert order == [(m, p) for m in range(2) for p in
+                     ("ffn_fwd", "combine", "combine_bwd", "dgrad", "dispatch_bwd")]
+    start = {(t["mb"], t["phase"]): t["start_ms"] for t in tm}
+    end = {(t["mb"], t["phase"]): t["end_ms"] for t in tm}
+    for m in range(2):
+        assert start[(m, "ffn_fwd")] >= end[(m, "dispatch")]
+        assert start[(m, "wgrad")] >= end[(m, "dgrad")]
+
+
 @pytest.mark.slow
-def test_two_microbatch_workload_overlap_matches_serial():
+@pytest.mark.parametrize("overlap", [True, 2])
+def test_two_microbatch_workload_overlap_matches_serial(overlap):
     d, inps, bufs = make_pair("two_microbatch")
     run(d, bufs, overlap=False, defer=False, steps=1)
     ref = [collect(b, i) for b, i in zip(bufs, inps)]
-    run(d, bufs, overlap=True, defer=True, steps=1)
+    run(d, bufs, overlap=overlap, defer=True, steps=1)
     got = [collect(b, i) for b, i in zip(bufs, inps)]
     for m in range(2):
         for key in ref[m]:
             assert np.array_equal(got[m][key], ref[m][key]), (m, key)
 
 
-@pytest.mark.parametrize("gemm_sms", [8, 30, 120])
-def test_capped_gemm_grid_is_bit_identical(gemm_sms):
+@pytest.mark.parametrize("overlap,gemm_sms", [(True, 8), (True, 30), (True, 120), (2, 8),
+                                              (2, 112), (2, 150)])
+def test_capped_gemm_grid_is_bit_identical(overlap, gemm_sms):
     """With the GEMM grid capped, each CTA of a chained expert GEMM (FC1 -> FC2,
     FC2 dgrad -> FC1 dgrad) works through many rounds of tiles and the second
-    GEMM's tiles wait on other CTAs' first-GEMM tiles: same bits as uncapped."""
+    GEMM's tiles wait on other CTAs' first-GEMM tiles; under overlap = 2 the cap
+    splits the GPU between expert forward 0 and dispatch 1, whose blocks then
+    take several token tiles each. Same bits as uncapped."""
     d, inps, bufs = make_pair(**SMALL)
     run(d, bufs, overlap=False, defer=False)
     ref = [collect(b, i) for b, i in zip(bufs, inps)]
     for b in bufs:
         for n in ("y", "dx", "dw1", "dw2", "dw_r", "a", "h", "o", "da", "d_o", "dx_perm"):
             getattr(b, n).zero_()
-    run(d, bufs, overlap=True, defer=True, gemm_sms=gemm_sms)
+    run(d, bufs, overlap=overlap, defer=True, gemm_sms=gemm_sms)
     got = [collect(b, i) for b, i in zip(bufs, inps)]
     for m in range(2):
         for key in ref[m]:
-            assert np.array_equal(got[m][key], ref[m][key]), (gemm_sms, m, key)
+            assert np.array_equal(got[m][key], ref[m][key]), (overlap, gemm_sms, m, key)
