@@ -421,6 +421,8 @@ class Scheduler:
         self._h = h
 
     def step(self, mb0: LayerBuffers, mb1: LayerBuffers, overlap, defer_wgrad: bool):
+        """overlap: 0 (or False) serial, 1 (or True) overlapped, 2 dispatch-only
+        overlap (moe_sched_step in include/moe.h)."""
         arr = (MbBufs * 2)(mb0.struct(), mb1.struct())
         _check(lib().moe_sched_step(self._h, arr, int(overlap), int(defer_wgrad)), "moe_sched_step")
 
