@@ -34,8 +34,12 @@ __device__ __forceinline__ void unpack8_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
-__device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
-  return v1 > v2 || (v1 == v2 && e1 < e2);
+// An unsigned key in the order of the fp32 values (larger value, larger key),
+// -0 mapped to +0 so that the two tie as they compare; every key of a value is
+// above 0, which marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
 // Top-k (or the forced set), softmax over all E and renormalised gates of one
@@ -70,31 +74,36 @@ __device__ __forceinline__ void topk_row(const float* zt, int t, int32_t* __rest
       my_p = expf(zt[my_e] - m) / s;
     }
   } else {
+    // k rounds of a warp argmax: the largest value among the experts not yet
+    // taken, ties (equal values; -0 equals +0) to the lower expert index. A
+    // round is two warp reductions: the largest key, then the lowest expert
+    // among the lanes holding it (each lane offers its own best, the first of
+    // its equal keys being its lowest expert).
+    uint32_t key[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) key[i] = lane + 32 * i < E ? order_key(v[i]) : 0u;
     uint32_t taken = 0;
     for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+      uint32_t lk = 0u;
+      int li = 0;
+      float lv = 0.f;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (be == 0x7fffffff || better(v[i], e, bv, be))) {
-          bv = v[i];
-          be = e;
+        const uint32_t ki = ((taken >> i) & 1u) ? 0u : key[i];
+        if (ki > lk) {
+          lk = ki;
+          li = i;
+          lv = v[i];
         }
       }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (oe != 0x7fffffff && (be == 0x7fffffff || better(ov, oe, bv, be))) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if (be != 0x7fffffff && (be & 31) == lane) taken |= 1u << (be >> 5);
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, lk);
+      const uint32_t be =
+          __reduce_min_sync(0xffffffffu, lk == mk && mk != 0u ? (uint32_t)(lane + 32 * li) : ~0u);
+      const float bv = __shfl_sync(0xffffffffu, lv, (int)(be & 31u));
+      if (be != ~0u && (int)(be & 31u) == lane) taken |= 1u << (be >> 5);
       if (lane == j) {
-        my_e = be;
-        my_p = expf(bv - m) / s;
+        my_e = be != ~0u ? (int)be : -1;
+        my_p = be != ~0u ? expf(bv - m) / s : 0.f;
       }
     }
   }
